@@ -1,0 +1,198 @@
+/*
+ * ck.h -- C ABI of libck: training passes of a leaky-tanh recurrence over a
+ * fixed sparse directed graph, for one NVIDIA GB300 (sm_103a).
+ *
+ * The method (connectome-kernels page, intro): every node i holds one scalar
+ * state per batch column; one microstep computes
+ *     proposal_i = tanh( sum_j W_ij h_j + drive_i + bias_i )
+ *     h_i       <- (1 - leak_i) h_i + leak_i * proposal_i
+ * and `microsteps` microsteps run per input step.  W is sparse with a fixed
+ * pattern and one trainable scalar per (src, dst) edge; the drive enters only
+ * at a designated set of input nodes.  Readings this library takes where the
+ * page leaves a step open:
+ *   - an edge src[e] -> dst[e] carries W[dst][src] = edge_values[e]; repeated
+ *     (src, dst) pairs add up; self-loops are allowed;
+ *   - all nodes of a microstep read the state left by the previous microstep;
+ *   - the drive of input step t is added in each of its microsteps;
+ *   - the output of input step t is the state after its last microstep;
+ *   - leak is used exactly as passed (the caller squashes it, e.g. sigmoid).
+ *
+ * Conventions for every call below:
+ *   - Pointers marked (device) are CUDA device pointers on the current device;
+ *     arrays are dense, row-major, with the shapes given.  Nothing is retained
+ *     after a call returns except by ck_graph_create.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work on it and return without waiting, except
+ *     where a call says it synchronises.
+ *   - Every call returns a ck_status; none aborts the process or throws.  On
+ *     failure ck_last_error_message() gives a one-line reason (per thread).
+ *   - There is no CPU fallback: without a usable CUDA device, calls fail with
+ *     CK_ERR_CUDA.
+ *   - Memory: the library allocates device memory only inside
+ *     ck_graph_create (the graph arrays, freed by ck_graph_destroy) and
+ *     temporarily during that call.  The caller owns and allocates `saved` and
+ *     `scratch`, sized by ck_workspace_size.
+ */
+#ifndef CK_H
+#define CK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CK_OK = 0,
+    CK_ERR_INVALID_ARG = 1,    /* bad size, null pointer, index out of range, duplicate input node */
+    CK_ERR_CUDA = 2,           /* a CUDA runtime call failed (message names it) */
+    CK_ERR_OUT_OF_MEMORY = 3,  /* device allocation failed inside ck_graph_create */
+    CK_ERR_TIMEOUT = 4,        /* a bounded device-side wait gave up (see ck_query_status) */
+    CK_ERR_WORKSPACE = 5,      /* saved or scratch smaller than ck_workspace_size asks */
+    CK_ERR_INTERNAL = 6,       /* an internal invariant failed */
+    CK_ERR_UNSUPPORTED = 7     /* shape outside what this build supports (message says which) */
+} ck_status;
+
+/* Opaque graph handle; owned by the library. */
+typedef struct ck_graph ck_graph;
+
+/*
+ * ck_graph_create -- build the graph once (connectome-kernels page, "Use":
+ * SparseGraph(src, dst, num_nodes, input_nodes); "Design notes": a transposed
+ * compressed-row copy serves the state gradient; "Use": edge parameters stay in
+ * the caller's order and the internal permutation is invisible).
+ *
+ *   src, dst      (device) int64[E]; edge e runs src[e] -> dst[e]; 0 <= src, dst < N
+ *   E             number of edges, 0 <= E < 2^31
+ *   N             number of nodes, 1 <= N < 2^31
+ *   input_nodes   (device) int64[n_in]; distinct node ids; drive row k enters
+ *                 node input_nodes[k]; may be NULL when n_in == 0
+ *   n_in          0 <= n_in <= N
+ *   out           (host) receives the new handle; set to NULL on failure
+ *
+ * Builds on the GPU, with the library's own kernels, the rows keyed by dst
+ * (row_ptr[N+1], col = src in row order, perm = caller's edge id of each row
+ * position) and the same keyed by src (rowT_ptr, colT = dst, permT), both by a
+ * stable sort (equal keys keep ascending edge id), and slot[N] (k where
+ * input_nodes[k] = i, else -1).  Validates every index and input-node
+ * uniqueness on the device; synchronises `stream` to read the verdict.
+ * Errors: CK_ERR_INVALID_ARG (sizes, null pointers, an index out of range, a
+ * repeated input node), CK_ERR_OUT_OF_MEMORY, CK_ERR_CUDA.
+ */
+ck_status ck_graph_create(const int64_t *src, const int64_t *dst, int64_t E, int64_t N,
+                          const int64_t *input_nodes, int64_t n_in, void *stream,
+                          ck_graph **out);
+
+/* Frees the handle and its device arrays (synchronises the device first).  NULL is a no-op. */
+ck_status ck_graph_destroy(ck_graph *g);
+
+/* Sizes recorded in the handle (any output pointer may be NULL). */
+ck_status ck_graph_info(const ck_graph *g, int64_t *N, int64_t *E, int64_t *n_in);
+
+/*
+ * ck_graph_export -- copy the graph arrays out, for tests: (device) int32
+ * row_ptr[N+1], col[E], perm[E], rowT_ptr[N+1], colT[E], permT[E], slot[N].
+ * Any pointer may be NULL to skip that array.  Asynchronous on `stream`.
+ */
+ck_status ck_graph_export(const ck_graph *g, int32_t *row_ptr, int32_t *col, int32_t *perm,
+                          int32_t *rowT_ptr, int32_t *colT, int32_t *permT, int32_t *slot,
+                          void *stream);
+
+/*
+ * ck_workspace_size -- bytes of the two caller-owned buffers for batch B,
+ * T input steps and `microsteps` microsteps per step, on the current device.
+ *   saved_bytes    activations kept from ck_forward for ck_backward: the state
+ *                  and pre-activation after every microstep plus the initial
+ *                  state (connectome-kernels page, "Design notes": 2 x T x M x
+ *                  N x B floats saved), rows padded to a multiple of 8 floats
+ *   scratch_bytes  temporary device memory for one ck_forward or ck_backward
+ *                  call; one scratch buffer may serve both, but two calls that
+ *                  run at the same time need two buffers
+ * Both depend on the device's SM count: query on the device that will run the calls.
+ * Errors: CK_ERR_INVALID_ARG (B, T, microsteps < 1), CK_ERR_UNSUPPORTED (B > 512,
+ * or sizes whose element offsets overflow the index types).
+ */
+ck_status ck_workspace_size(const ck_graph *g, int64_t B, int64_t T, int64_t microsteps,
+                            size_t *saved_bytes, size_t *scratch_bytes);
+
+/*
+ * ck_forward -- run the whole window of T input steps x microsteps
+ * (connectome-kernels page, intro equations; "Use": sparse_recurrence returns
+ * out[T, B, N], the node states after each input step).
+ *
+ *   edge_values  (device) float[E], the caller's edge order
+ *   leak, bias   (device) float[N]
+ *   drives       (device) float[T][n_in][B]; may be NULL when n_in == 0
+ *   state0       (device) float[B][N]
+ *   states_out   (device) float[T][B][N], overwritten
+ *   saved        (device) >= saved_bytes, 16-byte aligned; filled for ck_backward
+ *   scratch      (device) >= scratch_bytes, 16-byte aligned
+ * Runs as one persistent cooperative kernel with bounded grid-wide barriers
+ * between microsteps.  Asynchronous.  A device-side wait that times out makes
+ * the kernel stop early and is reported by ck_query_status.
+ * Errors: CK_ERR_INVALID_ARG, CK_ERR_WORKSPACE, CK_ERR_UNSUPPORTED, CK_ERR_CUDA.
+ */
+ck_status ck_forward(const ck_graph *g, const float *edge_values, const float *leak,
+                     const float *bias, const float *drives, const float *state0,
+                     int64_t B, int64_t T, int64_t microsteps, float *states_out,
+                     void *saved, size_t saved_bytes, void *scratch, size_t scratch_bytes,
+                     void *stream);
+
+/*
+ * ck_backward -- gradients of L = sum_t <d_states[t], states_out[t]> with
+ * respect to all five inputs of ck_forward (connectome-kernels page, intro:
+ * three backward parts -- elementwise terms with per-node reductions, the
+ * transposed sparse product for the state gradient, a per-edge dot product
+ * over the batch for the edge gradient; "Use": differentiable in every
+ * argument).
+ *
+ *   edge_values, leak   the same values given to ck_forward
+ *   saved               (device) as filled by ck_forward with the same g, B, T, microsteps
+ *   d_states            (device) float[T][B][N]
+ *   d_edge_values       (device) float[E], caller's edge order, overwritten
+ *   d_leak, d_bias      (device) float[N], overwritten
+ *   d_drives            (device) float[T][n_in][B], overwritten; may be NULL when n_in == 0
+ *   d_state0            (device) float[B][N], overwritten
+ *   scratch             (device) >= scratch_bytes
+ * Gradients are written, not accumulated into.  Asynchronous.
+ * Errors: as ck_forward.
+ */
+ck_status ck_backward(const ck_graph *g, const float *edge_values, const float *leak,
+                      int64_t B, int64_t T, int64_t microsteps,
+                      const void *saved, size_t saved_bytes, const float *d_states,
+                      float *d_edge_values, float *d_leak, float *d_bias, float *d_drives,
+                      float *d_state0, void *scratch, size_t scratch_bytes, void *stream);
+
+/*
+ * ck_query_status -- synchronise `stream` and report whether the last
+ * ck_forward / ck_backward that used `scratch` finished every device-side wait:
+ * CK_OK, or CK_ERR_TIMEOUT if a bounded wait gave up (its kernel then stopped
+ * early and its outputs are not valid).  Also reports pending CUDA errors.
+ */
+ck_status ck_query_status(const void *scratch, void *stream);
+
+/* Tuning and test switches, process-wide; take effect on the next call. */
+typedef enum {
+    CK_OPT_PERSISTENT = 0,          /* 1 (default): one launch per call; 0: one launch per microstep */
+    CK_OPT_BARRIER_TIMEOUT_NS = 1,  /* bound on any device-side wait (default 4e9 ns) */
+    CK_OPT_TEST_BARRIER_EXTRA = 2,  /* test hook: barriers wait for this many extra arrivals
+                                       that never come, so every wait runs out (default 0) */
+    CK_OPT_GRAPH_IN_SMEM = 3,       /* 1 (default): keep each CTA's slice of the graph in
+                                       shared memory when it fits; 0: always stream it */
+    CK_OPT_THREADS = 4              /* threads per CTA: 512 (default) or 1024 */
+} ck_option;
+
+ck_status ck_set_option(ck_option opt, int64_t value);
+int64_t ck_get_option(ck_option opt);
+
+/* Number of kernel launches the last ck_forward / ck_backward on this thread enqueued. */
+int64_t ck_last_launch_count(void);
+
+const char *ck_status_string(ck_status s);
+const char *ck_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CK_H */

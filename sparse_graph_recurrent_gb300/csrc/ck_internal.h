@@ -1,0 +1,84 @@
+// Internal declarations shared by the translation units of libck.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ck.h"
+
+struct ck_graph {
+    int device;
+    int num_sms;
+    int64_t N, E, n_in;
+    int *row_ptr, *col, *perm;     // rows keyed by dst: col = src
+    int *rowT_ptr, *colT, *permT;  // rows keyed by src: colT = dst
+    int *slot;                     // slot[i] = k if input_nodes[k] == i, else -1
+};
+
+namespace ck {
+
+// Per-thread error reporting used by every ABI entry point.
+ck_status fail(ck_status s, const char *fmt, ...);
+ck_status cuda_fail(cudaError_t e, const char *what);
+
+// Graph build (graph.cu).  Fills g's device arrays; synchronises `stream`.
+ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
+                      const int64_t *input_nodes, cudaStream_t stream);
+
+// Device-side status words written by the recurrence kernels.
+enum : int { kDevOk = 0, kDevTimeout = 1, kDevInternal = 2 };
+
+// Launch description of one ck_forward / ck_backward call (recurrence.cu).
+struct Plan {
+    int N, E, n_in;
+    int B, Bp, LPE, EPW, NC, T, M, S;
+    int P;          // CTAs (one per SM)
+    int threads;    // threads per CTA
+    int warps;      // warps per CTA == sub-ranges per CTA
+    int cap;        // bound on edges in one CTA's range
+    bool smem_graph_fwd, smem_graph_bwd;
+    size_t smem_fwd, smem_bwd;
+    // scratch layout (byte offsets)
+    size_t off_ctrl, ctrl_bytes;
+    size_t off_carry;   // float [P][Bp]
+    size_t off_wperm;   // float [E]
+    size_t off_dwperm;  // float [E]
+    size_t off_G;       // float [N][Bp]
+    size_t off_da;      // float [2][N][Bp]
+    size_t scratch_bytes;
+    size_t saved_bytes; // float [(S+1) + S][N][Bp]
+};
+
+struct Options {
+    int persistent = 1;
+    long long timeout_ns = 4000000000LL;
+    int barrier_extra = 0;
+    int graph_in_smem = 1;
+    int threads = 512;
+};
+Options &options();
+
+ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p);
+
+struct FwdIO {
+    const float *w, *leak, *bias, *drives, *state0;
+    float *out;
+    float *saved;
+    void *scratch;
+};
+
+struct BwdIO {
+    const float *w, *leak;
+    const float *saved;
+    const float *dout;
+    float *dw, *dleak, *dbias, *ddrives, *dstate0;
+    void *scratch;
+};
+
+ck_status launch_forward(const ck_graph *g, const Plan &p, const FwdIO &io, cudaStream_t s,
+                         int64_t *launches);
+ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cudaStream_t s,
+                          int64_t *launches);
+
+}  // namespace ck

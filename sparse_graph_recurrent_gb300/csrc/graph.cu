@@ -1,0 +1,339 @@
+// Graph build on the GPU: validation, the input-slot map, and two stable sorts
+// of the edge list (by dst for the forward rows, by src for the transposed rows).
+//
+// connectome-kernels page, "Use": the graph is built once from int64 (src, dst)
+// lists on the GPU; edge parameters stay in the caller's order and the internal
+// compressed-row permutation is invisible.  "Design notes": the state gradient
+// runs over a precomputed transposed copy.
+//
+// The sort is a least-significant-digit radix sort with 8-bit digits.  Each
+// pass is a counting sort over tiles of 4096 keys: a per-tile digit histogram,
+// an exclusive scan of the histograms in (digit, tile) order, and a scatter in
+// which every key's rank among equal digits of its tile comes from warp match
+// masks taken in element order.  Every pass keeps equal keys in their previous
+// order, so the result lists each row's edges in ascending caller edge id.
+#include "ck_internal.h"
+
+namespace ck {
+namespace {
+
+constexpr int kTile = 4096;      // keys per CTA in a radix pass
+constexpr int kSortThreads = 256;
+constexpr int kScanThreads = 1024;
+constexpr int kScanItems = 4;    // per thread
+constexpr int kScanBlock = kScanThreads * kScanItems;
+
+enum : unsigned { kBadEdge = 1u, kBadInput = 2u, kDupInput = 4u };
+
+__global__ void k_validate(const int64_t *__restrict__ src, const int64_t *__restrict__ dst,
+                           int64_t E, int64_t N, int *__restrict__ key_dst,
+                           int *__restrict__ key_src, int *__restrict__ ids,
+                           int *__restrict__ ids2, unsigned *__restrict__ flags) {
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < E;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        int64_t s = src[e], d = dst[e];
+        if (s < 0 || s >= N || d < 0 || d >= N) {
+            atomicOr(flags, kBadEdge);
+            s = 0;
+            d = 0;
+        }
+        key_src[e] = (int)s;
+        key_dst[e] = (int)d;
+        ids[e] = (int)e;
+        ids2[e] = (int)e;
+    }
+}
+
+__global__ void k_slots(const int64_t *__restrict__ inp, int64_t n_in, int64_t N,
+                        int *__restrict__ slot, unsigned *__restrict__ flags) {
+    for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < n_in;
+         k += (int64_t)gridDim.x * blockDim.x) {
+        int64_t v = inp[k];
+        if (v < 0 || v >= N) {
+            atomicOr(flags, kBadInput);
+            continue;
+        }
+        if (atomicCAS(&slot[v], -1, (int)k) != -1) atomicOr(flags, kDupInput);
+    }
+}
+
+// Per-tile digit counts, stored digit-major: hist[digit * ntiles + tile].
+__global__ void __launch_bounds__(kSortThreads) k_radix_hist(const int *__restrict__ keys, int n,
+                                                             int shift, int *__restrict__ hist,
+                                                             int ntiles) {
+    __shared__ int h[256];
+    h[threadIdx.x] = 0;
+    __syncthreads();
+    const int base = blockIdx.x * kTile;
+    for (int i = threadIdx.x; i < kTile; i += kSortThreads) {
+        int idx = base + i;
+        if (idx < n) atomicAdd(&h[(keys[idx] >> shift) & 255], 1);
+    }
+    __syncthreads();
+    hist[threadIdx.x * ntiles + blockIdx.x] = h[threadIdx.x];
+}
+
+// Stable scatter of one tile: element order inside the tile decides ranks.
+__global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
+    const int *__restrict__ kin, const int *__restrict__ vin, int *__restrict__ kout,
+    int *__restrict__ vout, int n, int shift, const int *__restrict__ offs, int ntiles) {
+    constexpr int W = kSortThreads / 32;
+    __shared__ int run[256];
+    __shared__ int wcnt[W][256];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    run[tid] = offs[tid * ntiles + blockIdx.x];
+    const int base = blockIdx.x * kTile;
+    for (int c = 0; c < kTile; c += kSortThreads) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) wcnt[w][tid] = 0;
+        __syncthreads();
+        const int idx = base + c + tid;
+        const bool valid = idx < n;
+        int key = 0, val = 0, digit = -1;
+        if (valid) {
+            key = kin[idx];
+            val = vin[idx];
+            digit = (key >> shift) & 255;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, digit);
+        const int rank = __popc(peers & lt);
+        if (valid && (__ffs(peers) - 1) == lane) wcnt[warp][digit] = __popc(peers);
+        __syncthreads();
+        {
+            int r = run[tid];
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                int cnt = wcnt[w][tid];
+                wcnt[w][tid] = r;
+                r += cnt;
+            }
+            run[tid] = r;
+        }
+        __syncthreads();
+        if (valid) {
+            const int pos = wcnt[warp][digit] + rank;
+            kout[pos] = key;
+            vout[pos] = val;
+        }
+        __syncthreads();
+    }
+}
+
+// Exclusive scan, three kernels: per-block scan + block totals, scan of the
+// totals (recursively), add the scanned totals back.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int s = (lane < (int)(blockDim.x >> 5)) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;  // inclusive
+    }
+    __syncthreads();
+    const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+    if (total && threadIdx.x == blockDim.x - 1) *total = before + v;
+    return before;
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_scan_block(const int *__restrict__ in,
+                                                             int *__restrict__ out, int n,
+                                                             int *__restrict__ block_sums) {
+    __shared__ int warp_sums[32];
+    __shared__ int tot;
+    const int base = blockIdx.x * kScanBlock + threadIdx.x * kScanItems;
+    int v[kScanItems];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+        v[i] = (base + i < n) ? in[base + i] : 0;
+        sum += v[i];
+    }
+    int run = block_exclusive_scan(sum, warp_sums, &tot);
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+        if (base + i < n) out[base + i] = run;
+        run += v[i];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) block_sums[blockIdx.x] = tot;
+}
+
+__global__ void k_scan_add(int *__restrict__ out, int n, const int *__restrict__ block_offs) {
+    const int b = blockIdx.x;
+    const int add = block_offs[b];
+    const int base = b * kScanBlock;
+    for (int i = threadIdx.x; i < kScanBlock; i += blockDim.x)
+        if (base + i < n) out[base + i] += add;
+}
+
+// In-place safe: each block reads its inputs before any block's output is added to.
+cudaError_t exclusive_scan(const int *in, int *out, int n, int *tmp, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int nb = (n + kScanBlock - 1) / kScanBlock;
+    int *sums = tmp;
+    int *sums_scanned = tmp + nb;
+    k_scan_block<<<nb, kScanThreads, 0, s>>>(in, out, n, sums);
+    if (nb > 1) {
+        cudaError_t e = exclusive_scan(sums, sums_scanned, nb, tmp + 2 * nb, s);
+        if (e != cudaSuccess) return e;
+        k_scan_add<<<nb, kScanThreads, 0, s>>>(out, n, sums_scanned);
+    }
+    return cudaGetLastError();
+}
+
+size_t scan_tmp_ints(int n) {
+    size_t t = 0;
+    while (n > 0) {
+        int nb = (n + kScanBlock - 1) / kScanBlock;
+        t += 2 * (size_t)nb;
+        if (nb <= 1) break;
+        n = nb;
+    }
+    return t + 2;
+}
+
+// row_ptr[i] = first position whose key >= i, for i in [0, N].
+__global__ void k_row_ptr(const int *__restrict__ sorted_keys, int E, int N,
+                          int *__restrict__ row_ptr) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= N; i += gridDim.x * blockDim.x) {
+        int lo = 0, hi = E;
+        while (lo < hi) {
+            int mid = (lo + hi) >> 1;
+            if (sorted_keys[mid] < i) lo = mid + 1;
+            else hi = mid;
+        }
+        row_ptr[i] = lo;
+    }
+}
+
+__global__ void k_gather_other(const int64_t *__restrict__ other, const int *__restrict__ perm,
+                               int E, int *__restrict__ col) {
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < E; k += gridDim.x * blockDim.x)
+        col[k] = (int)other[perm[k]];
+}
+
+struct DevBuf {
+    void *p = nullptr;
+    ~DevBuf() {
+        if (p) cudaFree(p);
+    }
+};
+
+// Stable sort of (keys, vals) by key; *in_b tells which pair holds the result.
+cudaError_t radix_sort(int *ka, int *va, int *kb, int *vb, int n, int key_bits, int *hist,
+                       int *scan_tmp, cudaStream_t s, bool *in_b) {
+    const int ntiles = (n + kTile - 1) / kTile;
+    *in_b = false;
+    for (int shift = 0; shift < key_bits; shift += 8) {
+        k_radix_hist<<<ntiles, kSortThreads, 0, s>>>(ka, n, shift, hist, ntiles);
+        cudaError_t e = exclusive_scan(hist, hist, 256 * ntiles, scan_tmp, s);
+        if (e != cudaSuccess) return e;
+        k_radix_scatter<<<ntiles, kSortThreads, 0, s>>>(ka, va, kb, vb, n, shift, hist, ntiles);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        int *t = ka; ka = kb; kb = t;
+        t = va; va = vb; vb = t;
+        *in_b = !*in_b;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
+                      const int64_t *input_nodes, cudaStream_t s) {
+    const int N = (int)g->N, E = (int)g->E, n_in = (int)g->n_in;
+    cudaError_t e;
+#define CK_TRY(call, what)                                                              \
+    do {                                                                                \
+        e = (call);                                                                     \
+        if (e != cudaSuccess)                                                           \
+            return (e == cudaErrorMemoryAllocation)                                     \
+                       ? fail(CK_ERR_OUT_OF_MEMORY, "%s: %s", what, cudaGetErrorString(e)) \
+                       : cuda_fail(e, what);                                            \
+    } while (0)
+
+    const size_t E1 = (size_t)(E > 0 ? E : 1);
+    CK_TRY(cudaMalloc((void **)&g->row_ptr, sizeof(int) * (N + 1)), "cudaMalloc row_ptr");
+    CK_TRY(cudaMalloc((void **)&g->rowT_ptr, sizeof(int) * (N + 1)), "cudaMalloc rowT_ptr");
+    CK_TRY(cudaMalloc((void **)&g->slot, sizeof(int) * N), "cudaMalloc slot");
+    CK_TRY(cudaMalloc((void **)&g->col, sizeof(int) * E1), "cudaMalloc col");
+    CK_TRY(cudaMalloc((void **)&g->perm, sizeof(int) * E1), "cudaMalloc perm");
+    CK_TRY(cudaMalloc((void **)&g->colT, sizeof(int) * E1), "cudaMalloc colT");
+    CK_TRY(cudaMalloc((void **)&g->permT, sizeof(int) * E1), "cudaMalloc permT");
+
+    const int ntiles = (E + kTile - 1) / kTile;
+    const size_t n_hist = 256 * (size_t)(ntiles > 0 ? ntiles : 1);
+    const size_t n_tmp = scan_tmp_ints((int)n_hist);
+    // key_dst, key_src, ids, ids2, kb, vb; histograms; scan temp; flags
+    const size_t ints = 6 * E1 + n_hist + n_tmp + 4;
+    DevBuf tmp;
+    CK_TRY(cudaMalloc(&tmp.p, ints * sizeof(int)), "cudaMalloc build temp");
+    int *key_dst = (int *)tmp.p;
+    int *key_src = key_dst + E1;
+    int *ids = key_src + E1;
+    int *ids2 = ids + E1;
+    int *kb = ids2 + E1;
+    int *vb = kb + E1;
+    int *hist = vb + E1;
+    int *scan_tmp = hist + n_hist;
+    unsigned *flags = (unsigned *)(scan_tmp + n_tmp);
+
+    CK_TRY(cudaMemsetAsync(flags, 0, sizeof(unsigned), s), "cudaMemsetAsync flags");
+    CK_TRY(cudaMemsetAsync(g->slot, 0xff, sizeof(int) * N, s), "cudaMemsetAsync slot");
+    const int blocks = g->num_sms * 4;
+    if (E > 0)
+        k_validate<<<blocks, 256, 0, s>>>(src, dst, E, N, key_dst, key_src, ids, ids2, flags);
+    if (n_in > 0) k_slots<<<blocks, 256, 0, s>>>(input_nodes, n_in, N, g->slot, flags);
+    CK_TRY(cudaGetLastError(), "validate launch");
+    unsigned hflags = 0;
+    CK_TRY(cudaMemcpyAsync(&hflags, flags, sizeof(unsigned), cudaMemcpyDeviceToHost, s),
+           "cudaMemcpyAsync flags");
+    CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (validation)");
+    if (hflags & kBadEdge) return fail(CK_ERR_INVALID_ARG, "an edge endpoint is outside [0, N)");
+    if (hflags & kBadInput) return fail(CK_ERR_INVALID_ARG, "an input node is outside [0, N)");
+    if (hflags & kDupInput) return fail(CK_ERR_INVALID_ARG, "input_nodes repeats a node");
+
+    int key_bits = 0;  // keys are < N
+    while (key_bits < 31 && ((int64_t)1 << key_bits) < (int64_t)N) ++key_bits;
+    struct Side {
+        int *keys, *vals, *row_ptr, *col, *perm;
+        const int64_t *other;
+    } sides[2] = {{key_dst, ids, g->row_ptr, g->col, g->perm, src},
+                  {key_src, ids2, g->rowT_ptr, g->colT, g->permT, dst}};
+    for (auto &sd : sides) {
+        int *ks = sd.keys, *vs = sd.vals;
+        if (E > 0) {
+            bool in_b = false;
+            CK_TRY(radix_sort(sd.keys, sd.vals, kb, vb, E, key_bits, hist, scan_tmp, s, &in_b),
+                   "radix sort");
+            if (in_b) {
+                ks = kb;
+                vs = vb;
+            }
+            CK_TRY(cudaMemcpyAsync(sd.perm, vs, sizeof(int) * E, cudaMemcpyDeviceToDevice, s),
+                   "copy perm");
+            k_gather_other<<<blocks, 256, 0, s>>>(sd.other, sd.perm, E, sd.col);
+        }
+        k_row_ptr<<<(N + 256) / 256, 256, 0, s>>>(ks, E, N, sd.row_ptr);
+        CK_TRY(cudaGetLastError(), "row_ptr launch");
+        // the second side reuses kb/vb; stream order already serialises it
+    }
+    CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (graph build)");
+#undef CK_TRY
+    return CK_OK;
+}
+
+}  // namespace ck
