@@ -1,0 +1,129 @@
+"""sparse_graph_recurrent_gb300 -- a leaky-tanh recurrence over a fixed sparse
+directed graph, trained with hand-written CUDA kernels for one GB300 (sm_103a).
+
+Python surface (connectome-kernels page, "Use"):
+
+    graph = SparseGraph(src, dst, num_nodes=N, input_nodes=input_nodes)
+    out = sparse_recurrence(edge_values, leak, bias, drives, state0, graph, microsteps=2)
+    # out: [T, B, N] node states after each input step; differentiable in
+    # edge_values, leak, bias, drives [T, n_in, B] and state0 [B, N]
+
+Everything runs in libck (include/ck.h); this package only marshals arguments.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _ck
+from ._ck import CKError  # noqa: F401
+
+__all__ = ["SparseGraph", "sparse_recurrence", "CKError", "forward", "backward"]
+
+
+class SparseGraph:
+    """A fixed directed graph src[e] -> dst[e] with designated input nodes.
+
+    Built once on the GPU by ck_graph_create; edge parameters stay in the
+    caller's edge order.
+    """
+
+    def __init__(self, src, dst, num_nodes: int, input_nodes):
+        if src.shape != dst.shape or src.dim() != 1:
+            raise ValueError("src and dst must be 1-D and of equal length")
+        self.device = src.device
+        self.num_nodes = int(num_nodes)
+        self.num_edges = int(src.numel())
+        self.num_inputs = int(input_nodes.numel())
+        with torch.cuda.device(self.device):
+            self._h = _ck.ck_graph_create(src.contiguous(), dst.contiguous(), self.num_nodes,
+                                          input_nodes.contiguous())
+        self._ws = {}
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            try:
+                _ck.ck_graph_destroy(h)
+            except Exception:
+                pass
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def export(self):
+        with torch.cuda.device(self.device):
+            return _ck.ck_graph_export(self._h, self.device)
+
+    def workspace_size(self, B: int, T: int, microsteps: int):
+        return _ck.ck_workspace_size(self._h, B, T, microsteps)
+
+    def scratch(self, B: int, T: int, microsteps: int):
+        """A cached scratch buffer for (B, T, microsteps) on this graph's device."""
+        key = (B, T, microsteps)
+        buf = self._ws.get(key)
+        if buf is None:
+            _, nbytes = self.workspace_size(B, T, microsteps)
+            buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            self._ws = {key: buf}
+        return buf
+
+
+def forward(graph: SparseGraph, edge_values, leak, bias, drives, state0, microsteps: int):
+    """Raw forward: returns (out [T,B,N], saved buffer, scratch buffer)."""
+    B, N = state0.shape
+    T = drives.shape[0]
+    saved_b, _ = graph.workspace_size(B, T, microsteps)
+    saved = torch.empty(saved_b, dtype=torch.uint8, device=state0.device)
+    scratch = graph.scratch(B, T, microsteps)
+    out = torch.empty((T, B, N), dtype=torch.float32, device=state0.device)
+    _ck.ck_forward(graph.handle, edge_values, leak, bias, drives, state0, microsteps, out,
+                   saved, scratch)
+    return out, saved, scratch
+
+
+def backward(graph: SparseGraph, edge_values, leak, B: int, T: int, microsteps: int, saved,
+             d_out, scratch=None):
+    """Raw backward: returns (d_edge_values, d_leak, d_bias, d_drives, d_state0)."""
+    dev = d_out.device
+    N, E, n_in = graph.num_nodes, graph.num_edges, graph.num_inputs
+    if scratch is None:
+        scratch = graph.scratch(B, T, microsteps)
+    dw = torch.empty(E, dtype=torch.float32, device=dev)
+    dl = torch.empty(N, dtype=torch.float32, device=dev)
+    db = torch.empty(N, dtype=torch.float32, device=dev)
+    dd = torch.empty((T, n_in, B), dtype=torch.float32, device=dev)
+    dh = torch.empty((B, N), dtype=torch.float32, device=dev)
+    _ck.ck_backward(graph.handle, edge_values, leak, B, T, microsteps, saved, d_out.contiguous(),
+                    dw, dl, db, dd, dh, scratch)
+    return dw, dl, db, dd, dh
+
+
+class _SparseRecurrence(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, edge_values, leak, bias, drives, state0, graph, microsteps):
+        ev = edge_values.detach().contiguous()
+        lk = leak.detach().contiguous()
+        out, saved, _ = forward(graph, ev, lk, bias.detach().contiguous(),
+                                drives.detach().contiguous(), state0.detach().contiguous(),
+                                microsteps)
+        ctx.graph, ctx.microsteps = graph, microsteps
+        ctx.shape = (state0.shape[0], drives.shape[0])
+        ctx.saved_buf = saved
+        ctx.save_for_backward(ev, lk)
+        return out
+
+    @staticmethod
+    def backward(ctx, d_out):
+        ev, lk = ctx.saved_tensors
+        B, T = ctx.shape
+        grads = backward(ctx.graph, ev, lk, B, T, ctx.microsteps, ctx.saved_buf, d_out)
+        ctx.saved_buf = None
+        return (*grads, None, None)
+
+
+def sparse_recurrence(edge_values, leak, bias, drives, state0, graph: SparseGraph,
+                      microsteps: int = 1):
+    """out[T, B, N]: node states after each of the T input steps."""
+    return _SparseRecurrence.apply(edge_values, leak, bias, drives, state0, graph, microsteps)

@@ -1,0 +1,179 @@
+"""ctypes binding of libck's C ABI (include/ck.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and takes torch
+CUDA tensors in place of raw device pointers.  All computation happens in the
+library's CUDA kernels; if the library cannot be built or loaded this module
+raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+CK_OK = 0
+STATUS = {0: "CK_OK", 1: "CK_ERR_INVALID_ARG", 2: "CK_ERR_CUDA", 3: "CK_ERR_OUT_OF_MEMORY",
+          4: "CK_ERR_TIMEOUT", 5: "CK_ERR_WORKSPACE", 6: "CK_ERR_INTERNAL",
+          7: "CK_ERR_UNSUPPORTED"}
+OPT_PERSISTENT, OPT_BARRIER_TIMEOUT_NS, OPT_TEST_BARRIER_EXTRA, OPT_GRAPH_IN_SMEM, OPT_THREADS = range(5)
+
+_lib = None
+
+
+class CKError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libck.so, building it with nvcc first if it is missing or stale."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.build()
+    if not os.path.exists(path):
+        raise ImportError(f"libck.so not found at {path}")
+    lib = ctypes.CDLL(path)
+    p, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    psz = ctypes.POINTER(ctypes.c_size_t)
+    pi64 = ctypes.POINTER(ctypes.c_int64)
+    sig = {
+        "ck_graph_create": [p, p, i64, i64, p, i64, p, ctypes.POINTER(p)],
+        "ck_graph_destroy": [p],
+        "ck_graph_info": [p, pi64, pi64, pi64],
+        "ck_graph_export": [p, p, p, p, p, p, p, p, p],
+        "ck_workspace_size": [p, i64, i64, i64, psz, psz],
+        "ck_forward": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p, sz, p],
+        "ck_backward": [p, p, p, i64, i64, i64, p, sz, p, p, p, p, p, p, p, sz, p],
+        "ck_query_status": [p, p],
+        "ck_set_option": [ctypes.c_int, i64],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.ck_get_option.argtypes = [ctypes.c_int]
+    lib.ck_get_option.restype = i64
+    lib.ck_last_launch_count.argtypes = []
+    lib.ck_last_launch_count.restype = i64
+    lib.ck_status_string.argtypes = [ctypes.c_int]
+    lib.ck_status_string.restype = ctypes.c_char_p
+    lib.ck_last_error_message.argtypes = []
+    lib.ck_last_error_message.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != CK_OK:
+        raise CKError(status, load().ck_last_error_message().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name):
+    if t is None:
+        return
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def ck_graph_create(src, dst, num_nodes: int, input_nodes, stream=None):
+    for t, n in ((src, "src"), (dst, "dst"), (input_nodes, "input_nodes")):
+        _need(t, torch.int64, n)
+    h = ctypes.c_void_p()
+    n_in = 0 if input_nodes is None else input_nodes.numel()
+    _check(load().ck_graph_create(_ptr(src), _ptr(dst), src.numel(), num_nodes,
+                                  _ptr(input_nodes) if n_in else None, n_in, _stream(stream),
+                                  ctypes.byref(h)))
+    return h
+
+
+def ck_graph_destroy(handle):
+    _check(load().ck_graph_destroy(handle))
+
+
+def ck_graph_info(handle):
+    n, e, k = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(load().ck_graph_info(handle, ctypes.byref(n), ctypes.byref(e), ctypes.byref(k)))
+    return n.value, e.value, k.value
+
+
+def ck_graph_export(handle, device=None, stream=None):
+    N, E, _ = ck_graph_info(handle)
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    mk = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
+    out = dict(row_ptr=mk(N + 1), col=mk(E), perm=mk(E), rowT_ptr=mk(N + 1), colT=mk(E),
+               permT=mk(E), slot=mk(N))
+    _check(load().ck_graph_export(handle, *(_ptr(out[k]) for k in
+                                            ("row_ptr", "col", "perm", "rowT_ptr", "colT",
+                                             "permT", "slot")), _stream(stream)))
+    return out
+
+
+def ck_workspace_size(handle, B: int, T: int, microsteps: int):
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().ck_workspace_size(handle, B, T, microsteps, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def ck_forward(handle, edge_values, leak, bias, drives, state0, microsteps, states_out,
+               saved, scratch, stream=None):
+    for t, n in ((edge_values, "edge_values"), (leak, "leak"), (bias, "bias"),
+                 (drives, "drives"), (state0, "state0"), (states_out, "states_out")):
+        _need(t, torch.float32, n)
+    B = state0.shape[0]
+    T = states_out.shape[0]
+    _check(load().ck_forward(handle, _ptr(edge_values), _ptr(leak), _ptr(bias),
+                             _ptr(drives) if drives is not None and drives.numel() else None,
+                             _ptr(state0), B, T, microsteps, _ptr(states_out),
+                             _ptr(saved), saved.numel() * saved.element_size(),
+                             _ptr(scratch), scratch.numel() * scratch.element_size(),
+                             _stream(stream)))
+
+
+def ck_backward(handle, edge_values, leak, B, T, microsteps, saved, d_states, d_edge_values,
+                d_leak, d_bias, d_drives, d_state0, scratch, stream=None):
+    for t, n in ((edge_values, "edge_values"), (leak, "leak"), (d_states, "d_states"),
+                 (d_edge_values, "d_edge_values"), (d_leak, "d_leak"), (d_bias, "d_bias"),
+                 (d_drives, "d_drives"), (d_state0, "d_state0")):
+        _need(t, torch.float32, n)
+    _check(load().ck_backward(handle, _ptr(edge_values), _ptr(leak), B, T, microsteps,
+                              _ptr(saved), saved.numel() * saved.element_size(),
+                              _ptr(d_states), _ptr(d_edge_values), _ptr(d_leak), _ptr(d_bias),
+                              _ptr(d_drives) if d_drives is not None and d_drives.numel() else None,
+                              _ptr(d_state0), _ptr(scratch),
+                              scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def ck_query_status(scratch, stream=None):
+    _check(load().ck_query_status(_ptr(scratch), _stream(stream)))
+
+
+def ck_set_option(opt: int, value: int):
+    _check(load().ck_set_option(opt, int(value)))
+
+
+def ck_get_option(opt: int) -> int:
+    return int(load().ck_get_option(opt))
+
+
+def ck_last_launch_count() -> int:
+    return int(load().ck_last_launch_count())
