@@ -1,0 +1,347 @@
+#!/usr/bin/env python
+"""Training steps/s (forward + backward) of the sparse-graph leaky-tanh
+recurrence on one GB300, for the FlyGPT launch shape (connectome-kernels page,
+"Why" table: N=5,000, E=524,324, B=32, T x microsteps = 64 x 2).
+
+One step = ck_forward + ck_backward over the whole window, inputs resident in
+HBM; the L2 is flushed (a 512 MB write) before every timed step and the flush
+is outside the timed events.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (under torchrun) every rank runs an independent replica of the
+same step (the method has no exchange between replicas): weak scaling.
+--impl reference times the CPU oracle (fp64, single thread) on one batch
+column per step, scaled to the whole batch.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "train steps/sec (fwd+bwd) at N=5k,E=524k,B=32,T=64×2; % of HBM/L2 roofline"
+PAGE_STEPS_PER_S = 1000.0 / 15.5  # the page's fused-kernel step time for this workload (B200)
+HBM_FALLBACK = 6800.0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK, "fallback"
+
+
+def byte_model(N, E, B, T, M, n_in):
+    """Algorithmic bytes per launch (every byte that must reach the SMs).
+
+    Forward microstep: graph 8E + 4(N+1), gathered source rows 4EB, own row
+    read plus state and pre-activation written 12NB, drives 4 n_in B.
+    Backward microstep: transposed graph 8E + 4(N+1), edge-gradient
+    read-modify-write 8E, gathered rows 4EB, own rows 16NB.
+    Per input step: the output write (forward) and dOut read (backward), 4NB each.
+    """
+    S = T * M
+    fwd = S * (8 * E + 4 * (N + 1) + 4 * E * B + 12 * N * B + 4 * n_in * B) + T * 4 * N * B
+    bwd = S * (8 * E + 4 * (N + 1) + 8 * E + 4 * E * B + 16 * N * B) + T * 4 * N * B
+    return fwd, bwd
+
+
+def hbm_bytes(N, E, B, T, M, n_in):
+    """Compulsory DRAM bytes per step when graph and state stay in L2: saved
+    activations written and read back, out, dOut, drives and their gradient,
+    state0 and its gradient, parameters and their gradients."""
+    S = T * M
+    saved = 2 * 4 * (2 * S + 1) * N * B
+    io = 4 * (2 * T * N * B + 2 * T * n_in * B + 2 * N * B + 2 * E + 4 * N)
+    return saved + io
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_sample(c, cols):
+    """Time the oracle (single thread) on some batch columns of the workload."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.run_case(c, batch_cols=cols)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, c, rank):
+    if rank != 0:
+        return
+    B = c["B"]
+    for _ in range(args.warmup):
+        cpu_oracle_sample(c, [0])
+    times = [cpu_oracle_sample(c, [k % B]) for k in range(args.steps)]
+    per_step = statistics.mean(times) * B
+    value = 1.0 / per_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / PAGE_STEPS_PER_S, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _workload_name(c), "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                         "sample": f"1 of {B} batch columns per step (full graph, T, M), "
+                                   f"time x{B}"},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _workload_name(c):
+    return f"flygpt N={c['N']} E={c['E']} B={c['B']} T={c['T']} M={c['M']}"
+
+
+def run_ours(args, c, rank, world, dist):
+    import torch
+
+    import sparse_graph_recurrent_gb300 as pkg
+    from sparse_graph_recurrent_gb300 import _ck
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tt = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    N, E, B, T, M, n_in = c["N"], c["E"], c["B"], c["T"], c["M"], c["n_in"]
+    g = pkg.SparseGraph(tt(c["src"]), tt(c["dst"]), N, tt(c["input_nodes"]))
+    w, leak, bias, drives, state0, dout = (tt(c[k]) for k in ("w", "leak", "bias", "drives",
+                                                              "state0", "dout"))
+    saved_b, scratch_b = g.workspace_size(B, T, M)
+    saved = torch.empty(saved_b, dtype=torch.uint8, device=dev)
+    scratch = torch.empty(scratch_b, dtype=torch.uint8, device=dev)
+    out = torch.empty((T, B, N), device=dev)
+    dw, dl, db = (torch.empty(n, device=dev) for n in (E, N, N))
+    dd = torch.empty((T, n_in, B), device=dev)
+    dh = torch.empty((B, N), device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    launches = [0]
+
+    def step():
+        _ck.ck_forward(g.handle, w, leak, bias, drives, state0, M, out, saved, scratch)
+        launches[0] += _ck.ck_last_launch_count()
+        _ck.ck_backward(g.handle, w, leak, B, T, M, saved, dout, dw, dl, db, dd, dh, scratch)
+        launches[0] += _ck.ck_last_launch_count()
+
+    for _ in range(args.warmup):
+        step()
+    _ck.ck_query_status(scratch)
+    torch.cuda.synchronize()
+
+    # L2 peaks in this run: dense read of a 64 MB buffer, and a gather of
+    # random 128-byte rows from a state-sized table (the forward's pattern)
+    sink = torch.zeros(1, device=dev)
+    buf = torch.ones(16 << 20, device=dev)
+    rows = torch.ones((N, 32), device=dev)
+    idx = torch.randint(0, N, (E,), dtype=torch.int32, device=dev)
+
+    def probe(fn, nbytes, reps=20):
+        fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return nbytes / (e0.elapsed_time(e1) / 1e3 / reps) / 1e9
+
+    l2_read = probe(lambda: _ck.ck_probe_read(buf, 10, sink), buf.numel() * 4 * 10)
+    l2_gather = probe(lambda: _ck.ck_probe_gather(rows, idx, sink), E * 128)
+
+    clocks = Clocks(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches[0] = 0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.fill_(k & 0xff)
+        ev[k][0].record(stream)
+        _ck.ck_forward(g.handle, w, leak, bias, drives, state0, M, out, saved, scratch)
+        launches[0] += _ck.ck_last_launch_count()
+        ev[k][1].record(stream)
+        _ck.ck_backward(g.handle, w, leak, B, T, M, saved, dout, dw, dl, db, dd, dh, scratch)
+        launches[0] += _ck.ck_last_launch_count()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    _ck.ck_query_status(scratch)
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c2) for _, b, c2 in ev]
+    total_ms = sum(a.elapsed_time(c2) for a, _, c2 in ev)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps / (total_ms / 1e3)
+
+    # end to end through the public API: host inputs in, host results out
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_in = {k: pin(c[k]) for k in ("w", "leak", "bias", "drives", "state0", "dout")}
+    h_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (out, dw, dl, db, dd, dh)]
+    h2d = sum(x.numel() * 4 for x in h_in.values())
+    d2h = sum(x.numel() * 4 for x in h_out)
+
+    def e2e_step():
+        d = {k: v.to(dev, non_blocking=True) for k, v in h_in.items()}
+        o, sv, sc = pkg.forward(g, d["w"], d["leak"], d["bias"], d["drives"], d["state0"], M)
+        grads = pkg.backward(g, d["w"], d["leak"], B, T, M, sv, d["dout"], sc)
+        for hdst, src in zip(h_out, (o, *grads)):
+            hdst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return
+    fb, bb = byte_model(N, E, B, T, M, n_in)
+    f_mean, b_mean = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    dom, dom_bytes, dom_ms = ("backward", bb, b_mean) if b_mean >= f_mean else ("forward", fb, f_mean)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    hbm_peak, hbm_src = _peaks()
+    q_hbm = hbm_bytes(N, E, B, T, M, n_in)
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": value / PAGE_STEPS_PER_S,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": _workload_name(c), "parallelism": "replicas",
+                   "l2": "flushed by a 512 MB write before every timed step (outside the events)"},
+        "roofline": {"bound": "l2", "kernel": dom, "achieved": achieved, "peak": l2_read,
+                     "unit": "GB/s", "frac": achieved / l2_read, "traffic": None,
+                     "peak_source": "measured in this run: dense 16-byte L2 reads of a 64 MB buffer"},
+        "roofline_hbm": {"bound": "hbm", "achieved": q_hbm / (ms_per_step / 1e3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": q_hbm / (ms_per_step / 1e3) / 1e9 / hbm_peak,
+                         "peak_source": f"{hbm_src} (MEASURED_PEAKS.json hbm_gbs)",
+                         "bytes_per_step": q_hbm},
+        "l2_probe": {"dense_read_gbs": l2_read, "row_gather_gbs": l2_gather},
+        "kernels": {"forward_ms": f_mean, "backward_ms": b_mean,
+                    "forward_gbs": fb / (f_mean / 1e3) / 1e9, "backward_gbs": bb / (b_mean / 1e3) / 1e9,
+                    "forward_bytes": fb, "backward_bytes": bb},
+        "e2e": {"value": world / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches[0],
+        "clocks": clk,
+        "samples_ms": [round(a + b, 4) for a, b in zip(fwd_ms, bwd_ms)],
+    }
+    if not args.no_cpu_baseline and world == 1:
+        cols = list(range(args.cpu_cols))
+        secs = cpu_oracle_sample(c, cols)
+        per_step = secs * B / len(cols)
+        line["cpu_baseline"] = {"value": 1.0 / per_step, "unit": "steps/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{len(cols)} of {B} batch columns, full graph and window "
+                                          f"({secs:.1f} s), scaled x{B / len(cols):g}"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-cols", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    import workloads
+    c = workloads.make(1)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, c, rank)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    run_ours(args, c, rank, world, dist)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -189,6 +189,22 @@ int64_t ck_get_option(ck_option opt);
 /* Number of kernel launches the last ck_forward / ck_backward on this thread enqueued. */
 int64_t ck_last_launch_count(void);
 
+/*
+ * Bandwidth probes (no counterpart on the pages: they measure the L2 rates
+ * that bound the recurrence kernels, which the device does not report).
+ *   ck_probe_read    reads `bytes` of (device) `buf` (16-byte aligned) `reps`
+ *                    times with 16-byte L2-cached loads.
+ *   ck_probe_gather  reads nidx whole rows rows[idx[k]][0:row_floats] of a
+ *                    (device) float[nrows][row_floats] table, row_floats in
+ *                    {8, 16, 32, 64, 128}; every idx[k] must lie in [0, nrows)
+ *                    (the kernel does not check it).
+ * `sink` is a (device) float[1] the kernels may write.  Asynchronous; time
+ * them with events on `stream`.
+ */
+ck_status ck_probe_read(const void *buf, size_t bytes, int64_t reps, float *sink, void *stream);
+ck_status ck_probe_gather(const float *rows, int64_t nrows, int64_t row_floats,
+                          const int32_t *idx, int64_t nidx, float *sink, void *stream);
+
 const char *ck_status_string(ck_status s);
 const char *ck_last_error_message(void);
 

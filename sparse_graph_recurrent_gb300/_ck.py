@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
         "ck_backward": [p, p, p, i64, i64, i64, p, sz, p, p, p, p, p, p, p, sz, p],
         "ck_query_status": [p, p],
         "ck_set_option": [ctypes.c_int, i64],
+        "ck_probe_read": [p, sz, i64, p, p],
+        "ck_probe_gather": [p, i64, i64, p, i64, p, p],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -165,6 +167,18 @@ def ck_backward(handle, edge_values, leak, B, T, microsteps, saved, d_states, d_
 
 def ck_query_status(scratch, stream=None):
     _check(load().ck_query_status(_ptr(scratch), _stream(stream)))
+
+
+def ck_probe_read(buf, reps, sink, stream=None):
+    _check(load().ck_probe_read(_ptr(buf), buf.numel() * buf.element_size(), reps, _ptr(sink),
+                                _stream(stream)))
+
+
+def ck_probe_gather(rows, idx, sink, stream=None):
+    _need(rows, torch.float32, "rows")
+    _need(idx, torch.int32, "idx")
+    _check(load().ck_probe_gather(_ptr(rows), rows.shape[0], rows.shape[1], _ptr(idx),
+                                  idx.numel(), _ptr(sink), _stream(stream)))
 
 
 def ck_set_option(opt: int, value: int):

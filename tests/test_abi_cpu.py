@@ -1,0 +1,73 @@
+"""Host-side checks of libck that need no GPU: it builds for sm_103a, loads,
+exports every entry point include/ck.h declares, and rejects bad arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_graph_recurrent_gb300 import _ck
+    return _ck.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(ck_[a-z_0-9]+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"ck_graph_create", "ck_forward", "ck_backward", "ck_workspace_size"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in [(0, b"CK_OK"), (1, b"CK_ERR_INVALID_ARG"), (4, b"CK_ERR_TIMEOUT"),
+                       (5, b"CK_ERR_WORKSPACE"), (7, b"CK_ERR_UNSUPPORTED")]:
+        assert lib.ck_status_string(code) == name
+
+
+def test_options_validate(lib):
+    from sparse_graph_recurrent_gb300 import _ck
+    assert _ck.ck_get_option(_ck.OPT_PERSISTENT) == 1
+    assert _ck.ck_get_option(_ck.OPT_THREADS) == 512
+    with pytest.raises(_ck.CKError) as e:
+        _ck.ck_set_option(_ck.OPT_THREADS, 300)
+    assert e.value.name == "CK_ERR_INVALID_ARG"
+    with pytest.raises(_ck.CKError):
+        _ck.ck_set_option(_ck.OPT_BARRIER_TIMEOUT_NS, 10)
+    assert _ck.ck_get_option(_ck.OPT_THREADS) == 512
+
+
+def test_graph_create_rejects_bad_sizes_before_cuda(lib):
+    h = ctypes.c_void_p()
+    # N < 1, negative E, n_in > N, NULL output: all refused on the host
+    assert lib.ck_graph_create(None, None, 0, 0, None, 0, None, ctypes.byref(h)) == 1
+    assert lib.ck_graph_create(None, None, -1, 4, None, 0, None, ctypes.byref(h)) == 1
+    assert lib.ck_graph_create(None, None, 0, 4, None, 5, None, ctypes.byref(h)) == 1
+    assert lib.ck_graph_create(None, None, 0, 4, None, 0, None, None) == 1
+    assert lib.ck_graph_create(None, None, 3, 4, None, 0, None, ctypes.byref(h)) == 1  # NULL src
+    assert b"NULL" in lib.ck_last_error_message()
+    assert lib.ck_workspace_size(None, 1, 1, 1, None, None) == 1
+
+
+def test_no_cpu_fallback_without_a_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    src = (ctypes.c_int64 * 1)(0)
+    st = lib.ck_graph_create(src, src, 1, 1, None, 0, None, ctypes.byref(h))
+    assert st == 2 and not h.value  # CK_ERR_CUDA, no handle
