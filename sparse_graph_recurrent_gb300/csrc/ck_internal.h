@@ -14,6 +14,10 @@ struct ck_graph {
     int *row_ptr, *col, *perm;     // rows keyed by dst: col = src
     int *rowT_ptr, *colT, *permT;  // rows keyed by src: colT = dst
     int *slot;                     // slot[i] = k if input_nodes[k] == i, else -1
+    // Per direction (0: rows keyed by dst, 1: keyed by src), with the work cut
+    // into num_sms equal pieces of the merge path of (row ends, edges): the
+    // most rows any piece finishes and the most edges any piece holds.
+    int max_rows[2], max_edges[2];
 };
 
 namespace ck {
@@ -29,16 +33,25 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
 // Device-side status words written by the recurrence kernels.
 enum : int { kDevOk = 0, kDevTimeout = 1, kDevInternal = 2 };
 
+// Shared-memory layout of one direction's kernel (byte offsets).
+struct SmemLayout {
+    int o_grp, o_srp, o_prm, o_slot, o_head, o_carry, o_rows, o_tile, o_col, o_w, o_dw;
+    size_t bytes;
+    bool graph;  // the CTA's slice of the graph lives in shared memory
+    bool rows;   // row sums live in shared memory (else in global scratch)
+};
+
 // Launch description of one ck_forward / ck_backward call (recurrence.cu).
 struct Plan {
     int N, E, n_in;
     int B, Bp, LPE, EPW, NC, T, M, S;
-    int P;          // CTAs (one per SM)
-    int threads;    // threads per CTA
-    int warps;      // warps per CTA == sub-ranges per CTA
-    int cap;        // bound on edges in one CTA's range
-    bool smem_graph_fwd, smem_graph_bwd;
-    size_t smem_fwd, smem_bwd;
+    int P;            // CTAs (one per SM)
+    int threads;      // threads per CTA
+    int warps;        // warps per CTA
+    int groups;       // lane groups per CTA (warps * EPW)
+    int cap[2];       // bound on edges in one CTA's piece (0: forward rows, 1: transposed)
+    int rows_cap[2];  // bound on rows one CTA touches, plus 2
+    SmemLayout lay_fwd, lay_bwd;
     // scratch layout (byte offsets)
     size_t off_ctrl, ctrl_bytes;
     size_t off_carry;   // float [P][Bp]
@@ -46,6 +59,8 @@ struct Plan {
     size_t off_dwperm;  // float [E]
     size_t off_G;       // float [N][Bp]
     size_t off_da;      // float [2][N][Bp]
+    size_t off_rowsum;  // float [N][Bp]
+    size_t off_doutT;   // float [T][N][Bp]
     size_t scratch_bytes;
     size_t saved_bytes; // float [(S+1) + S][N][Bp]
 };

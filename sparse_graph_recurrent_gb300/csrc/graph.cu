@@ -12,6 +12,9 @@
 // which every key's rank among equal digits of its tile comes from warp match
 // masks taken in element order.  Every pass keeps equal keys in their previous
 // order, so the result lists each row's edges in ascending caller edge id.
+#include <algorithm>
+#include <vector>
+
 #include "ck_internal.h"
 
 namespace ck {
@@ -224,6 +227,23 @@ __global__ void k_gather_other(const int64_t *__restrict__ other, const int *__r
         col[k] = (int)other[perm[k]];
 }
 
+// First row and edge of each of P equal pieces of the merge path of
+// (row ends, edges): the largest r with row_ptr[r] + r <= floor(c (N+E) / P).
+__global__ void k_piece_bounds(const int *__restrict__ row_ptr, int N, int E, int P,
+                               int *__restrict__ out_r, int *__restrict__ out_e) {
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c <= P; c += gridDim.x * blockDim.x) {
+        const long long d = (long long)c * ((long long)N + E) / P;
+        int lo = 0, hi = (int)(d < N ? d : N);
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if ((long long)row_ptr[mid] + mid <= d) lo = mid;
+            else hi = mid - 1;
+        }
+        out_r[c] = lo;
+        out_e[c] = (int)(d - lo);
+    }
+}
+
 struct DevBuf {
     void *p = nullptr;
     ~DevBuf() {
@@ -265,7 +285,7 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
                        : cuda_fail(e, what);                                            \
     } while (0)
 
-    const size_t E1 = (size_t)(E > 0 ? E : 1);
+    const size_t E1 = std::max<size_t>((size_t)E, 2 * (size_t)g->num_sms + 8);
     CK_TRY(cudaMalloc((void **)&g->row_ptr, sizeof(int) * (N + 1)), "cudaMalloc row_ptr");
     CK_TRY(cudaMalloc((void **)&g->rowT_ptr, sizeof(int) * (N + 1)), "cudaMalloc rowT_ptr");
     CK_TRY(cudaMalloc((void **)&g->slot, sizeof(int) * N), "cudaMalloc slot");
@@ -331,7 +351,29 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
         CK_TRY(cudaGetLastError(), "row_ptr launch");
         // the second side reuses kb/vb; stream order already serialises it
     }
-    CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (graph build)");
+    // piece bounds for launch sizing (one piece per SM)
+    {
+        const int P = g->num_sms;
+        int *pr = kb, *pe = kb + (P + 1);  // kb is free now and holds >= 2 (P + 1) ints
+        std::vector<int> hr(P + 1), he(P + 1);
+        const int *rps[2] = {g->row_ptr, g->rowT_ptr};
+        for (int d = 0; d < 2; ++d) {
+            k_piece_bounds<<<(P + 256) / 256, 256, 0, s>>>(rps[d], N, E, P, pr, pe);
+            CK_TRY(cudaGetLastError(), "piece bounds launch");
+            CK_TRY(cudaMemcpyAsync(hr.data(), pr, sizeof(int) * (P + 1), cudaMemcpyDeviceToHost, s),
+                   "copy piece rows");
+            CK_TRY(cudaMemcpyAsync(he.data(), pe, sizeof(int) * (P + 1), cudaMemcpyDeviceToHost, s),
+                   "copy piece edges");
+            CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (piece bounds)");
+            int mr = 0, me = 0;
+            for (int c = 0; c < P; ++c) {
+                mr = std::max(mr, hr[c + 1] - hr[c]);
+                me = std::max(me, he[c + 1] - he[c]);
+            }
+            g->max_rows[d] = mr;
+            g->max_edges[d] = me;
+        }
+    }
 #undef CK_TRY
     return CK_OK;
 }

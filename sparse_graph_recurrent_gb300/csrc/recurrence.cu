@@ -2,41 +2,41 @@
 //
 // connectome-kernels page:
 //   intro           proposal = tanh(W h + drive + bias); h <- (1-leak) h +
-//                   leak * proposal, `microsteps` times per input step; one
-//                   fused forward per microstep; the backward has elementwise
-//                   terms with per-node row reductions, a transposed sparse
-//                   product for the state gradient and a per-edge dot product
-//                   over the batch for the edge gradient.  Everything fp32.
+//                   leak * proposal, `microsteps` times per input step; the
+//                   backward has elementwise terms with per-node row
+//                   reductions, a transposed sparse product for the state
+//                   gradient and a per-edge dot product over the batch for the
+//                   edge gradient.  Everything fp32.
 //   "Design notes"  states stored [N, B] so a node's batch row is contiguous;
 //                   rows with many edges split across warps with an on-chip
 //                   reduction; transposed CSR for the state gradient; state and
 //                   pre-activation saved after every microstep.
 //
-// Layout in device memory (all fp32, rows padded to Bp = B rounded up to 8):
+// Layout in device memory (fp32, rows padded to Bp = B rounded up to 8):
 //   H[s+1][N][Bp]  state after microstep s; H[0] = state0 transposed
 //   A[s][N][Bp]    pre-activation of microstep s
 //   G[N][Bp]       running state gradient (backward)
 //   da[2][N][Bp]   d(loss)/d(pre-activation), ping-pong between microsteps
+//   dOutT[T][N][Bp]  dOut transposed once at the start of the backward
 //
-// Work split.  One CTA per SM, one persistent cooperative launch per call;
+// Work split.  One CTA per SM and one persistent cooperative launch per call;
 // microsteps are separated by a grid-wide barrier whose wait is bounded.  The
-// rows and edges of the compressed layout are cut into P*U equal pieces along
-// the merge path of (row ends, edges) -- every warp gets the same number of
-// row ends plus edges, so a hub row is spread over as many warps (and CTAs) as
-// its size asks for.  A warp sums whole rows itself; a row cut by a piece
-// boundary leaves partial sums ("carries") that the warp owning the row's end
-// adds up in a fixed order after a CTA barrier (shared memory) or, across
-// CTAs, after a flag the producing CTA publishes (global memory).  No atomics
-// touch values, and the summation order never depends on timing.
-//
-// Lanes.  A warp processes EPW edges at once; each edge's batch row is read by
-// LPE lanes with 16-byte loads (LPE = Bp/4 when Bp <= 128, else 32 lanes that
-// loop over NC column chunks of 128).
-//
-// When one CTA's slice of the graph fits in shared memory it is loaded there
-// once per call (column ids, edge values in row order, and the edge-gradient
-// accumulators in the backward); otherwise it is read from global memory in
-// every microstep.
+// merge path of (row ends, edges) is cut into P x G equal pieces, one per lane
+// group (LPE lanes that together hold one batch row with 16-byte loads; a warp
+// holds 32 / LPE groups).  Each microstep has two parts:
+//   A  every group walks its piece in order, eight items at a time: all the
+//      gathers of a batch are issued before any is used, whatever rows they
+//      belong to.  At a row end the group's running sum goes to a row-sum slot
+//      in shared memory; the partial sum of the row its piece ends inside
+//      ("carry") goes to a per-group slot.
+//   B  after a CTA barrier, warps finish the CTA's rows, lane = batch column,
+//      four rows at a time: row sum, plus the carries of the earlier groups
+//      (and, for the CTA's first row, the carries earlier CTAs published),
+//      then the elementwise terms.  A row is finished only by the CTA that
+//      holds its row end, in a fixed summation order: results do not depend on
+//      timing.
+// When a CTA's slice of the graph fits in shared memory it is loaded there
+// once per call; otherwise it streams from global memory every microstep.
 #include <algorithm>
 #include <cstring>
 
@@ -47,18 +47,23 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxSmem = 227 * 1024;
-constexpr int kSmemReserve = 2048;  // static shared memory and slack
+constexpr int kStaticSmem = 64;
 
 struct KArgs {
-    int N, E, n_in, B, Bp, LPE, EPW, LPE_P2, EPW_P2, T, M, S;
-    int P, U, cap;
+    int N, E, n_in, B, Bp, LPE, EPW, LPE_P2, T, M, S;
+    int P, G;               // CTAs; lane groups per CTA
+    int cap, rows_cap;      // edges / rows (+2) bounds per CTA, for shared memory
+    int rs_smem;            // row sums in shared memory (else in global scratch)
+    // dynamic shared memory layout (byte offsets)
+    int o_grp, o_srp, o_prm, o_slot, o_head, o_carry, o_rows, o_tile, o_col, o_w, o_dw;
     const int *row_ptr, *col, *perm, *slot;
     const float *w, *leak, *bias, *drives, *state0;
     float *out;
     float *H, *A;
     const float *dout;
+    float *doutT;
     float *dw, *dleak, *dbias, *ddrives, *dstate0;
-    float *G, *da;
+    float *G_, *da, *rowsum_g;
     unsigned *bar;
     int *err;
     unsigned *flags;
@@ -78,6 +83,9 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
 __device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -92,76 +100,25 @@ __device__ __forceinline__ void fma4(float4 &a, float w, const float4 &x) {
     a.z = fmaf(w, x.z, a.z);
     a.w = fmaf(w, x.w, a.w);
 }
-__device__ __forceinline__ void add4(float4 &a, const float4 &x) {
-    a.x += x.x;
-    a.y += x.y;
-    a.z += x.z;
-    a.w += x.w;
+__device__ __forceinline__ float dot4(const float4 &a, const float4 &b, float d) {
+    d = fmaf(a.x, b.x, d);
+    d = fmaf(a.y, b.y, d);
+    d = fmaf(a.z, b.z, d);
+    return fmaf(a.w, b.w, d);
 }
-__device__ __forceinline__ float4 shfl_down4(const float4 &v, int d) {
-    return make_float4(__shfl_down_sync(kFull, v.x, d), __shfl_down_sync(kFull, v.y, d),
-                       __shfl_down_sync(kFull, v.z, d), __shfl_down_sync(kFull, v.w, d));
-}
-__device__ __forceinline__ float f4get(const float4 &v, int q) {
-    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
-}
-__device__ __forceinline__ void f4set(float4 &v, int q, float x) {
-    if (q == 0) v.x = x;
-    else if (q == 1) v.y = x;
-    else if (q == 2) v.z = x;
-    else v.w = x;
-}
-
-// Lane roles inside a warp.
-struct Lanes {
-    int lane, g, lig;
-    bool active;  // g < EPW
-    bool lead;    // g == 0: writes a row's results
-};
-
-__device__ __forceinline__ Lanes make_lanes(const KArgs &a, int lane) {
-    Lanes L;
-    L.lane = lane;
-    L.g = lane / a.LPE;
-    L.lig = lane - L.g * a.LPE;
-    L.active = L.g < a.EPW;
-    L.lead = L.g == 0;
-    return L;
-}
-template <int NC>
-__device__ __forceinline__ int col_of(const Lanes &L, int c) {
-    return c * 128 + L.lig * 4;
-}
-
-// Sum over the LPE lanes of each group; valid in the group's lane lig == 0.
-__device__ __forceinline__ float group_sum(float v, const KArgs &a, const Lanes &L) {
-    for (int o = a.LPE_P2 >> 1; o >= 1; o >>= 1) {
-        float y = __shfl_down_sync(kFull, v, o);
-        if (L.lig + o < a.LPE) v += y;
-    }
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     return v;
 }
 
-// Sum the EPW groups' partial rows into group 0.
-template <int NC>
-__device__ __forceinline__ void reduce_groups(float4 (&acc)[NC], const KArgs &a, const Lanes &L) {
-    for (int o = a.EPW_P2 >> 1; o >= 1; o >>= 1) {
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            float4 y = shfl_down4(acc[c], o * a.LPE);
-            if (L.g + o < a.EPW) add4(acc[c], y);
-        }
-    }
-}
-
-// Grid-wide barrier, bounded by a.timeout_ns.  Returns false (for the whole
-// CTA) once any CTA has recorded an error, so every CTA leaves together.
+// Grid-wide barrier, bounded by a.timeout_ns.  Returns false for the whole
+// CTA once any CTA has recorded an error, so every CTA leaves together.
 __device__ bool grid_sync(const KArgs &a, unsigned idx, int *s_ok) {
     __syncthreads();
     if (threadIdx.x == 0) {
         const unsigned target = (a.bar_base + idx + 1u) * (unsigned)a.P + a.bar_extra;
-        __threadfence();
-        atomicAdd(a.bar, 1u);
+        red_release_add(a.bar, 1u);
         const unsigned long long t0 = globaltimer();
         int e = 0;
         while (ld_acquire(a.bar) < target) {
@@ -172,14 +129,13 @@ __device__ bool grid_sync(const KArgs &a, unsigned idx, int *s_ok) {
                 break;
             }
         }
-        __threadfence();
         *s_ok = (e == 0 && ld_err(a.err) == 0) ? 1 : 0;
     }
     __syncthreads();
     return *s_ok != 0;
 }
 
-// Bounded wait for another CTA's carry flag.
+// Bounded wait for another CTA's carry flag (all lanes of a warp call it).
 __device__ __forceinline__ void wait_flag(const KArgs &a, const unsigned *f, unsigned want) {
     const unsigned long long t0 = globaltimer();
     while (ld_acquire(f) < want) {
@@ -191,9 +147,6 @@ __device__ __forceinline__ void wait_flag(const KArgs &a, const unsigned *f, uns
     }
 }
 
-__device__ __forceinline__ long long diag_of(long long gu, long long items, long long nsub) {
-    return (gu * items) / nsub;
-}
 // Merge-path split: the largest r in [0, min(d, N)] with row_ptr[r] + r <= d.
 __device__ __forceinline__ int merge_search(const int *row_ptr, int N, long long d) {
     int lo = 0, hi = (int)(d < (long long)N ? d : (long long)N);
@@ -205,328 +158,483 @@ __device__ __forceinline__ int merge_search(const int *row_ptr, int N, long long
     return lo;
 }
 
-// Where a warp's piece of the merge path starts and ends, and whom it waits for.
-struct Piece {
-    int r0, e0, r1, e1;
-    bool head;   // row r0 is finished here but started in an earlier piece
-    int u_lo;    // first local piece whose carry belongs to row r0
-    int c_lo;    // first CTA whose published carry belongs to row r0 (== own CTA: none)
+// Transposes between the caller's batch-major [B][N] arrays and the
+// node-major [N][Bp] rows, for rows [r0, r1), through a 32x33 tile.
+// Every thread of the CTA must call these.
+template <int THREADS>
+__device__ void to_rows(float *__restrict__ dst, const float *__restrict__ src, int r0, int r1,
+                        int B, int Bp, int N, float *tile) {
+    const int tid = threadIdx.x;
+    for (int rb = r0; rb < r1; rb += 32) {
+        for (int cb = 0; cb < Bp; cb += 32) {
+            for (int x = tid; x < 32 * 32; x += THREADS) {
+                const int rr = x & 31, bb = x >> 5;
+                const int r = rb + rr, b = cb + bb;
+                tile[bb * 33 + rr] = (r < r1 && b < B) ? __ldg(src + (size_t)b * N + r) : 0.f;
+            }
+            __syncthreads();
+            for (int x = tid; x < 32 * 32; x += THREADS) {
+                const int bb = x & 31, rr = x >> 5;
+                const int r = rb + rr, b = cb + bb;
+                if (r < r1 && b < Bp) dst[(size_t)r * Bp + b] = tile[bb * 33 + rr];
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <int THREADS>
+__device__ void from_rows(float *__restrict__ dst, const float *__restrict__ src, int r0, int r1,
+                          int B, int Bp, int N, float *tile) {
+    const int tid = threadIdx.x;
+    for (int rb = r0; rb < r1; rb += 32) {
+        for (int cb = 0; cb < B; cb += 32) {
+            for (int x = tid; x < 32 * 32; x += THREADS) {
+                const int bb = x & 31, rr = x >> 5;
+                const int r = rb + rr, b = cb + bb;
+                tile[bb * 33 + rr] = (r < r1 && b < B) ? __ldcg(src + (size_t)r * Bp + b) : 0.f;
+            }
+            __syncthreads();
+            for (int x = tid; x < 32 * 32; x += THREADS) {
+                const int rr = x & 31, bb = x >> 5;
+                const int r = rb + rr, b = cb + bb;
+                if (r < r1 && b < B) __stcs(dst + (size_t)b * N + r, tile[bb * 33 + rr]);
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Per-CTA view of its piece of the work, in shared memory.
+struct Cta {
+    int *grp_r, *grp_e;  // [G+1] first row / edge of each group's piece
+    int *srp;            // row_ptr[cta_r0 + i], i < nrows + 2 (clamped at N)
+    float2 *prm;         // {leak, bias} of rows cta_r0 + i
+    int *sslot;          // slot of rows cta_r0 + i
+    int *head;           // finishing group of row cta_r0 + i if carries reach it, else -1
+    float *scarry;       // [G][Bp]
+    float *rows;         // [nrows][Bp] row sums (shared or global)
+    float *tile;         // [32][33]
+    int *scol;
+    float *sw, *sdw;
+    int r0, nrows, e0, e1, c_lo, p_lo;
+    bool publish;
 };
 
-// ------------------------------------------------------------ gather loops
+// ------------------------------------------------------------ part A
 
-// Accumulate sum_k w[k] * rows[col[k]] over edges [elo, ehi) into acc (per
-// group); in the backward also add each edge's dot product with the own row
-// `hp` into the edge-gradient accumulator.
+// Walk this lane group's piece: gather rows[col[k]] * w[k] into per-row sums.
+// Backward: also add each edge's dot product with the state h_{s-1} of its
+// source row into the edge-gradient accumulator.
 template <int NC, bool SMEMG, bool BWD, int UNR>
-__device__ __forceinline__ void gather(const KArgs &a, const Lanes &L, const int *scol,
-                                       const float *sw, float *sdw, int cta_e0,
-                                       const float *__restrict__ rows, int elo, int ehi,
-                                       float4 (&acc)[NC], const float4 (&hp)[NC]) {
+__device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int gam, int g, int lig,
+                                             bool active, const float *__restrict__ rows,
+                                             const float *__restrict__ hprev) {
     const int Bp = a.Bp;
-    for (int base = elo; base < ehi; base += a.EPW * UNR) {
-        int kk[UNR];
-        float wv[UNR];
-        float4 v[UNR][NC];
+    int r = 0, e = 0, items = 0, rend = 0;
+    if (active) {
+        r = c.grp_r[gam];
+        e = c.grp_e[gam];
+        items = (c.grp_r[gam + 1] - r) + (c.grp_e[gam + 1] - e);
+        rend = c.srp[r - c.r0 + 1];
+    }
+    const int trips = (__reduce_max_sync(kFull, (unsigned)items) + UNR - 1) / UNR;
+    float4 acc[NC];
+#pragma unroll
+    for (int ch = 0; ch < NC; ++ch) acc[ch] = zero4();
+    for (int it = 0; it < trips; ++it) {
+        int kind[UNR], idx[UNR], rq[UNR];
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
-            const int k = base + q * a.EPW + L.g;
-            const bool ok = L.active && k < ehi;
-            int c = 0;
-            float wq = 0.f;
-            if (ok) {
-                if (SMEMG) {
-                    c = scol[k - cta_e0];
-                    wq = sw[k - cta_e0];
+            kind[q] = 0;
+            idx[q] = 0;
+            rq[q] = r;
+            if (items > 0) {
+                if (e < rend) {
+                    kind[q] = 1;
+                    idx[q] = e++;
                 } else {
-                    c = __ldg(a.col + k);
-                    wq = __ldcg(a.wperm + k);
+                    kind[q] = 2;
+                    idx[q] = r++;
+                    rend = c.srp[r - c.r0 + 1];
+                }
+                --items;
+            }
+        }
+        float wq[UNR];
+        float4 v[UNR][NC];
+        float4 hq[BWD ? UNR : 1][NC];
+#pragma unroll
+        for (int q = 0; q < UNR; ++q) {
+            int cc = 0;
+            wq[q] = 0.f;
+            if (kind[q] == 1) {
+                if (SMEMG) {
+                    cc = c.scol[idx[q] - c.e0];
+                    wq[q] = c.sw[idx[q] - c.e0];
+                } else {
+                    cc = __ldg(a.col + idx[q]);
+                    wq[q] = __ldcg(a.wperm + idx[q]);
                 }
             }
-            kk[q] = ok ? k : -1;
-            wv[q] = wq;
-            const float *rp = rows + (size_t)c * Bp;
+            const float *rp = rows + (size_t)cc * Bp;
+            const float *hp = hprev + (size_t)rq[q] * Bp;
 #pragma unroll
             for (int ch = 0; ch < NC; ++ch) {
-                const int col0 = col_of<NC>(L, ch);
-                v[q][ch] = (ok && col0 < Bp) ? __ldcg(reinterpret_cast<const float4 *>(rp + col0))
+                const int col0 = ch * 128 + lig * 4;
+                const bool ok = kind[q] == 1 && col0 < Bp;
+                v[q][ch] = ok ? __ldcg(reinterpret_cast<const float4 *>(rp + col0)) : zero4();
+                if (BWD)
+                    hq[BWD ? q : 0][ch] = ok ? __ldg(reinterpret_cast<const float4 *>(hp + col0))
                                              : zero4();
             }
         }
 #pragma unroll
-        for (int q = 0; q < UNR; ++q)
+        for (int q = 0; q < UNR; ++q) {
+            if (kind[q] == 1) {
 #pragma unroll
-            for (int ch = 0; ch < NC; ++ch) fma4(acc[ch], wv[q], v[q][ch]);
+                for (int ch = 0; ch < NC; ++ch) fma4(acc[ch], wq[q], v[q][ch]);
+            } else if (kind[q] == 2) {
+                float *dst = c.rows + (size_t)(idx[q] - c.r0) * Bp;
+#pragma unroll
+                for (int ch = 0; ch < NC; ++ch) {
+                    const int col0 = ch * 128 + lig * 4;
+                    if (col0 < Bp) *reinterpret_cast<float4 *>(dst + col0) = acc[ch];
+                    acc[ch] = zero4();
+                }
+            }
+        }
         if (BWD) {
 #pragma unroll
             for (int q = 0; q < UNR; ++q) {
                 float d = 0.f;
 #pragma unroll
-                for (int ch = 0; ch < NC; ++ch) {
-                    d = fmaf(v[q][ch].x, hp[ch].x, d);
-                    d = fmaf(v[q][ch].y, hp[ch].y, d);
-                    d = fmaf(v[q][ch].z, hp[ch].z, d);
-                    d = fmaf(v[q][ch].w, hp[ch].w, d);
+                for (int ch = 0; ch < NC; ++ch) d = dot4(v[q][ch], hq[BWD ? q : 0][ch], d);
+                for (int o = a.LPE_P2 >> 1; o >= 1; o >>= 1) {
+                    const float y = __shfl_down_sync(kFull, d, o);
+                    if (lig + o < a.LPE) d += y;
                 }
-                d = group_sum(d, a, L);
-                if (L.lig == 0 && kk[q] >= 0) {
-                    if (SMEMG) sdw[kk[q] - cta_e0] += d;
-                    else a.dwperm[kk[q]] += d;
+                if (lig == 0 && kind[q] == 1) {
+                    if (SMEMG) c.sdw[idx[q] - c.e0] += d;
+                    else a.dwperm[idx[q]] += d;
                 }
             }
         }
     }
+    if (active) {
+#pragma unroll
+        for (int ch = 0; ch < NC; ++ch) {
+            const int col0 = ch * 128 + lig * 4;
+            if (col0 < Bp) *reinterpret_cast<float4 *>(c.scarry + (size_t)gam * Bp + col0) = acc[ch];
+        }
+    }
+    (void)g;
 }
 
-// ------------------------------------------------------- row finalisation
+// ------------------------------------------------------------ part B
 
-// Forward: pre-activation, tanh, leak blend, saved copies and the output.
-template <int NC>
-__device__ void fwd_finalize(const KArgs &a, const Lanes &L, int r, const float4 (&acc)[NC],
-                             int s) {
-    if (!L.lead) return;
-    const int t = s / a.M, m = s - t * a.M;
-    const int Bp = a.Bp, B = a.B;
-    const size_t NBp = (size_t)a.N * Bp;
-    const float *hin = a.H + (size_t)s * NBp + (size_t)r * Bp;
-    float *hout = a.H + (size_t)(s + 1) * NBp + (size_t)r * Bp;
-    float *aout = a.A + (size_t)s * NBp + (size_t)r * Bp;
-    const float lam = __ldg(a.leak + r), bia = __ldg(a.bias + r);
-    const int sl = __ldg(a.slot + r);
-    const float *drv = sl >= 0 ? a.drives + ((size_t)t * a.n_in + sl) * B : nullptr;
-    const bool emit = (m == a.M - 1);
-#pragma unroll
-    for (int ch = 0; ch < NC; ++ch) {
-        const int col0 = col_of<NC>(L, ch);
-        if (col0 >= Bp) continue;
-        const float4 hp = __ldcg(reinterpret_cast<const float4 *>(hin + col0));
-        float4 av = acc[ch], hn;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int b = col0 + q;
-            float x = f4get(av, q) + bia, y = 0.f;
-            if (b < B) {
-                if (drv) x += __ldg(drv + b);
-                const float p = tanhf(x);
-                y = fmaf(lam, p, (1.f - lam) * f4get(hp, q));
-                if (emit) __stcs(a.out + ((size_t)t * B + b) * a.N + r, y);
-            } else {
-                x = 0.f;
+// Sum of row i's partial sums for column b: the finishing group's own part,
+// then the carries of earlier groups of this CTA, then those published by
+// earlier CTAs (global carries only reach the CTA's first row).
+__device__ __forceinline__ float row_total(const KArgs &a, const Cta &c, int i, int b,
+                                           unsigned phase_id, bool pro) {
+    if (pro) return 0.f;
+    float x = a.rs_smem ? c.rows[(size_t)i * a.Bp + b] : __ldcg(c.rows + (size_t)i * a.Bp + b);
+    const int gf = c.head[i];
+    if (gf >= 0) {
+        const int r = c.r0 + i;
+        int v = gf - 1, lo = gf;
+        while (v >= 0) {
+            lo = v;
+            if (c.grp_r[v] != r) break;
+            --v;
+        }
+        for (int u = lo; u < gf; ++u) x += c.scarry[(size_t)u * a.Bp + b];
+        if (v < 0 && i == 0) {
+            for (int cc = c.c_lo; cc < (int)blockIdx.x; ++cc) {
+                wait_flag(a, a.flags + cc, phase_id);
+                x += __ldcg(a.carry + (size_t)cc * a.Bp + b);
             }
-            f4set(av, q, x);
-            f4set(hn, q, y);
         }
-        __stcs(reinterpret_cast<float4 *>(aout + col0), av);
-        *reinterpret_cast<float4 *>(hout + col0) = hn;
     }
+    return x;
 }
 
-// Backward elementwise terms of microstep q for node j, given Gn = dL/dh_q[j]:
-// da = Gn * leak * (1 - p^2), p = tanh(a_q); leak and bias row reductions;
-// the drive gradient at input nodes.  All lanes call this (for the shuffles).
-template <int NC>
-__device__ void elementwise(const KArgs &a, const Lanes &L, int j, const float4 (&Gn)[NC], int q,
-                            float lam) {
-    const int Bp = a.Bp, B = a.B;
-    const size_t NBp = (size_t)a.N * Bp;
-    const float *Aq = a.A + (size_t)q * NBp + (size_t)j * Bp;
-    const float *Hq = a.H + (size_t)q * NBp + (size_t)j * Bp;  // state entering microstep q
-    float *daq = a.da + (size_t)(q & 1) * NBp + (size_t)j * Bp;
-    const int sl = __ldg(a.slot + j);
-    const int tq = q / a.M;
-    const bool first = (q - tq * a.M) == a.M - 1;  // first visit of step tq going backwards
-    float *dd = sl >= 0 ? a.ddrives + ((size_t)tq * a.n_in + sl) * B : nullptr;
-    float dl = 0.f, db = 0.f;
+// Forward finish of rows: pre-activation, tanh, leak blend, saved copies.
+template <int THREADS>
+__device__ void finish_fwd(const KArgs &a, const Cta &c, int s, unsigned phase_id) {
+    constexpr int U = THREADS / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Bp = a.Bp, B = a.B, N = a.N;
+    const int t = s / a.M;
+    const size_t NBp = (size_t)N * Bp;
+    const float *hin = a.H + (size_t)s * NBp;
+    float *hout = a.H + (size_t)(s + 1) * NBp;
+    float *aout = a.A + (size_t)s * NBp;
+    const int NCH = (Bp + 31) >> 5;
+    const int cpb = NCH < 4 ? NCH : 4;
+    const int RB = 4 / cpb;
+    const int CB = (NCH + cpb - 1) / cpb;
+    for (int i0 = warp * RB; i0 < c.nrows; i0 += U * RB) {
+        for (int cb = 0; cb < CB; ++cb) {
+            float x[4], hp[4], dr[4];
+            int bcol[4], irow[4];
+            bool ok[4];
 #pragma unroll
-    for (int ch = 0; ch < NC; ++ch) {
-        const int col0 = col_of<NC>(L, ch);
-        if (!L.lead || col0 >= Bp) continue;
-        *reinterpret_cast<float4 *>(a.G + (size_t)j * Bp + col0) = Gn[ch];
-        const float4 av = __ldcs(reinterpret_cast<const float4 *>(Aq + col0));
-        const float4 hv = __ldg(reinterpret_cast<const float4 *>(Hq + col0));
-        float4 d4;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int b = col0 + k;
-            float d = 0.f;
-            if (b < B) {
-                const float g = f4get(Gn[ch], k);
-                const float p = tanhf(f4get(av, k));
-                d = g * lam * (1.f - p * p);
-                dl = fmaf(g, p - f4get(hv, k), dl);
-                db += d;
-                if (dd) dd[b] = first ? d : dd[b] + d;
+            for (int el = 0; el < 4; ++el) {
+                const int ri = el / cpb, ci = el - ri * cpb;
+                const int i = i0 + ri, cc = cb * cpb + ci, b = cc * 32 + lane;
+                ok[el] = ri < RB && i < c.nrows && cc < NCH && b < Bp;
+                irow[el] = i;
+                bcol[el] = b;
+                x[el] = hp[el] = dr[el] = 0.f;
+                if (ok[el]) {
+                    const int r = c.r0 + i;
+                    hp[el] = __ldcg(hin + (size_t)r * Bp + b);
+                    const int sl = c.sslot[i];
+                    if (sl >= 0 && b < B) dr[el] = __ldg(a.drives + ((size_t)t * a.n_in + sl) * B + b);
+                }
             }
-            f4set(d4, k, d);
-        }
-        *reinterpret_cast<float4 *>(daq + col0) = d4;
-    }
-    dl = group_sum(dl, a, L);
-    db = group_sum(db, a, L);
-    if (L.lead && L.lig == 0) {
-        if (q == a.S - 1) {
-            a.dleak[j] = dl;
-            a.dbias[j] = db;
-        } else {
-            a.dleak[j] += dl;
-            a.dbias[j] += db;
+#pragma unroll
+            for (int el = 0; el < 4; ++el) {
+                // warp-uniform: every lane of an element slot shares its row
+                const int ri = el / cpb;
+                const bool row_ok = ri < RB && irow[el] < c.nrows;
+                if (row_ok) x[el] = row_total(a, c, irow[el], ok[el] ? bcol[el] : 0, phase_id, false);
+            }
+#pragma unroll
+            for (int el = 0; el < 4; ++el) {
+                if (!ok[el]) continue;
+                const int i = irow[el], r = c.r0 + i, b = bcol[el];
+                const float2 pr = c.prm[i];
+                float av = x[el] + pr.y + dr[el], hv = 0.f;
+                if (b < B) hv = fmaf(pr.x, tanhf(av), (1.f - pr.x) * hp[el]);
+                else av = 0.f;
+                hout[(size_t)r * Bp + b] = hv;
+                __stcs(aout + (size_t)r * Bp + b, av);
+            }
         }
     }
 }
 
-// Backward: finish G_{s-1}[j] = G_s[j] (1 - leak) + (W^T da_s)[j] (+ dOut of the
-// step that ends at microstep s-1), then the elementwise terms of microstep s-1;
-// at s == 0 the result is the gradient of state0.
-template <int NC>
-__device__ void bwd_finalize(const KArgs &a, const Lanes &L, int j, const float4 (&acc)[NC],
-                             int s) {
-    const int Bp = a.Bp, B = a.B;
-    const float lam = __ldg(a.leak + j);
+// Backward finish of rows for microstep s: G_{s-1} = G_s (1 - leak) + row
+// total (+ dOut of the step ending at s-1), then the elementwise terms of
+// microstep q = s-1.  s == S is the prologue (G_{S-1} = dOut[T-1]); s == 0
+// leaves G_{-1} in G for the final transpose into d_state0.
+template <int THREADS>
+__device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_id) {
+    constexpr int U = THREADS / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Bp = a.Bp, B = a.B, N = a.N, M = a.M;
+    const size_t NBp = (size_t)N * Bp;
+    const bool pro = s == a.S;
     const int q = s - 1;
-    const int tq = q >= 0 ? q / a.M : 0;
-    const bool add_dout = q >= 0 && (q - tq * a.M) == a.M - 1;
-    float4 Gn[NC];
+    const int tq = q >= 0 ? q / M : 0;
+    const bool step_end = q >= 0 && q - tq * M == M - 1;
+    const float *Aq = a.A + (size_t)(q >= 0 ? q : 0) * NBp;
+    const float *Hq = a.H + (size_t)(q >= 0 ? q : 0) * NBp;
+    const float *dO = a.doutT + (size_t)tq * NBp;
+    float *daq = a.da + (size_t)(q & 1) * NBp;
+    const int NCH = (Bp + 31) >> 5;
+    const int cpb = NCH < 4 ? NCH : 4;
+    const int RB = 4 / cpb;
+    const int CB = (NCH + cpb - 1) / cpb;
+    for (int i0 = warp * RB; i0 < c.nrows; i0 += U * RB) {
+        float dl[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int cb = 0; cb < CB; ++cb) {
+            float x[4], gv[4], ov[4], av[4], hv[4];
+            int bcol[4], irow[4];
+            bool ok[4];
 #pragma unroll
-    for (int ch = 0; ch < NC; ++ch) {
-        const int col0 = col_of<NC>(L, ch);
-        Gn[ch] = zero4();
-        if (!L.lead || col0 >= Bp) continue;
-        const float4 g = __ldcg(reinterpret_cast<const float4 *>(a.G + (size_t)j * Bp + col0));
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int b = col0 + k;
-            float x = 0.f;
-            if (b < B) {
-                x = fmaf(f4get(g, k), 1.f - lam, f4get(acc[ch], k));
-                if (add_dout) x += __ldg(a.dout + ((size_t)tq * B + b) * a.N + j);
-                if (s == 0) a.dstate0[(size_t)b * a.N + j] = x;
+            for (int el = 0; el < 4; ++el) {
+                const int ri = el / cpb, ci = el - ri * cpb;
+                const int i = i0 + ri, cc = cb * cpb + ci, b = cc * 32 + lane;
+                ok[el] = ri < RB && i < c.nrows && cc < NCH && b < Bp;
+                irow[el] = i;
+                bcol[el] = b;
+                x[el] = gv[el] = ov[el] = av[el] = hv[el] = 0.f;
+                if (ok[el]) {
+                    const size_t o = (size_t)(c.r0 + i) * Bp + b;
+                    if (!pro) gv[el] = __ldcg(a.G_ + o);
+                    if (step_end) ov[el] = __ldcg(dO + o);
+                    if (q >= 0) {
+                        av[el] = __ldcs(Aq + o);
+                        hv[el] = __ldg(Hq + o);
+                    }
+                }
             }
-            f4set(Gn[ch], k, x);
+#pragma unroll
+            for (int el = 0; el < 4; ++el) {
+                const int ri = el / cpb;
+                const bool row_ok = ri < RB && irow[el] < c.nrows;
+                if (row_ok) x[el] = row_total(a, c, irow[el], ok[el] ? bcol[el] : 0, phase_id, pro);
+            }
+#pragma unroll
+            for (int el = 0; el < 4; ++el) {
+                if (!ok[el]) continue;
+                const int i = irow[el], r = c.r0 + i, b = bcol[el];
+                const size_t o = (size_t)r * Bp + b;
+                const float lam = c.prm[i].x;
+                float gn = fmaf(gv[el], 1.f - lam, x[el]) + ov[el];
+                if (b >= B) gn = 0.f;
+                a.G_[o] = gn;
+                if (q < 0) continue;
+                float d = 0.f;
+                if (b < B) {
+                    const float p = tanhf(av[el]);
+                    d = gn * lam * (1.f - p * p);
+                    dl[el / cpb] = fmaf(gn, p - hv[el], dl[el / cpb]);
+                    db[el / cpb] += d;
+                    const int sl = c.sslot[i];
+                    if (sl >= 0) {
+                        float *dd = a.ddrives + ((size_t)tq * a.n_in + sl) * B + b;
+                        *dd = (q - tq * M == M - 1) ? d : *dd + d;
+                    }
+                }
+                daq[o] = d;
+            }
+        }
+        if (q >= 0) {
+#pragma unroll
+            for (int ri = 0; ri < 4; ++ri) {
+                if (ri >= RB) break;
+                const int i = i0 + ri;
+                if (i >= c.nrows) break;
+                const float sl = warp_sum(dl[ri]), sb = warp_sum(db[ri]);
+                if (lane == 0) {
+                    const int r = c.r0 + i;
+                    if (q == a.S - 1) {
+                        a.dleak[r] = sl;
+                        a.dbias[r] = sb;
+                    } else {
+                        a.dleak[r] += sl;
+                        a.dbias[r] += sb;
+                    }
+                }
+            }
         }
     }
-    if (s > 0) elementwise<NC>(a, L, j, Gn, q, lam);
+}
+
+// Publish this CTA's carry for the row its last piece ends inside.
+__device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsigned phase_id) {
+    const int lane = threadIdx.x & 31;
+    for (int b = lane; b < a.Bp; b += 32) {
+        float x = 0.f;
+        for (int u = c.p_lo; u < a.G; ++u) x += c.scarry[(size_t)u * a.Bp + b];
+        __stcg(a.carry + (size_t)blockIdx.x * a.Bp + b, x);
+    }
+    __syncwarp();
+    if (lane == 0) st_release(a.flags + blockIdx.x, phase_id);
 }
 
 // ------------------------------------------------------------------ kernel
 
 template <int THREADS, int NC, bool SMEMG, bool BWD>
 __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
-    constexpr int U = THREADS / 32;
     constexpr int UNR = NC == 1 ? 8 : (NC == 2 ? 4 : 2);
-    extern __shared__ float4 smem_dyn[];
-    __shared__ int sub_r[U + 1], sub_e[U + 1];
-    __shared__ int s_ok;
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int s_ok, s_meta[4];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta = blockIdx.x;
-    const Lanes L = make_lanes(a, lane);
     const int N = a.N, Bp = a.Bp;
     const size_t NBp = (size_t)N * Bp;
+    const int g = lane / a.LPE, lig = lane - (lane / a.LPE) * a.LPE;
+    const bool active = g < a.EPW;
+    const int gam = warp * a.EPW + g;  // this lane's group in the CTA (if active)
 
-    // ---- this warp's piece of the merge path
-    const long long items = (long long)N + a.E, nsub = (long long)a.P * U;
-    Piece pc;
-    {
-        int r0 = 0, e0 = 0, r1 = 0, e1 = 0;
-        if (lane == 0) {
-            const long long d0 = diag_of((long long)cta * U + warp, items, nsub);
-            const long long d1 = diag_of((long long)cta * U + warp + 1, items, nsub);
-            r0 = merge_search(a.row_ptr, N, d0);
-            r1 = merge_search(a.row_ptr, N, d1);
-            e0 = (int)(d0 - r0);
-            e1 = (int)(d1 - r1);
-        }
-        pc.r0 = __shfl_sync(kFull, r0, 0);
-        pc.e0 = __shfl_sync(kFull, e0, 0);
-        pc.r1 = __shfl_sync(kFull, r1, 0);
-        pc.e1 = __shfl_sync(kFull, e1, 0);
-        if (lane == 0) {
-            sub_r[warp] = pc.r0;
-            sub_e[warp] = pc.e0;
-            if (warp == U - 1) {
-                sub_r[U] = pc.r1;
-                sub_e[U] = pc.e1;
-            }
+    Cta c;
+    c.grp_r = reinterpret_cast<int *>(smem + a.o_grp);
+    c.grp_e = c.grp_r + (a.G + 1);
+    c.srp = reinterpret_cast<int *>(smem + a.o_srp);
+    c.prm = reinterpret_cast<float2 *>(smem + a.o_prm);
+    c.sslot = reinterpret_cast<int *>(smem + a.o_slot);
+    c.head = reinterpret_cast<int *>(smem + a.o_head);
+    c.scarry = reinterpret_cast<float *>(smem + a.o_carry);
+    c.tile = reinterpret_cast<float *>(smem + a.o_tile);
+    c.scol = reinterpret_cast<int *>(smem + a.o_col);
+    c.sw = reinterpret_cast<float *>(smem + a.o_w);
+    c.sdw = reinterpret_cast<float *>(smem + a.o_dw);
+
+    // ---- pieces of the merge path, one per lane group
+    const long long items = (long long)N + a.E, nsub = (long long)a.P * a.G;
+    if (active && lig == 0) {
+        const long long gg = (long long)cta * a.G + gam;
+        const long long d0 = gg * items / nsub;
+        const int r0 = merge_search(a.row_ptr, N, d0);
+        c.grp_r[gam] = r0;
+        c.grp_e[gam] = (int)(d0 - r0);
+        if (gam == a.G - 1) {
+            const long long d1 = (gg + 1) * items / nsub;
+            const int r1 = merge_search(a.row_ptr, N, d1);
+            c.grp_r[a.G] = r1;
+            c.grp_e[a.G] = (int)(d1 - r1);
         }
     }
     __syncthreads();
-    const int cta_e0 = sub_e[0], cta_e1 = sub_e[U];
-    {
-        const int R = pc.r0;
-        pc.head = pc.r0 < pc.r1 && pc.e0 > __ldg(a.row_ptr + R);
-        pc.u_lo = warp;
-        pc.c_lo = cta;
-        if (pc.head) {
-            int v = warp - 1;
-            while (v >= 0) {
-                pc.u_lo = v;
-                if (sub_r[v] != R) break;
-                --v;
-            }
-            if (v < 0 && cta > 0) {
-                int c = cta - 1;
-                if (lane == 0) {
-                    while (c > 0 && merge_search(a.row_ptr, N, diag_of((long long)c * U, items, nsub)) == R)
-                        --c;
-                }
-                pc.c_lo = __shfl_sync(kFull, c, 0);
-            }
-        }
-    }
-    // carries this CTA publishes: pieces [p_lo, U) all end inside row Rc
-    const int Rc = sub_r[U];
-    const bool publish = cta + 1 < a.P && Rc < N;
-    int p_lo = U - 1;
-    while (p_lo > 0 && sub_r[p_lo] == Rc) --p_lo;
-
-    // ---- shared memory: carries, then this CTA's slice of the graph
-    float *scarry = reinterpret_cast<float *>(smem_dyn);  // [U][Bp]
-    int *scol = reinterpret_cast<int *>(scarry + (size_t)U * Bp);
-    float *sw = reinterpret_cast<float *>(scol + a.cap);
-    float *sdw = sw + a.cap;
-    if (SMEMG && cta_e1 - cta_e0 > a.cap) {
+    c.r0 = c.grp_r[0];
+    c.nrows = c.grp_r[a.G] - c.r0;
+    c.e0 = c.grp_e[0];
+    c.e1 = c.grp_e[a.G];
+    c.rows = a.rs_smem ? reinterpret_cast<float *>(smem + a.o_rows) : a.rowsum_g + (size_t)c.r0 * Bp;
+    if (c.nrows + 2 > a.rows_cap || (SMEMG && c.e1 - c.e0 > a.cap)) {
         if (tid == 0) atomicCAS(a.err, 0, kDevInternal);
-        return;  // the other CTAs see the error word at their next wait
+        return;  // every other CTA sees the error word at its next wait
     }
-    for (int k = cta_e0 + tid; k < cta_e1; k += THREADS) {
+    for (int i = tid; i < c.nrows + 2; i += THREADS) c.srp[i] = __ldg(a.row_ptr + min(c.r0 + i, N));
+    for (int i = tid; i < c.nrows; i += THREADS) {
+        const int r = c.r0 + i;
+        c.prm[i] = make_float2(__ldg(a.leak + r), BWD ? 0.f : __ldg(a.bias + r));
+        c.sslot[i] = __ldg(a.slot + r);
+        c.head[i] = -1;
+    }
+    for (int k = c.e0 + tid; k < c.e1; k += THREADS) {
         if (SMEMG) {
-            scol[k - cta_e0] = __ldg(a.col + k);
-            sw[k - cta_e0] = __ldg(a.w + __ldg(a.perm + k));
-            if (BWD) sdw[k - cta_e0] = 0.f;
+            c.scol[k - c.e0] = __ldg(a.col + k);
+            c.sw[k - c.e0] = __ldg(a.w + __ldg(a.perm + k));
+            if (BWD) c.sdw[k - c.e0] = 0.f;
         } else if (a.do_prologue) {
             a.wperm[k] = __ldg(a.w + __ldg(a.perm + k));
             if (BWD) a.dwperm[k] = 0.f;
         }
     }
     __syncthreads();
+    // rows whose partial sums arrive from earlier groups: the group finishing them
+    for (int u = tid; u < a.G; u += THREADS) {
+        const int r = c.grp_r[u];
+        if (r < c.grp_r[u + 1] && c.grp_e[u] > c.srp[r - c.r0]) c.head[r - c.r0] = u;
+    }
+    if (tid == 0) {
+        // earlier CTAs whose carries reach this CTA's first row
+        int clo = cta;
+        if (cta > 0 && c.grp_e[0] > c.srp[0]) {
+            clo = cta - 1;
+            while (clo > 0 && merge_search(a.row_ptr, N, (long long)clo * items / a.P) == c.r0) --clo;
+        }
+        s_meta[0] = clo;
+        // pieces whose carry belongs to the row this CTA's last piece ends inside
+        const int Rc = c.grp_r[a.G];
+        int plo = a.G - 1;
+        while (plo > 0 && c.grp_r[plo] == Rc) --plo;
+        s_meta[1] = plo;
+        s_meta[2] = (cta + 1 < a.P && Rc < N) ? 1 : 0;
+    }
+    __syncthreads();
+    c.c_lo = s_meta[0];
+    c.p_lo = s_meta[1];
+    c.publish = s_meta[2] != 0;
 
     unsigned nbar = 0;
     if (a.do_prologue) {
         if (!BWD) {
-            // state0 [B][N] -> H[0] [N][Bp], pad columns zero
-            const size_t total = NBp;
-            for (size_t i = (size_t)cta * THREADS + tid; i < total; i += (size_t)a.P * THREADS) {
-                const int node = (int)(i / Bp), b = (int)(i - (size_t)node * Bp);
-                a.H[i] = b < a.B ? __ldg(a.state0 + (size_t)b * N + node) : 0.f;
-            }
+            to_rows<THREADS>(a.H, a.state0, c.r0, c.r0 + c.nrows, a.B, Bp, N, c.tile);
         } else {
-            // G_{S-1} = dOut[T-1]^T, then the elementwise terms of the last microstep
-            for (int j = pc.r0; j < pc.r1; ++j) {
-                float4 Gn[NC];
-#pragma unroll
-                for (int ch = 0; ch < NC; ++ch) {
-                    const int col0 = col_of<NC>(L, ch);
-                    Gn[ch] = zero4();
-                    if (!L.lead || col0 >= Bp) continue;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int b = col0 + k;
-                        if (b < a.B)
-                            f4set(Gn[ch], k, __ldg(a.dout + ((size_t)(a.T - 1) * a.B + b) * N + j));
-                    }
-                }
-                elementwise<NC>(a, L, j, Gn, a.S - 1, __ldg(a.leak + j));
-            }
+            for (int t = 0; t < a.T; ++t)
+                to_rows<THREADS>(a.doutT + (size_t)t * NBp, a.dout + (size_t)t * a.B * N, c.r0,
+                                 c.r0 + c.nrows, a.B, Bp, N, c.tile);
+            __syncthreads();
+            finish_bwd<THREADS>(a, c, a.S, 0u);
         }
         if (!grid_sync(a, nbar++, &s_ok)) return;
     }
@@ -535,107 +643,26 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         const int s = BWD ? a.s_first - it : a.s_first + it;
         const unsigned phase_id = BWD ? (unsigned)(a.S - s) : (unsigned)(s + 1);
         const float *rows = BWD ? a.da + (size_t)(s & 1) * NBp : a.H + (size_t)s * NBp;
-        float4 head[NC];
-#pragma unroll
-        for (int ch = 0; ch < NC; ++ch) head[ch] = zero4();
-
-        for (int r = pc.r0; r <= pc.r1 && r < N; ++r) {
-            const int elo = max(__ldg(a.row_ptr + r), pc.e0);
-            const int ehi = min(__ldg(a.row_ptr + r + 1), pc.e1);
-            float4 acc[NC], hp[NC];
-#pragma unroll
-            for (int ch = 0; ch < NC; ++ch) {
-                acc[ch] = zero4();
-                hp[ch] = zero4();
-                if (BWD) {
-                    const int col0 = col_of<NC>(L, ch);
-                    if (L.active && col0 < Bp && elo < ehi)
-                        hp[ch] = __ldg(reinterpret_cast<const float4 *>(
-                            a.H + (size_t)s * NBp + (size_t)r * Bp + col0));
-                }
-            }
-            gather<NC, SMEMG, BWD, UNR>(a, L, scol, sw, sdw, cta_e0, rows, elo, ehi, acc, hp);
-            reduce_groups<NC>(acc, a, L);
-            if (r == pc.r1) {
-                if (L.lead) {
-#pragma unroll
-                    for (int ch = 0; ch < NC; ++ch) {
-                        const int col0 = col_of<NC>(L, ch);
-                        if (col0 < Bp)
-                            *reinterpret_cast<float4 *>(scarry + (size_t)warp * Bp + col0) = acc[ch];
-                    }
-                }
-            } else if (r == pc.r0 && pc.head) {
-#pragma unroll
-                for (int ch = 0; ch < NC; ++ch) head[ch] = acc[ch];
-            } else {
-                if (BWD) bwd_finalize<NC>(a, L, r, acc, s);
-                else fwd_finalize<NC>(a, L, r, acc, s);
-            }
-        }
+        stream_piece<NC, SMEMG, BWD, UNR>(a, c, gam, g, lig, active, rows,
+                                          a.H + (size_t)s * NBp);
         __syncthreads();
-
-        // publish this CTA's carry for row Rc
-        if (publish && warp == U - 1) {
-            if (L.lead) {
-#pragma unroll
-                for (int ch = 0; ch < NC; ++ch) {
-                    const int col0 = col_of<NC>(L, ch);
-                    if (col0 >= Bp) continue;
-                    float4 sum = zero4();
-                    for (int v = p_lo; v < U; ++v)
-                        add4(sum, *reinterpret_cast<const float4 *>(scarry + (size_t)v * Bp + col0));
-                    __stcg(reinterpret_cast<float4 *>(a.carry + (size_t)cta * Bp + col0), sum);
-                }
-                __threadfence();
-            }
-            __syncwarp();
-            if (lane == 0) st_release(a.flags + cta, phase_id);
-        }
-        // finish the head row: earlier CTAs' carries, earlier local pieces, own part
-        if (pc.head) {
-            float4 tot[NC];
-#pragma unroll
-            for (int ch = 0; ch < NC; ++ch) tot[ch] = zero4();
-            for (int c = pc.c_lo; c < cta; ++c) {
-                wait_flag(a, a.flags + c, phase_id);
-                if (L.lead) {
-#pragma unroll
-                    for (int ch = 0; ch < NC; ++ch) {
-                        const int col0 = col_of<NC>(L, ch);
-                        if (col0 < Bp)
-                            add4(tot[ch], __ldcg(reinterpret_cast<const float4 *>(
-                                              a.carry + (size_t)c * Bp + col0)));
-                    }
-                }
-            }
-            __syncwarp();
-            if (L.lead) {
-                for (int v = pc.u_lo; v < warp; ++v) {
-#pragma unroll
-                    for (int ch = 0; ch < NC; ++ch) {
-                        const int col0 = col_of<NC>(L, ch);
-                        if (col0 < Bp)
-                            add4(tot[ch],
-                                 *reinterpret_cast<const float4 *>(scarry + (size_t)v * Bp + col0));
-                    }
-                }
-#pragma unroll
-                for (int ch = 0; ch < NC; ++ch) add4(tot[ch], head[ch]);
-            }
-            if (BWD) bwd_finalize<NC>(a, L, pc.r0, tot, s);
-            else fwd_finalize<NC>(a, L, pc.r0, tot, s);
-        }
+        if (warp == 0 && c.publish) publish_carry(a, c, phase_id);
+        if (BWD) finish_bwd<THREADS>(a, c, s, phase_id);
+        else finish_fwd<THREADS>(a, c, s, phase_id);
         if (it + 1 < a.s_count)
             if (!grid_sync(a, nbar++, &s_ok)) return;
     }
 
-    if (BWD && a.do_epilogue) {
-        // edge gradients back to the caller's edge order
+    if (a.do_epilogue) {
         __syncthreads();
-        for (int k = cta_e0 + tid; k < cta_e1; k += THREADS) {
-            const float v = SMEMG ? sdw[k - cta_e0] : a.dwperm[k];
-            a.dw[__ldg(a.perm + k)] = v;
+        if (!BWD) {
+            for (int t = 0; t < a.T; ++t)
+                from_rows<THREADS>(a.out + (size_t)t * a.B * N, a.H + (size_t)(t + 1) * a.M * NBp,
+                                   c.r0, c.r0 + c.nrows, a.B, Bp, N, c.tile);
+        } else {
+            from_rows<THREADS>(a.dstate0, a.G_, c.r0, c.r0 + c.nrows, a.B, Bp, N, c.tile);
+            for (int k = c.e0 + tid; k < c.e1; k += THREADS)
+                a.dw[__ldg(a.perm + k)] = SMEMG ? c.sdw[k - c.e0] : a.dwperm[k];
         }
     }
 }
@@ -665,8 +692,35 @@ int pow2ceil(int x) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
-void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch) {
+// Shared-memory layout of one direction.
+SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_rows) {
+    SmemLayout L;
+    size_t o = 0;
+    const int rc = p.rows_cap[dir];
+    L.o_grp = (int)o; o = align16(o + 8 * (size_t)(p.groups + 1));
+    L.o_srp = (int)o; o = align16(o + 4 * (size_t)rc);
+    L.o_prm = (int)o; o = align16(o + 8 * (size_t)rc);
+    L.o_slot = (int)o; o = align16(o + 4 * (size_t)rc);
+    L.o_head = (int)o; o = align16(o + 4 * (size_t)rc);
+    L.o_carry = (int)o; o = align16(o + 4 * (size_t)p.groups * p.Bp);
+    L.o_tile = (int)o; o = align16(o + 4 * 32 * 33);
+    const size_t base = o;
+    const size_t rows_b = 4 * (size_t)rc * p.Bp;
+    const size_t graph_b = (dir == 0 ? 8 : 12) * (size_t)p.cap[dir];
+    const size_t budget = kMaxSmem - kStaticSmem - 1024;
+    L.rows = want_rows && base + rows_b <= budget;
+    L.graph = want_graph && base + (L.rows ? rows_b : 0) + graph_b <= budget;
+    L.o_rows = (int)o; o = align16(o + (L.rows ? rows_b : 0));
+    L.o_col = (int)o; o = align16(o + (L.graph ? 4 * (size_t)p.cap[dir] : 0));
+    L.o_w = (int)o; o = align16(o + (L.graph ? 4 * (size_t)p.cap[dir] : 0));
+    L.o_dw = (int)o; o = align16(o + (L.graph && dir == 1 ? 4 * (size_t)p.cap[dir] : 0));
+    L.bytes = o;
+    return L;
+}
+
+void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int dir) {
     std::memset(&k, 0, sizeof(k));
     k.N = p.N;
     k.E = p.E;
@@ -676,13 +730,26 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch) {
     k.LPE = p.LPE;
     k.EPW = p.EPW;
     k.LPE_P2 = pow2ceil(p.LPE);
-    k.EPW_P2 = pow2ceil(p.EPW);
     k.T = p.T;
     k.M = p.M;
     k.S = p.S;
     k.P = p.P;
-    k.U = p.warps;
-    k.cap = p.cap;
+    k.G = p.groups;
+    k.cap = p.cap[dir];
+    k.rows_cap = p.rows_cap[dir];
+    const SmemLayout &L = dir == 0 ? p.lay_fwd : p.lay_bwd;
+    k.rs_smem = L.rows ? 1 : 0;
+    k.o_grp = L.o_grp;
+    k.o_srp = L.o_srp;
+    k.o_prm = L.o_prm;
+    k.o_slot = L.o_slot;
+    k.o_head = L.o_head;
+    k.o_carry = L.o_carry;
+    k.o_rows = L.o_rows;
+    k.o_tile = L.o_tile;
+    k.o_col = L.o_col;
+    k.o_w = L.o_w;
+    k.o_dw = L.o_dw;
     k.slot = g->slot;
     char *sc = (char *)scratch;
     k.bar = (unsigned *)(sc + p.off_ctrl);
@@ -691,26 +758,26 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch) {
     k.carry = (float *)(sc + p.off_carry);
     k.wperm = (float *)(sc + p.off_wperm);
     k.dwperm = (float *)(sc + p.off_dwperm);
-    k.G = (float *)(sc + p.off_G);
+    k.G_ = (float *)(sc + p.off_G);
     k.da = (float *)(sc + p.off_da);
+    k.rowsum_g = (float *)(sc + p.off_rowsum);
+    k.doutT = (float *)(sc + p.off_doutT);
     k.bar_extra = (unsigned)options().barrier_extra;
     k.timeout_ns = (unsigned long long)options().timeout_ns;
 }
 
-ck_status launch_all(KArgs &k, const Plan &p, bool bwd, bool smem, size_t smem_bytes,
-                     cudaStream_t s, int64_t *launches) {
-    KernelFn fn = pick_kernel(p.threads, p.NC, smem, bwd);
+ck_status launch_all(KArgs &k, const Plan &p, bool bwd, cudaStream_t s, int64_t *launches) {
+    const SmemLayout &L = bwd ? p.lay_bwd : p.lay_fwd;
+    KernelFn fn = pick_kernel(p.threads, p.NC, L.graph, bwd);
     cudaError_t e = cudaFuncSetAttribute((const void *)fn,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_bytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)fn, p.threads,
-                                                      smem_bytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)fn, p.threads, L.bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     if (per_sm < 1)
         return fail(CK_ERR_UNSUPPORTED, "kernel does not fit on an SM (%d threads, %zu B shared)",
-                    p.threads, smem_bytes);
+                    p.threads, L.bytes);
     e = cudaMemsetAsync((char *)k.bar, 0, p.ctrl_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (control words)");
     int64_t n = 0;
@@ -733,8 +800,8 @@ ck_status launch_all(KArgs &k, const Plan &p, bool bwd, bool smem, size_t smem_b
             ki.bar_base = i == 0 ? 0u : 1u;
         }
         void *args[] = {&ki};
-        e = cudaLaunchCooperativeKernel((const void *)fn, dim3(p.P), dim3(p.threads), args,
-                                        smem_bytes, s);
+        e = cudaLaunchCooperativeKernel((const void *)fn, dim3(p.P), dim3(p.threads), args, L.bytes,
+                                        s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
         ++n;
     }
@@ -765,18 +832,17 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     q.P = g->num_sms;
     q.threads = options().threads == 1024 ? 1024 : 512;
     q.warps = q.threads / 32;
-    const int64_t items = g->N + g->E;
-    q.cap = (int)(items / q.P + 2);
-    const size_t carry_smem = (size_t)q.warps * q.Bp * 4;
-    const size_t budget = kMaxSmem - kSmemReserve;
-    const bool allow = options().graph_in_smem && options().persistent;
-    q.smem_fwd = carry_smem + (size_t)q.cap * 8;
-    q.smem_bwd = carry_smem + (size_t)q.cap * 12;
-    q.smem_graph_fwd = allow && q.smem_fwd <= budget;
-    q.smem_graph_bwd = allow && q.smem_bwd <= budget;
-    if (!q.smem_graph_fwd) q.smem_fwd = carry_smem;
-    if (!q.smem_graph_bwd) q.smem_bwd = carry_smem;
-    if (carry_smem > budget) return fail(CK_ERR_UNSUPPORTED, "carry buffers exceed shared memory");
+    q.groups = q.warps * q.EPW;
+    for (int d = 0; d < 2; ++d) {
+        q.cap[d] = g->max_edges[d] + 1;
+        q.rows_cap[d] = g->max_rows[d] + 3;
+    }
+    const bool want_graph = options().graph_in_smem && options().persistent;
+    q.lay_fwd = smem_layout(q, 0, want_graph, true);
+    q.lay_bwd = smem_layout(q, 1, want_graph, true);
+    if (q.lay_fwd.bytes > (size_t)(kMaxSmem - kStaticSmem) ||
+        q.lay_bwd.bytes > (size_t)(kMaxSmem - kStaticSmem))
+        return fail(CK_ERR_UNSUPPORTED, "per-CTA tables exceed shared memory (rows per SM too many)");
     const size_t NBp = (size_t)q.N * q.Bp;
     const size_t E1 = (size_t)(q.E > 0 ? q.E : 1);
     size_t off = 0;
@@ -793,6 +859,10 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     off = align256(off + 4 * NBp);
     q.off_da = off;
     off = align256(off + 8 * NBp);
+    q.off_rowsum = off;
+    off = align256(off + 4 * NBp);
+    q.off_doutT = off;
+    off = align256(off + 4 * NBp * (size_t)q.T);
     q.scratch_bytes = off;
     q.saved_bytes = 4 * NBp * (size_t)(2 * q.S + 1);
     *p = q;
@@ -802,7 +872,7 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
 ck_status launch_forward(const ck_graph *g, const Plan &p, const FwdIO &io, cudaStream_t s,
                          int64_t *launches) {
     KArgs k;
-    fill_common(k, g, p, io.scratch);
+    fill_common(k, g, p, io.scratch, 0);
     k.row_ptr = g->row_ptr;
     k.col = g->col;
     k.perm = g->perm;
@@ -814,13 +884,13 @@ ck_status launch_forward(const ck_graph *g, const Plan &p, const FwdIO &io, cuda
     k.out = io.out;
     k.H = io.saved;
     k.A = io.saved + (size_t)(p.S + 1) * p.N * p.Bp;
-    return launch_all(k, p, false, p.smem_graph_fwd, p.smem_fwd, s, launches);
+    return launch_all(k, p, false, s, launches);
 }
 
 ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cudaStream_t s,
                           int64_t *launches) {
     KArgs k;
-    fill_common(k, g, p, io.scratch);
+    fill_common(k, g, p, io.scratch, 1);
     k.row_ptr = g->rowT_ptr;
     k.col = g->colT;
     k.perm = g->permT;
@@ -834,7 +904,7 @@ ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cud
     k.dbias = io.dbias;
     k.ddrives = io.ddrives;
     k.dstate0 = io.dstate0;
-    return launch_all(k, p, true, p.smem_graph_bwd, p.smem_bwd, s, launches);
+    return launch_all(k, p, true, s, launches);
 }
 
 }  // namespace ck
