@@ -14,6 +14,7 @@ struct ck_graph {
     int *row_ptr, *col, *perm;     // rows keyed by dst: col = src
     int *rowT_ptr, *colT, *permT;  // rows keyed by src: colT = dst
     int *slot;                     // slot[i] = k if input_nodes[k] == i, else -1
+    int *rowid, *rowidT;           // row of each row-ordered edge (dst[perm[k]], src[permT[k]])
     // Per direction (0: rows keyed by dst, 1: keyed by src), with the work cut
     // into num_sms equal pieces of the merge path of (row ends, edges): the
     // most rows any piece finishes and the most edges any piece holds.
@@ -35,7 +36,7 @@ enum : int { kDevOk = 0, kDevTimeout = 1, kDevInternal = 2 };
 
 // Shared-memory layout of one direction's kernel (byte offsets).
 struct SmemLayout {
-    int o_grp, o_srp, o_prm, o_slot, o_head, o_carry, o_rows, o_tile, o_col, o_w, o_dw;
+    int o_srp, o_prm, o_slot, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;
     size_t bytes;
     bool graph;  // the CTA's slice of the graph lives in shared memory
     bool rows;   // row sums live in shared memory (else in global scratch)

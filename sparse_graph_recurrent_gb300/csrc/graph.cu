@@ -293,6 +293,8 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
     CK_TRY(cudaMalloc((void **)&g->perm, sizeof(int) * E1), "cudaMalloc perm");
     CK_TRY(cudaMalloc((void **)&g->colT, sizeof(int) * E1), "cudaMalloc colT");
     CK_TRY(cudaMalloc((void **)&g->permT, sizeof(int) * E1), "cudaMalloc permT");
+    CK_TRY(cudaMalloc((void **)&g->rowid, sizeof(int) * E1), "cudaMalloc rowid");
+    CK_TRY(cudaMalloc((void **)&g->rowidT, sizeof(int) * E1), "cudaMalloc rowidT");
 
     const int ntiles = (E + kTile - 1) / kTile;
     const size_t n_hist = 256 * (size_t)(ntiles > 0 ? ntiles : 1);
@@ -329,10 +331,10 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
     int key_bits = 0;  // keys are < N
     while (key_bits < 31 && ((int64_t)1 << key_bits) < (int64_t)N) ++key_bits;
     struct Side {
-        int *keys, *vals, *row_ptr, *col, *perm;
-        const int64_t *other;
-    } sides[2] = {{key_dst, ids, g->row_ptr, g->col, g->perm, src},
-                  {key_src, ids2, g->rowT_ptr, g->colT, g->permT, dst}};
+        int *keys, *vals, *row_ptr, *col, *perm, *rowid;
+        const int64_t *other, *own;
+    } sides[2] = {{key_dst, ids, g->row_ptr, g->col, g->perm, g->rowid, src, dst},
+                  {key_src, ids2, g->rowT_ptr, g->colT, g->permT, g->rowidT, dst, src}};
     for (auto &sd : sides) {
         int *ks = sd.keys, *vs = sd.vals;
         if (E > 0) {
@@ -346,6 +348,7 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
             CK_TRY(cudaMemcpyAsync(sd.perm, vs, sizeof(int) * E, cudaMemcpyDeviceToDevice, s),
                    "copy perm");
             k_gather_other<<<blocks, 256, 0, s>>>(sd.other, sd.perm, E, sd.col);
+            k_gather_other<<<blocks, 256, 0, s>>>(sd.own, sd.perm, E, sd.rowid);
         }
         k_row_ptr<<<(N + 256) / 256, 256, 0, s>>>(ks, E, N, sd.row_ptr);
         CK_TRY(cudaGetLastError(), "row_ptr launch");

@@ -20,21 +20,22 @@
 //   dOutT[T][N][Bp]  dOut transposed once at the start of the backward
 //
 // Work split.  One CTA per SM and one persistent cooperative launch per call;
-// microsteps are separated by a grid-wide barrier whose wait is bounded.  The
-// merge path of (row ends, edges) is cut into P x G equal pieces, one per lane
-// group (LPE lanes that together hold one batch row with 16-byte loads; a warp
-// holds 32 / LPE groups).  Each microstep has two parts:
-//   A  every group walks its piece in order, eight items at a time: all the
-//      gathers of a batch are issued before any is used, whatever rows they
-//      belong to.  At a row end the group's running sum goes to a row-sum slot
-//      in shared memory; the partial sum of the row its piece ends inside
-//      ("carry") goes to a per-group slot.
+// microsteps are separated by a grid-wide barrier whose wait is bounded.  CTA
+// c owns the c-th of P equal pieces of the merge path of (row ends, edges):
+// a range of edges and the rows whose ends fall in its piece.  Inside the CTA
+// the edge range is cut into G equal sub-ranges, one per lane group (LPE
+// lanes that together hold one batch row as NC chunks of 16-byte loads; a
+// warp holds 32 / LPE groups).  Each microstep has two parts:
+//   A  every group walks its edges in order, UNR at a time: all the gathers of
+//      a batch are issued before any is used, whatever rows they belong to.
+//      When the row id changes, the group's running sum of the row that ended
+//      goes to that row's slot in shared memory; the partial sum of the row it
+//      stops inside goes to the group's carry slot.
 //   B  after a CTA barrier, warps finish the CTA's rows, lane = batch column,
-//      four rows at a time: row sum, plus the carries of the earlier groups
-//      (and, for the CTA's first row, the carries earlier CTAs published),
-//      then the elementwise terms.  A row is finished only by the CTA that
-//      holds its row end, in a fixed summation order: results do not depend on
-//      timing.
+//      up to four rows at a time: row slot, plus the carries of the groups
+//      that hold the row's earlier edges (and, for the CTA's first row, the
+//      carries earlier CTAs published), then the elementwise terms.  Every sum
+//      is taken in a fixed order: results do not depend on timing.
 // When a CTA's slice of the graph fits in shared memory it is loaded there
 // once per call; otherwise it streams from global memory every microstep.
 #include <algorithm>
@@ -55,8 +56,8 @@ struct KArgs {
     int cap, rows_cap;      // edges / rows (+2) bounds per CTA, for shared memory
     int rs_smem;            // row sums in shared memory (else in global scratch)
     // dynamic shared memory layout (byte offsets)
-    int o_grp, o_srp, o_prm, o_slot, o_head, o_carry, o_rows, o_tile, o_col, o_w, o_dw;
-    const int *row_ptr, *col, *perm, *slot;
+    int o_srp, o_prm, o_slot, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;
+    const int *row_ptr, *col, *perm, *slot, *rowid;
     const float *w, *leak, *bias, *drives, *state0;
     float *out;
     float *H, *A;
@@ -207,102 +208,104 @@ __device__ void from_rows(float *__restrict__ dst, const float *__restrict__ src
 
 // Per-CTA view of its piece of the work, in shared memory.
 struct Cta {
-    int *grp_r, *grp_e;  // [G+1] first row / edge of each group's piece
-    int *srp;            // row_ptr[cta_r0 + i], i < nrows + 2 (clamped at N)
-    float2 *prm;         // {leak, bias} of rows cta_r0 + i
-    int *sslot;          // slot of rows cta_r0 + i
-    int *head;           // finishing group of row cta_r0 + i if carries reach it, else -1
-    float *scarry;       // [G][Bp]
-    float *rows;         // [nrows][Bp] row sums (shared or global)
-    float *tile;         // [32][33]
-    int *scol;
-    float *sw, *sdw;
-    int r0, nrows, e0, e1, c_lo, p_lo;
+    int *srp;       // row_ptr[r0 + i], i < nrows + 2 (clamped at N)
+    float2 *prm;    // {leak, bias} of rows r0 + i
+    int *sslot;     // slot of rows r0 + i
+    float *scarry;  // [G][Bp]
+    float *rows;    // [nrows][Bp] row slots (shared or global)
+    float *tile;    // [32][33]
+    int2 *scw;      // {col, bits of w} of the CTA's edges
+    int *srow;      // row of the CTA's edges
+    float *sdw;     // edge-gradient accumulators of the CTA's edges
+    int r0, nrows, e0, e1, c_lo;
     bool publish;
 };
 
+// The lane group whose edge sub-range holds edge k of the CTA (n = e1 - e0 > 0).
+__device__ __forceinline__ int group_of(const Cta &c, int G, int k) {
+    const long long n = c.e1 - c.e0;
+    const int g = (int)(((long long)(k - c.e0 + 1) * G - 1) / n);
+    return g < G - 1 ? g : G - 1;
+}
+
 // ------------------------------------------------------------ part A
 
-// Walk this lane group's piece: gather rows[col[k]] * w[k] into per-row sums.
+// Walk this lane group's edges: gather rows[col[k]] * w[k] into per-row sums.
 // Backward: also add each edge's dot product with the state h_{s-1} of its
 // source row into the edge-gradient accumulator.
 template <int NC, bool SMEMG, bool BWD, int UNR>
-__device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int gam, int g, int lig,
+__device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int gam, int lig,
                                              bool active, const float *__restrict__ rows,
                                              const float *__restrict__ hprev) {
-    const int Bp = a.Bp;
-    int r = 0, e = 0, items = 0, rend = 0;
-    if (active) {
-        r = c.grp_r[gam];
-        e = c.grp_e[gam];
-        items = (c.grp_r[gam + 1] - r) + (c.grp_e[gam + 1] - e);
-        rend = c.srp[r - c.r0 + 1];
+    const int Bp = a.Bp, CW = 4 * a.LPE;
+    const int n = c.e1 - c.e0;
+    int k0 = c.e0, k1 = c.e0;
+    if (active && n > 0) {
+        k0 = c.e0 + (int)((long long)gam * n / a.G);
+        k1 = c.e0 + (int)((long long)(gam + 1) * n / a.G);
     }
-    const int trips = (__reduce_max_sync(kFull, (unsigned)items) + UNR - 1) / UNR;
+    const int len = k1 - k0;
+    const int trips = (__reduce_max_sync(kFull, (unsigned)len) + UNR - 1) / UNR;
+    int cur = -1;
+    if (len > 0) cur = SMEMG ? c.srow[k0 - c.e0] : __ldg(a.rowid + k0);
     float4 acc[NC];
 #pragma unroll
     for (int ch = 0; ch < NC; ++ch) acc[ch] = zero4();
-    for (int it = 0; it < trips; ++it) {
-        int kind[UNR], idx[UNR], rq[UNR];
+    auto flush = [&](int row) {
+        const int i = row - c.r0;
+        if (i >= 0 && i < c.nrows) {
+            float *dst = c.rows + (size_t)i * Bp + lig * 4;
 #pragma unroll
-        for (int q = 0; q < UNR; ++q) {
-            kind[q] = 0;
-            idx[q] = 0;
-            rq[q] = r;
-            if (items > 0) {
-                if (e < rend) {
-                    kind[q] = 1;
-                    idx[q] = e++;
-                } else {
-                    kind[q] = 2;
-                    idx[q] = r++;
-                    rend = c.srp[r - c.r0 + 1];
-                }
-                --items;
-            }
+            for (int ch = 0; ch < NC; ++ch) *reinterpret_cast<float4 *>(dst + ch * CW) = acc[ch];
+        } else {
+            atomicCAS(a.err, 0, kDevInternal);  // cannot happen for a valid graph
         }
+#pragma unroll
+        for (int ch = 0; ch < NC; ++ch) acc[ch] = zero4();
+    };
+    int k = k0;
+    for (int it = 0; it < trips; ++it, k += UNR) {
+        int rid[UNR];
         float wq[UNR];
         float4 v[UNR][NC];
         float4 hq[BWD ? UNR : 1][NC];
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
+            const int kk = k + q;
+            const bool ok = kk < k1;
             int cc = 0;
+            rid[q] = cur;
             wq[q] = 0.f;
-            if (kind[q] == 1) {
+            if (ok) {
                 if (SMEMG) {
-                    cc = c.scol[idx[q] - c.e0];
-                    wq[q] = c.sw[idx[q] - c.e0];
+                    const int2 cw = c.scw[kk - c.e0];
+                    cc = cw.x;
+                    wq[q] = __int_as_float(cw.y);
+                    rid[q] = c.srow[kk - c.e0];
                 } else {
-                    cc = __ldg(a.col + idx[q]);
-                    wq[q] = __ldcg(a.wperm + idx[q]);
+                    cc = __ldg(a.col + kk);
+                    wq[q] = __ldcg(a.wperm + kk);
+                    rid[q] = __ldg(a.rowid + kk);
                 }
             }
-            const float *rp = rows + (size_t)cc * Bp;
-            const float *hp = hprev + (size_t)rq[q] * Bp;
+            const float *rp = rows + (size_t)cc * Bp + lig * 4;
+            const float *hp = hprev + (size_t)rid[q] * Bp + lig * 4;
 #pragma unroll
             for (int ch = 0; ch < NC; ++ch) {
-                const int col0 = ch * 128 + lig * 4;
-                const bool ok = kind[q] == 1 && col0 < Bp;
-                v[q][ch] = ok ? __ldcg(reinterpret_cast<const float4 *>(rp + col0)) : zero4();
+                v[q][ch] = ok ? __ldcg(reinterpret_cast<const float4 *>(rp + ch * CW)) : zero4();
                 if (BWD)
-                    hq[BWD ? q : 0][ch] = ok ? __ldg(reinterpret_cast<const float4 *>(hp + col0))
-                                             : zero4();
+                    hq[BWD ? q : 0][ch] =
+                        ok ? __ldg(reinterpret_cast<const float4 *>(hp + ch * CW)) : zero4();
             }
         }
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
-            if (kind[q] == 1) {
-#pragma unroll
-                for (int ch = 0; ch < NC; ++ch) fma4(acc[ch], wq[q], v[q][ch]);
-            } else if (kind[q] == 2) {
-                float *dst = c.rows + (size_t)(idx[q] - c.r0) * Bp;
-#pragma unroll
-                for (int ch = 0; ch < NC; ++ch) {
-                    const int col0 = ch * 128 + lig * 4;
-                    if (col0 < Bp) *reinterpret_cast<float4 *>(dst + col0) = acc[ch];
-                    acc[ch] = zero4();
-                }
+            if (rid[q] != cur) {
+                flush(cur);
+                cur = rid[q];
             }
+#pragma unroll
+            for (int ch = 0; ch < NC; ++ch) fma4(acc[ch], wq[q], v[q][ch]);
         }
         if (BWD) {
 #pragma unroll
@@ -314,47 +317,46 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                     const float y = __shfl_down_sync(kFull, d, o);
                     if (lig + o < a.LPE) d += y;
                 }
-                if (lig == 0 && kind[q] == 1) {
-                    if (SMEMG) c.sdw[idx[q] - c.e0] += d;
-                    else a.dwperm[idx[q]] += d;
+                if (lig == 0 && k + q < k1) {
+                    if (SMEMG) c.sdw[k + q - c.e0] += d;
+                    else a.dwperm[k + q] += d;
                 }
             }
         }
     }
     if (active) {
+        // the row this group stops in: finished here if its last edge is ours
+        // and its row end belongs to this CTA, else a carry
+        const bool fin = len > 0 && cur >= c.r0 && cur < c.r0 + c.nrows &&
+                         c.srp[cur - c.r0 + 1] == k1;
+        if (fin) flush(cur);
+        float *dst = c.scarry + (size_t)gam * Bp + lig * 4;
 #pragma unroll
-        for (int ch = 0; ch < NC; ++ch) {
-            const int col0 = ch * 128 + lig * 4;
-            if (col0 < Bp) *reinterpret_cast<float4 *>(c.scarry + (size_t)gam * Bp + col0) = acc[ch];
-        }
+        for (int ch = 0; ch < NC; ++ch) *reinterpret_cast<float4 *>(dst + ch * CW) = acc[ch];
     }
-    (void)g;
 }
 
 // ------------------------------------------------------------ part B
 
-// Sum of row i's partial sums for column b: the finishing group's own part,
-// then the carries of earlier groups of this CTA, then those published by
-// earlier CTAs (global carries only reach the CTA's first row).
+// Sum of row i's partial sums for column b: its slot (the part summed by the
+// group holding its last edge), then the carries of the groups holding its
+// earlier edges in this CTA, then those published by earlier CTAs (which can
+// only reach the CTA's first row).
 __device__ __forceinline__ float row_total(const KArgs &a, const Cta &c, int i, int b,
                                            unsigned phase_id, bool pro) {
     if (pro) return 0.f;
-    float x = a.rs_smem ? c.rows[(size_t)i * a.Bp + b] : __ldcg(c.rows + (size_t)i * a.Bp + b);
-    const int gf = c.head[i];
-    if (gf >= 0) {
-        const int r = c.r0 + i;
-        int v = gf - 1, lo = gf;
-        while (v >= 0) {
-            lo = v;
-            if (c.grp_r[v] != r) break;
-            --v;
-        }
-        for (int u = lo; u < gf; ++u) x += c.scarry[(size_t)u * a.Bp + b];
-        if (v < 0 && i == 0) {
-            for (int cc = c.c_lo; cc < (int)blockIdx.x; ++cc) {
-                wait_flag(a, a.flags + cc, phase_id);
-                x += __ldcg(a.carry + (size_t)cc * a.Bp + b);
-            }
+    const int rs = c.srp[i], re = c.srp[i + 1];
+    float x = 0.f;
+    if (re > rs && re - 1 >= c.e0) {
+        x = a.rs_smem ? c.rows[(size_t)i * a.Bp + b] : __ldcg(c.rows + (size_t)i * a.Bp + b);
+        const int ga = group_of(c, a.G, rs > c.e0 ? rs : c.e0);
+        const int gb = group_of(c, a.G, re - 1);
+        for (int u = ga; u < gb; ++u) x += c.scarry[(size_t)u * a.Bp + b];
+    }
+    if (i == 0 && rs < c.e0) {
+        for (int cc = c.c_lo; cc < (int)blockIdx.x; ++cc) {
+            wait_flag(a, a.flags + cc, phase_id);
+            x += __ldcg(a.carry + (size_t)cc * a.Bp + b);
         }
     }
     return x;
@@ -516,12 +518,15 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
     }
 }
 
-// Publish this CTA's carry for the row its last piece ends inside.
+// Publish this CTA's carry for the row its piece ends inside (row r0 + nrows):
+// the carries of the groups holding that row's edges here, in group order.
 __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsigned phase_id) {
     const int lane = threadIdx.x & 31;
+    const int ka = c.srp[c.nrows] > c.e0 ? c.srp[c.nrows] : c.e0;
+    const int ga = ka < c.e1 ? group_of(c, a.G, ka) : a.G;
     for (int b = lane; b < a.Bp; b += 32) {
         float x = 0.f;
-        for (int u = c.p_lo; u < a.G; ++u) x += c.scarry[(size_t)u * a.Bp + b];
+        for (int u = ga; u < a.G; ++u) x += c.scarry[(size_t)u * a.Bp + b];
         __stcg(a.carry + (size_t)blockIdx.x * a.Bp + b, x);
     }
     __syncwarp();
@@ -532,9 +537,9 @@ __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsi
 
 template <int THREADS, int NC, bool SMEMG, bool BWD>
 __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
-    constexpr int UNR = NC == 1 ? 8 : (NC == 2 ? 4 : 2);
+    constexpr int UNR = BWD ? (NC == 2 ? 4 : 2) : (NC == 2 ? 8 : 4);
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ int s_ok, s_meta[4];
+    __shared__ int s_ok, s_meta[8];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta = blockIdx.x;
@@ -545,38 +550,42 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     const int gam = warp * a.EPW + g;  // this lane's group in the CTA (if active)
 
     Cta c;
-    c.grp_r = reinterpret_cast<int *>(smem + a.o_grp);
-    c.grp_e = c.grp_r + (a.G + 1);
     c.srp = reinterpret_cast<int *>(smem + a.o_srp);
     c.prm = reinterpret_cast<float2 *>(smem + a.o_prm);
     c.sslot = reinterpret_cast<int *>(smem + a.o_slot);
-    c.head = reinterpret_cast<int *>(smem + a.o_head);
     c.scarry = reinterpret_cast<float *>(smem + a.o_carry);
     c.tile = reinterpret_cast<float *>(smem + a.o_tile);
-    c.scol = reinterpret_cast<int *>(smem + a.o_col);
-    c.sw = reinterpret_cast<float *>(smem + a.o_w);
+    c.scw = reinterpret_cast<int2 *>(smem + a.o_cw);
+    c.srow = reinterpret_cast<int *>(smem + a.o_row);
     c.sdw = reinterpret_cast<float *>(smem + a.o_dw);
 
-    // ---- pieces of the merge path, one per lane group
-    const long long items = (long long)N + a.E, nsub = (long long)a.P * a.G;
-    if (active && lig == 0) {
-        const long long gg = (long long)cta * a.G + gam;
-        const long long d0 = gg * items / nsub;
+    // ---- this CTA's piece of the merge path of (row ends, edges)
+    const long long items = (long long)N + a.E;
+    if (tid == 0) {
+        const long long d0 = (long long)cta * items / a.P;
+        const long long d1 = (long long)(cta + 1) * items / a.P;
         const int r0 = merge_search(a.row_ptr, N, d0);
-        c.grp_r[gam] = r0;
-        c.grp_e[gam] = (int)(d0 - r0);
-        if (gam == a.G - 1) {
-            const long long d1 = (gg + 1) * items / nsub;
-            const int r1 = merge_search(a.row_ptr, N, d1);
-            c.grp_r[a.G] = r1;
-            c.grp_e[a.G] = (int)(d1 - r1);
+        const int r1 = merge_search(a.row_ptr, N, d1);
+        s_meta[0] = r0;
+        s_meta[1] = r1 - r0;
+        s_meta[2] = (int)(d0 - r0);
+        s_meta[3] = (int)(d1 - r1);
+        // earlier CTAs whose carries reach this CTA's first row
+        int clo = cta;
+        if (cta > 0 && s_meta[2] > __ldg(a.row_ptr + r0)) {
+            clo = cta - 1;
+            while (clo > 0 && merge_search(a.row_ptr, N, (long long)clo * items / a.P) == r0) --clo;
         }
+        s_meta[4] = clo;
+        s_meta[5] = (cta + 1 < a.P && r1 < N) ? 1 : 0;
     }
     __syncthreads();
-    c.r0 = c.grp_r[0];
-    c.nrows = c.grp_r[a.G] - c.r0;
-    c.e0 = c.grp_e[0];
-    c.e1 = c.grp_e[a.G];
+    c.r0 = s_meta[0];
+    c.nrows = s_meta[1];
+    c.e0 = s_meta[2];
+    c.e1 = s_meta[3];
+    c.c_lo = s_meta[4];
+    c.publish = s_meta[5] != 0;
     c.rows = a.rs_smem ? reinterpret_cast<float *>(smem + a.o_rows) : a.rowsum_g + (size_t)c.r0 * Bp;
     if (c.nrows + 2 > a.rows_cap || (SMEMG && c.e1 - c.e0 > a.cap)) {
         if (tid == 0) atomicCAS(a.err, 0, kDevInternal);
@@ -587,12 +596,11 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         const int r = c.r0 + i;
         c.prm[i] = make_float2(__ldg(a.leak + r), BWD ? 0.f : __ldg(a.bias + r));
         c.sslot[i] = __ldg(a.slot + r);
-        c.head[i] = -1;
     }
     for (int k = c.e0 + tid; k < c.e1; k += THREADS) {
         if (SMEMG) {
-            c.scol[k - c.e0] = __ldg(a.col + k);
-            c.sw[k - c.e0] = __ldg(a.w + __ldg(a.perm + k));
+            c.scw[k - c.e0] = make_int2(__ldg(a.col + k), __float_as_int(__ldg(a.w + __ldg(a.perm + k))));
+            c.srow[k - c.e0] = __ldg(a.rowid + k);
             if (BWD) c.sdw[k - c.e0] = 0.f;
         } else if (a.do_prologue) {
             a.wperm[k] = __ldg(a.w + __ldg(a.perm + k));
@@ -600,30 +608,6 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         }
     }
     __syncthreads();
-    // rows whose partial sums arrive from earlier groups: the group finishing them
-    for (int u = tid; u < a.G; u += THREADS) {
-        const int r = c.grp_r[u];
-        if (r < c.grp_r[u + 1] && c.grp_e[u] > c.srp[r - c.r0]) c.head[r - c.r0] = u;
-    }
-    if (tid == 0) {
-        // earlier CTAs whose carries reach this CTA's first row
-        int clo = cta;
-        if (cta > 0 && c.grp_e[0] > c.srp[0]) {
-            clo = cta - 1;
-            while (clo > 0 && merge_search(a.row_ptr, N, (long long)clo * items / a.P) == c.r0) --clo;
-        }
-        s_meta[0] = clo;
-        // pieces whose carry belongs to the row this CTA's last piece ends inside
-        const int Rc = c.grp_r[a.G];
-        int plo = a.G - 1;
-        while (plo > 0 && c.grp_r[plo] == Rc) --plo;
-        s_meta[1] = plo;
-        s_meta[2] = (cta + 1 < a.P && Rc < N) ? 1 : 0;
-    }
-    __syncthreads();
-    c.c_lo = s_meta[0];
-    c.p_lo = s_meta[1];
-    c.publish = s_meta[2] != 0;
 
     unsigned nbar = 0;
     if (a.do_prologue) {
@@ -643,8 +627,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         const int s = BWD ? a.s_first - it : a.s_first + it;
         const unsigned phase_id = BWD ? (unsigned)(a.S - s) : (unsigned)(s + 1);
         const float *rows = BWD ? a.da + (size_t)(s & 1) * NBp : a.H + (size_t)s * NBp;
-        stream_piece<NC, SMEMG, BWD, UNR>(a, c, gam, g, lig, active, rows,
-                                          a.H + (size_t)s * NBp);
+        stream_piece<NC, SMEMG, BWD, UNR>(a, c, gam, lig, active, rows, a.H + (size_t)s * NBp);
         __syncthreads();
         if (warp == 0 && c.publish) publish_carry(a, c, phase_id);
         if (BWD) finish_bwd<THREADS>(a, c, s, phase_id);
@@ -673,11 +656,8 @@ using KernelFn = void (*)(const KArgs);
 
 template <int THREADS, bool BWD>
 KernelFn pick_nc(int nc, bool smem) {
-    switch (nc) {
-        case 1: return smem ? rec_kernel<THREADS, 1, true, BWD> : rec_kernel<THREADS, 1, false, BWD>;
-        case 2: return smem ? rec_kernel<THREADS, 2, true, BWD> : rec_kernel<THREADS, 2, false, BWD>;
-        default: return smem ? rec_kernel<THREADS, 4, true, BWD> : rec_kernel<THREADS, 4, false, BWD>;
-    }
+    if (nc == 2) return smem ? rec_kernel<THREADS, 2, true, BWD> : rec_kernel<THREADS, 2, false, BWD>;
+    return smem ? rec_kernel<THREADS, 4, true, BWD> : rec_kernel<THREADS, 4, false, BWD>;
 }
 
 KernelFn pick_kernel(int threads, int nc, bool smem, bool bwd) {
@@ -697,24 +677,23 @@ size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 // Shared-memory layout of one direction.
 SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_rows) {
     SmemLayout L;
+    std::memset(&L, 0, sizeof(L));
     size_t o = 0;
     const int rc = p.rows_cap[dir];
-    L.o_grp = (int)o; o = align16(o + 8 * (size_t)(p.groups + 1));
     L.o_srp = (int)o; o = align16(o + 4 * (size_t)rc);
     L.o_prm = (int)o; o = align16(o + 8 * (size_t)rc);
     L.o_slot = (int)o; o = align16(o + 4 * (size_t)rc);
-    L.o_head = (int)o; o = align16(o + 4 * (size_t)rc);
     L.o_carry = (int)o; o = align16(o + 4 * (size_t)p.groups * p.Bp);
     L.o_tile = (int)o; o = align16(o + 4 * 32 * 33);
     const size_t base = o;
     const size_t rows_b = 4 * (size_t)rc * p.Bp;
-    const size_t graph_b = (dir == 0 ? 8 : 12) * (size_t)p.cap[dir];
+    const size_t graph_b = (dir == 0 ? 12 : 16) * (size_t)p.cap[dir];
     const size_t budget = kMaxSmem - kStaticSmem - 1024;
     L.rows = want_rows && base + rows_b <= budget;
     L.graph = want_graph && base + (L.rows ? rows_b : 0) + graph_b <= budget;
     L.o_rows = (int)o; o = align16(o + (L.rows ? rows_b : 0));
-    L.o_col = (int)o; o = align16(o + (L.graph ? 4 * (size_t)p.cap[dir] : 0));
-    L.o_w = (int)o; o = align16(o + (L.graph ? 4 * (size_t)p.cap[dir] : 0));
+    L.o_cw = (int)o; o = align16(o + (L.graph ? 8 * (size_t)p.cap[dir] : 0));
+    L.o_row = (int)o; o = align16(o + (L.graph ? 4 * (size_t)p.cap[dir] : 0));
     L.o_dw = (int)o; o = align16(o + (L.graph && dir == 1 ? 4 * (size_t)p.cap[dir] : 0));
     L.bytes = o;
     return L;
@@ -739,16 +718,14 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.rows_cap = p.rows_cap[dir];
     const SmemLayout &L = dir == 0 ? p.lay_fwd : p.lay_bwd;
     k.rs_smem = L.rows ? 1 : 0;
-    k.o_grp = L.o_grp;
     k.o_srp = L.o_srp;
     k.o_prm = L.o_prm;
     k.o_slot = L.o_slot;
-    k.o_head = L.o_head;
     k.o_carry = L.o_carry;
     k.o_rows = L.o_rows;
     k.o_tile = L.o_tile;
-    k.o_col = L.o_col;
-    k.o_w = L.o_w;
+    k.o_cw = L.o_cw;
+    k.o_row = L.o_row;
     k.o_dw = L.o_dw;
     k.slot = g->slot;
     char *sc = (char *)scratch;
@@ -821,10 +798,10 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     q.E = (int)g->E;
     q.n_in = (int)g->n_in;
     q.B = (int)B;
-    q.Bp = (int)((B + 7) / 8 * 8);
-    q.NC = (q.Bp + 127) / 128;
-    if (q.NC == 3) q.NC = 4;  // three chunks run in the four-chunk kernel with masking
-    q.LPE = q.Bp <= 128 ? q.Bp / 4 : 32;
+    // a lane holds NC float4 chunks of a batch row; LPE lanes hold the row
+    q.Bp = (int)(B <= 256 ? (B + 7) / 8 * 8 : (B + 15) / 16 * 16);
+    q.NC = q.Bp <= 256 ? 2 : 4;
+    q.LPE = q.Bp / (4 * q.NC);
     q.EPW = 32 / q.LPE;
     q.T = (int)T;
     q.M = (int)M;
@@ -876,6 +853,7 @@ ck_status launch_forward(const ck_graph *g, const Plan &p, const FwdIO &io, cuda
     k.row_ptr = g->row_ptr;
     k.col = g->col;
     k.perm = g->perm;
+    k.rowid = g->rowid;
     k.w = io.w;
     k.leak = io.leak;
     k.bias = io.bias;
@@ -894,6 +872,7 @@ ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cud
     k.row_ptr = g->rowT_ptr;
     k.col = g->colT;
     k.perm = g->permT;
+    k.rowid = g->rowidT;
     k.w = io.w;
     k.leak = io.leak;
     k.H = const_cast<float *>(io.saved);
