@@ -300,7 +300,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
         }
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
-            if (rid[q] != cur) {
+            if (k + q < k1 && rid[q] != cur) {
                 flush(cur);
                 cur = rid[q];
             }
