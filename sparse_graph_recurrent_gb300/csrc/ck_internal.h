@@ -36,7 +36,7 @@ enum : int { kDevOk = 0, kDevTimeout = 1, kDevInternal = 2 };
 
 // Shared-memory layout of one direction's kernel (byte offsets).
 struct SmemLayout {
-    int o_srp, o_prm, o_slot, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;
+    int o_srp, o_prm, o_slot, o_grp, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;
     size_t bytes;
     bool graph;  // the CTA's slice of the graph lives in shared memory
     bool rows;   // row sums live in shared memory (else in global scratch)

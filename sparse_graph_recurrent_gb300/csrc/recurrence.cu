@@ -56,7 +56,7 @@ struct KArgs {
     int cap, rows_cap;      // edges / rows (+2) bounds per CTA, for shared memory
     int rs_smem;            // row sums in shared memory (else in global scratch)
     // dynamic shared memory layout (byte offsets)
-    int o_srp, o_prm, o_slot, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;
+    int o_srp, o_prm, o_slot, o_grp, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;
     const int *row_ptr, *col, *perm, *slot, *rowid;
     const float *w, *leak, *bias, *drives, *state0;
     float *out;
@@ -67,8 +67,8 @@ struct KArgs {
     float *G_, *da, *rowsum_g;
     unsigned *bar;
     int *err;
-    unsigned *flags;
-    float *carry, *wperm, *dwperm;
+    unsigned long long *carry;  // [P][Bp] {float bits, phase id} words
+    float *wperm, *dwperm;
     int s_first, s_count, do_prologue, do_epilogue;
     unsigned bar_base, bar_extra;
     unsigned long long timeout_ns;
@@ -81,11 +81,16 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
@@ -136,16 +141,24 @@ __device__ bool grid_sync(const KArgs &a, unsigned idx, int *s_ok) {
     return *s_ok != 0;
 }
 
-// Bounded wait for another CTA's carry flag (all lanes of a warp call it).
-__device__ __forceinline__ void wait_flag(const KArgs &a, const unsigned *f, unsigned want) {
-    const unsigned long long t0 = globaltimer();
-    while (ld_acquire(f) < want) {
-        if (ld_err(a.err) != 0) return;
-        if (globaltimer() - t0 > a.timeout_ns) {
-            atomicCAS(a.err, 0, kDevTimeout);
-            return;
-        }
+// Another CTA's published carry for column b: a 64-bit word whose high half
+// is the microstep's id, so the value and its validity arrive together (an
+// aligned 64-bit access is single-copy atomic).  Bounded wait.
+__device__ __forceinline__ float wait_carry(const KArgs &a, const unsigned long long *p,
+                                            unsigned phase_id) {
+    unsigned long long v = ld_relaxed64(p);
+    if ((unsigned)(v >> 32) != phase_id) {
+        const unsigned long long t0 = globaltimer();
+        do {
+            if (ld_err(a.err) != 0) return 0.f;
+            if (globaltimer() - t0 > a.timeout_ns) {
+                atomicCAS(a.err, 0, kDevTimeout);
+                return 0.f;
+            }
+            v = ld_relaxed64(p);
+        } while ((unsigned)(v >> 32) != phase_id);
     }
+    return __uint_as_float((unsigned)v);
 }
 
 // Merge-path split: the largest r in [0, min(d, N)] with row_ptr[r] + r <= d.
@@ -211,6 +224,7 @@ struct Cta {
     int *srp;       // row_ptr[r0 + i], i < nrows + 2 (clamped at N)
     float2 *prm;    // {leak, bias} of rows r0 + i
     int *sslot;     // slot of rows r0 + i
+    int *sgrp;      // groups [ga, gb) whose carries belong to row r0 + i, packed ga << 16 | gb
     float *scarry;  // [G][Bp]
     float *rows;    // [nrows][Bp] row slots (shared or global)
     float *tile;    // [32][33]
@@ -345,21 +359,23 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
 __device__ __forceinline__ float row_total(const KArgs &a, const Cta &c, int i, int b,
                                            unsigned phase_id, bool pro) {
     if (pro) return 0.f;
-    const int rs = c.srp[i], re = c.srp[i + 1];
+    const int gr = c.sgrp[i];
     float x = 0.f;
-    if (re > rs && re - 1 >= c.e0) {
+    if (gr >= 0) {
         x = a.rs_smem ? c.rows[(size_t)i * a.Bp + b] : __ldcg(c.rows + (size_t)i * a.Bp + b);
-        const int ga = group_of(c, a.G, rs > c.e0 ? rs : c.e0);
-        const int gb = group_of(c, a.G, re - 1);
-        for (int u = ga; u < gb; ++u) x += c.scarry[(size_t)u * a.Bp + b];
+        for (int u = gr >> 16, ue = gr & 0xffff; u < ue; ++u) x += c.scarry[(size_t)u * a.Bp + b];
     }
-    if (i == 0 && rs < c.e0) {
-        for (int cc = c.c_lo; cc < (int)blockIdx.x; ++cc) {
-            wait_flag(a, a.flags + cc, phase_id);
-            x += __ldcg(a.carry + (size_t)cc * a.Bp + b);
-        }
+    if (i == 0 && c.srp[0] < c.e0) {
+        for (int cc = c.c_lo; cc < (int)blockIdx.x; ++cc)
+            x += wait_carry(a, a.carry + (size_t)cc * a.Bp + b, phase_id);
     }
     return x;
+}
+
+// Ask L2 to fetch `bytes` from `p` (16-byte aligned, multiple of 16) ahead of use.
+__device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
+    if (bytes >= 16)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes & ~15u) : "memory");
 }
 
 // Forward finish of rows: pre-activation, tanh, leak blend, saved copies.
@@ -527,10 +543,9 @@ __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsi
     for (int b = lane; b < a.Bp; b += 32) {
         float x = 0.f;
         for (int u = ga; u < a.G; ++u) x += c.scarry[(size_t)u * a.Bp + b];
-        __stcg(a.carry + (size_t)blockIdx.x * a.Bp + b, x);
+        st_relaxed64(a.carry + (size_t)blockIdx.x * a.Bp + b,
+                     ((unsigned long long)phase_id << 32) | __float_as_uint(x));
     }
-    __syncwarp();
-    if (lane == 0) st_release(a.flags + blockIdx.x, phase_id);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -553,6 +568,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     c.srp = reinterpret_cast<int *>(smem + a.o_srp);
     c.prm = reinterpret_cast<float2 *>(smem + a.o_prm);
     c.sslot = reinterpret_cast<int *>(smem + a.o_slot);
+    c.sgrp = reinterpret_cast<int *>(smem + a.o_grp);
     c.scarry = reinterpret_cast<float *>(smem + a.o_carry);
     c.tile = reinterpret_cast<float *>(smem + a.o_tile);
     c.scw = reinterpret_cast<int2 *>(smem + a.o_cw);
@@ -596,6 +612,16 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         const int r = c.r0 + i;
         c.prm[i] = make_float2(__ldg(a.leak + r), BWD ? 0.f : __ldg(a.bias + r));
         c.sslot[i] = __ldg(a.slot + r);
+        // a row's last edge lies in this CTA iff it has edges here: then its slot
+        // holds the tail, and the groups holding its earlier edges carry the rest
+        const int rs = __ldg(a.row_ptr + r), re = __ldg(a.row_ptr + r + 1);
+        int gr = -1;
+        if (re > rs && re - 1 >= c.e0) {
+            const int ga = group_of(c, a.G, rs > c.e0 ? rs : c.e0);
+            const int gb = group_of(c, a.G, re - 1);
+            gr = (ga << 16) | gb;
+        }
+        c.sgrp[i] = gr;
     }
     for (int k = c.e0 + tid; k < c.e1; k += THREADS) {
         if (SMEMG) {
@@ -627,6 +653,21 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         const int s = BWD ? a.s_first - it : a.s_first + it;
         const unsigned phase_id = BWD ? (unsigned)(a.S - s) : (unsigned)(s + 1);
         const float *rows = BWD ? a.da + (size_t)(s & 1) * NBp : a.H + (size_t)s * NBp;
+        if (tid == 0 && c.nrows > 0) {
+            // part B's operands of this CTA's rows, fetched into L2 during part A
+            const unsigned rb = (unsigned)((size_t)c.nrows * Bp * 4);
+            const size_t ro = (size_t)c.r0 * Bp;
+            if (BWD) {
+                if (s > 0) {
+                    prefetch_l2(a.A + (size_t)(s - 1) * NBp + ro, rb);
+                    prefetch_l2(a.H + (size_t)(s - 1) * NBp + ro, rb);
+                    const int q = s - 1, tq = q / a.M;
+                    if (q - tq * a.M == a.M - 1) prefetch_l2(a.doutT + (size_t)tq * NBp + ro, rb);
+                }
+            } else {
+                prefetch_l2(a.H + (size_t)s * NBp + ro, rb);
+            }
+        }
         stream_piece<NC, SMEMG, BWD, UNR>(a, c, gam, lig, active, rows, a.H + (size_t)s * NBp);
         __syncthreads();
         if (warp == 0 && c.publish) publish_carry(a, c, phase_id);
@@ -683,6 +724,7 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_rows) 
     L.o_srp = (int)o; o = align16(o + 4 * (size_t)rc);
     L.o_prm = (int)o; o = align16(o + 8 * (size_t)rc);
     L.o_slot = (int)o; o = align16(o + 4 * (size_t)rc);
+    L.o_grp = (int)o; o = align16(o + 4 * (size_t)rc);
     L.o_carry = (int)o; o = align16(o + 4 * (size_t)p.groups * p.Bp);
     L.o_tile = (int)o; o = align16(o + 4 * 32 * 33);
     const size_t base = o;
@@ -721,6 +763,7 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.o_srp = L.o_srp;
     k.o_prm = L.o_prm;
     k.o_slot = L.o_slot;
+    k.o_grp = L.o_grp;
     k.o_carry = L.o_carry;
     k.o_rows = L.o_rows;
     k.o_tile = L.o_tile;
@@ -731,8 +774,7 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     char *sc = (char *)scratch;
     k.bar = (unsigned *)(sc + p.off_ctrl);
     k.err = (int *)(sc + p.off_ctrl + 4);
-    k.flags = (unsigned *)(sc + p.off_ctrl + 256);
-    k.carry = (float *)(sc + p.off_carry);
+    k.carry = (unsigned long long *)(sc + p.off_carry);
     k.wperm = (float *)(sc + p.off_wperm);
     k.dwperm = (float *)(sc + p.off_dwperm);
     k.G_ = (float *)(sc + p.off_G);
@@ -755,7 +797,8 @@ ck_status launch_all(KArgs &k, const Plan &p, bool bwd, cudaStream_t s, int64_t 
     if (per_sm < 1)
         return fail(CK_ERR_UNSUPPORTED, "kernel does not fit on an SM (%d threads, %zu B shared)",
                     p.threads, L.bytes);
-    e = cudaMemsetAsync((char *)k.bar, 0, p.ctrl_bytes, s);
+    // barrier counter, status word and published carries start at zero
+    e = cudaMemsetAsync((char *)k.bar, 0, p.off_carry - p.off_ctrl + 8 * (size_t)p.P * p.Bp, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (control words)");
     int64_t n = 0;
     const bool persistent = options().persistent != 0;
@@ -824,10 +867,10 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     const size_t E1 = (size_t)(q.E > 0 ? q.E : 1);
     size_t off = 0;
     q.off_ctrl = off;
-    q.ctrl_bytes = align256(256 + 4 * (size_t)q.P);
+    q.ctrl_bytes = 256;
     off += q.ctrl_bytes;
     q.off_carry = off;
-    off = align256(off + 4 * (size_t)q.P * q.Bp);
+    off = align256(off + 8 * (size_t)q.P * q.Bp);
     q.off_wperm = off;
     off = align256(off + 4 * E1);
     q.off_dwperm = off;
