@@ -178,9 +178,8 @@ typedef enum {
     CK_OPT_BARRIER_TIMEOUT_NS = 1,  /* bound on any device-side wait (default 4e9 ns) */
     CK_OPT_TEST_BARRIER_EXTRA = 2,  /* test hook: barriers wait for this many extra arrivals
                                        that never come, so every wait runs out (default 0) */
-    CK_OPT_GRAPH_IN_SMEM = 3,       /* 1 (default): keep each CTA's slice of the graph in
+    CK_OPT_GRAPH_IN_SMEM = 3        /* 1 (default): keep each CTA's slice of the graph in
                                        shared memory when it fits; 0: always stream it */
-    CK_OPT_THREADS = 4              /* threads per CTA: 512 (default) or 1024 */
 } ck_option;
 
 ck_status ck_set_option(ck_option opt, int64_t value);

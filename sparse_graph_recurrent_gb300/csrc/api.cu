@@ -84,10 +84,6 @@ ck_status ck_set_option(ck_option opt, int64_t v) {
             o.barrier_extra = (int)v;
             return CK_OK;
         case CK_OPT_GRAPH_IN_SMEM: o.graph_in_smem = v != 0; return CK_OK;
-        case CK_OPT_THREADS:
-            if (v != 512 && v != 1024) return fail(CK_ERR_INVALID_ARG, "threads must be 512 or 1024");
-            o.threads = (int)v;
-            return CK_OK;
     }
     return fail(CK_ERR_INVALID_ARG, "unknown option %d", (int)opt);
 }
@@ -99,7 +95,6 @@ int64_t ck_get_option(ck_option opt) {
         case CK_OPT_BARRIER_TIMEOUT_NS: return o.timeout_ns;
         case CK_OPT_TEST_BARRIER_EXTRA: return o.barrier_extra;
         case CK_OPT_GRAPH_IN_SMEM: return o.graph_in_smem;
-        case CK_OPT_THREADS: return o.threads;
     }
     return -1;
 }

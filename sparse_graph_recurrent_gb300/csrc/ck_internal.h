@@ -40,6 +40,8 @@ struct SmemLayout {
     size_t bytes;
     bool graph;  // the CTA's slice of the graph lives in shared memory
     bool rows;   // row sums live in shared memory (else in global scratch)
+    bool stage;  // finish operands staged in shared memory
+    int o_st0, o_st1, o_st2, o_st3, o_inp, o_acc;
 };
 
 // Launch description of one ck_forward / ck_backward call (recurrence.cu).
@@ -71,7 +73,6 @@ struct Options {
     long long timeout_ns = 4000000000LL;
     int barrier_extra = 0;
     int graph_in_smem = 1;
-    int threads = 512;
 };
 Options &options();
 

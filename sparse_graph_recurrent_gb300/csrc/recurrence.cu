@@ -49,6 +49,7 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kStaticSmem = 64;
+constexpr int kThreads = 512;
 
 struct KArgs {
     int N, E, n_in, B, Bp, LPE, EPW, LPE_P2, T, M, S;
@@ -57,6 +58,8 @@ struct KArgs {
     int rs_smem;            // row sums in shared memory (else in global scratch)
     // dynamic shared memory layout (byte offsets)
     int o_srp, o_prm, o_slot, o_grp, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;
+    int stage;  // finish operands staged in shared memory (see Cta)
+    int o_st0, o_st1, o_st2, o_st3, o_inp, o_acc;
     const int *row_ptr, *col, *perm, *slot, *rowid;
     const float *w, *leak, *bias, *drives, *state0;
     float *out;
@@ -231,9 +234,37 @@ struct Cta {
     int2 *scw;      // {col, bits of w} of the CTA's edges
     int *srow;      // row of the CTA's edges
     float *sdw;     // edge-gradient accumulators of the CTA's edges
+    // Staged finish operands (stage mode), rows r0 + i:
+    //   forward:  st0 = current state (resident across microsteps), st1 = drives
+    //             of the CTA's input rows for the current input step (row inp[i])
+    //   backward: st0 = G (resident), st1 = A[q], st2 = H[q], st3 = dOut[t(q)],
+    //             acc = {d_leak, d_bias} running sums (resident)
+    float *st0, *st1, *st2, *st3;
+    int *inp;
+    float2 *acc;
+    bool stage;
+    int n_inp;
     int r0, nrows, e0, e1, c_lo;
     bool publish;
 };
+
+__device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(sdst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *sdst, const void *gsrc) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(sdst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Copy this CTA's rows [r0, r0 + nrows) of a node-major array into shared memory.
+template <int THREADS>
+__device__ __forceinline__ void stage_rows(float *sdst, const float *gsrc, int nrows, int Bp) {
+    const int n16 = nrows * Bp / 4;
+    for (int j = threadIdx.x; j < n16; j += THREADS) cp_async16(sdst + 4 * j, gsrc + 4 * j);
+}
 
 // The lane group whose edge sub-range holds edge k of the CTA (n = e1 - e0 > 0).
 __device__ __forceinline__ int group_of(const Cta &c, int G, int k) {
@@ -408,9 +439,16 @@ __device__ void finish_fwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
                 x[el] = hp[el] = dr[el] = 0.f;
                 if (ok[el]) {
                     const int r = c.r0 + i;
-                    hp[el] = __ldcg(hin + (size_t)r * Bp + b);
-                    const int sl = c.sslot[i];
-                    if (sl >= 0 && b < B) dr[el] = __ldg(a.drives + ((size_t)t * a.n_in + sl) * B + b);
+                    if (c.stage) {
+                        hp[el] = c.st0[(size_t)i * Bp + b];
+                        const int j = c.inp[i];
+                        if (j >= 0 && b < B) dr[el] = c.st1[(size_t)j * Bp + b];
+                    } else {
+                        hp[el] = __ldcg(hin + (size_t)r * Bp + b);
+                        const int sl = c.sslot[i];
+                        if (sl >= 0 && b < B)
+                            dr[el] = __ldg(a.drives + ((size_t)t * a.n_in + sl) * B + b);
+                    }
                 }
             }
 #pragma unroll
@@ -428,6 +466,7 @@ __device__ void finish_fwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
                 float av = x[el] + pr.y + dr[el], hv = 0.f;
                 if (b < B) hv = fmaf(pr.x, tanhf(av), (1.f - pr.x) * hp[el]);
                 else av = 0.f;
+                if (c.stage) c.st0[(size_t)i * Bp + b] = hv;
                 hout[(size_t)r * Bp + b] = hv;
                 __stcs(aout + (size_t)r * Bp + b, av);
             }
@@ -471,7 +510,15 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
                 irow[el] = i;
                 bcol[el] = b;
                 x[el] = gv[el] = ov[el] = av[el] = hv[el] = 0.f;
-                if (ok[el]) {
+                if (ok[el] && c.stage) {
+                    const size_t o = (size_t)i * Bp + b;
+                    if (!pro) gv[el] = c.st0[o];
+                    if (step_end) ov[el] = c.st3[o];
+                    if (q >= 0) {
+                        av[el] = c.st1[o];
+                        hv[el] = c.st2[o];
+                    }
+                } else if (ok[el]) {
                     const size_t o = (size_t)(c.r0 + i) * Bp + b;
                     if (!pro) gv[el] = __ldcg(a.G_ + o);
                     if (step_end) ov[el] = __ldcg(dO + o);
@@ -495,7 +542,8 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
                 const float lam = c.prm[i].x;
                 float gn = fmaf(gv[el], 1.f - lam, x[el]) + ov[el];
                 if (b >= B) gn = 0.f;
-                a.G_[o] = gn;
+                if (c.stage) c.st0[(size_t)i * Bp + b] = gn;
+                else a.G_[o] = gn;
                 if (q < 0) continue;
                 float d = 0.f;
                 if (b < B) {
@@ -521,7 +569,10 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
                 const float sl = warp_sum(dl[ri]), sb = warp_sum(db[ri]);
                 if (lane == 0) {
                     const int r = c.r0 + i;
-                    if (q == a.S - 1) {
+                    if (c.stage) {
+                        const float2 o = q == a.S - 1 ? make_float2(0.f, 0.f) : c.acc[i];
+                        c.acc[i] = make_float2(o.x + sl, o.y + sb);
+                    } else if (q == a.S - 1) {
                         a.dleak[r] = sl;
                         a.dbias[r] = sb;
                     } else {
@@ -574,6 +625,13 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     c.scw = reinterpret_cast<int2 *>(smem + a.o_cw);
     c.srow = reinterpret_cast<int *>(smem + a.o_row);
     c.sdw = reinterpret_cast<float *>(smem + a.o_dw);
+    c.stage = a.stage != 0;
+    c.st0 = reinterpret_cast<float *>(smem + a.o_st0);
+    c.st1 = reinterpret_cast<float *>(smem + a.o_st1);
+    c.st2 = reinterpret_cast<float *>(smem + a.o_st2);
+    c.st3 = reinterpret_cast<float *>(smem + a.o_st3);
+    c.inp = reinterpret_cast<int *>(smem + a.o_inp);
+    c.acc = reinterpret_cast<float2 *>(smem + a.o_acc);
 
     // ---- this CTA's piece of the merge path of (row ends, edges)
     const long long items = (long long)N + a.E;
@@ -634,15 +692,36 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         }
     }
     __syncthreads();
+    if (c.stage && !BWD) {
+        // index of each input row among this CTA's input rows (their drives are staged)
+        if (tid == 0) {
+            int n = 0;
+            for (int i = 0; i < c.nrows; ++i) c.inp[i] = c.sslot[i] >= 0 ? n++ : -1;
+            s_meta[6] = n;
+        }
+        __syncthreads();
+    }
+    c.n_inp = (c.stage && !BWD) ? s_meta[6] : 0;
 
     unsigned nbar = 0;
     if (a.do_prologue) {
         if (!BWD) {
             to_rows<THREADS>(a.H, a.state0, c.r0, c.r0 + c.nrows, a.B, Bp, N, c.tile);
+            if (c.stage) {
+                for (int j = tid; j < c.nrows * Bp; j += THREADS)
+                    c.st0[j] = __ldcg(a.H + (size_t)c.r0 * Bp + j);
+            }
         } else {
             for (int t = 0; t < a.T; ++t)
                 to_rows<THREADS>(a.doutT + (size_t)t * NBp, a.dout + (size_t)t * a.B * N, c.r0,
                                  c.r0 + c.nrows, a.B, Bp, N, c.tile);
+            if (c.stage) {
+                const size_t ro = (size_t)c.r0 * Bp;
+                stage_rows<THREADS>(c.st1, a.A + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
+                stage_rows<THREADS>(c.st2, a.H + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
+                stage_rows<THREADS>(c.st3, a.doutT + (size_t)(a.T - 1) * NBp + ro, c.nrows, Bp);
+                cp_async_wait_all();
+            }
             __syncthreads();
             finish_bwd<THREADS>(a, c, a.S, 0u);
         }
@@ -653,7 +732,27 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         const int s = BWD ? a.s_first - it : a.s_first + it;
         const unsigned phase_id = BWD ? (unsigned)(a.S - s) : (unsigned)(s + 1);
         const float *rows = BWD ? a.da + (size_t)(s & 1) * NBp : a.H + (size_t)s * NBp;
-        if (tid == 0 && c.nrows > 0) {
+        if (c.stage) {
+            // part B's operands copied into shared memory while part A runs
+            const size_t ro = (size_t)c.r0 * Bp;
+            if (BWD && s > 0) {
+                const int q = s - 1, tq = q / a.M;
+                stage_rows<THREADS>(c.st1, a.A + (size_t)q * NBp + ro, c.nrows, Bp);
+                stage_rows<THREADS>(c.st2, a.H + (size_t)q * NBp + ro, c.nrows, Bp);
+                if (q - tq * a.M == a.M - 1)
+                    stage_rows<THREADS>(c.st3, a.doutT + (size_t)tq * NBp + ro, c.nrows, Bp);
+            } else if (!BWD && c.n_inp > 0 && s % a.M == 0) {
+                const int t = s / a.M;
+                for (int j = tid; j < c.nrows * a.B; j += THREADS) {
+                    const int i = j / a.B, b = j - i * a.B;
+                    const int ii = c.inp[i];
+                    if (ii >= 0)
+                        cp_async4(c.st1 + (size_t)ii * Bp + b,
+                                  a.drives + ((size_t)t * a.n_in + c.sslot[i]) * a.B + b);
+                }
+            }
+            cp_async_commit();
+        } else if (tid == 0 && c.nrows > 0) {
             // part B's operands of this CTA's rows, fetched into L2 during part A
             const unsigned rb = (unsigned)((size_t)c.nrows * Bp * 4);
             const size_t ro = (size_t)c.r0 * Bp;
@@ -669,6 +768,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
             }
         }
         stream_piece<NC, SMEMG, BWD, UNR>(a, c, gam, lig, active, rows, a.H + (size_t)s * NBp);
+        if (c.stage) cp_async_wait_all();
         __syncthreads();
         if (warp == 0 && c.publish) publish_carry(a, c, phase_id);
         if (BWD) finish_bwd<THREADS>(a, c, s, phase_id);
@@ -684,6 +784,14 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
                 from_rows<THREADS>(a.out + (size_t)t * a.B * N, a.H + (size_t)(t + 1) * a.M * NBp,
                                    c.r0, c.r0 + c.nrows, a.B, Bp, N, c.tile);
         } else {
+            if (c.stage) {
+                for (int j = tid; j < c.nrows * Bp; j += THREADS) a.G_[(size_t)c.r0 * Bp + j] = c.st0[j];
+                for (int i = tid; i < c.nrows; i += THREADS) {
+                    a.dleak[c.r0 + i] = c.acc[i].x;
+                    a.dbias[c.r0 + i] = c.acc[i].y;
+                }
+                __syncthreads();
+            }
             from_rows<THREADS>(a.dstate0, a.G_, c.r0, c.r0 + c.nrows, a.B, Bp, N, c.tile);
             for (int k = c.e0 + tid; k < c.e1; k += THREADS)
                 a.dw[__ldg(a.perm + k)] = SMEMG ? c.sdw[k - c.e0] : a.dwperm[k];
@@ -701,9 +809,8 @@ KernelFn pick_nc(int nc, bool smem) {
     return smem ? rec_kernel<THREADS, 4, true, BWD> : rec_kernel<THREADS, 4, false, BWD>;
 }
 
-KernelFn pick_kernel(int threads, int nc, bool smem, bool bwd) {
-    if (threads == 1024) return bwd ? pick_nc<1024, true>(nc, smem) : pick_nc<1024, false>(nc, smem);
-    return bwd ? pick_nc<512, true>(nc, smem) : pick_nc<512, false>(nc, smem);
+KernelFn pick_kernel(int nc, bool smem, bool bwd) {
+    return bwd ? pick_nc<kThreads, true>(nc, smem) : pick_nc<kThreads, false>(nc, smem);
 }
 
 int pow2ceil(int x) {
@@ -716,7 +823,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
 // Shared-memory layout of one direction.
-SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_rows) {
+SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage) {
     SmemLayout L;
     std::memset(&L, 0, sizeof(L));
     size_t o = 0;
@@ -727,16 +834,26 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_rows) 
     L.o_grp = (int)o; o = align16(o + 4 * (size_t)rc);
     L.o_carry = (int)o; o = align16(o + 4 * (size_t)p.groups * p.Bp);
     L.o_tile = (int)o; o = align16(o + 4 * 32 * 33);
-    const size_t base = o;
-    const size_t rows_b = 4 * (size_t)rc * p.Bp;
-    const size_t graph_b = (dir == 0 ? 12 : 16) * (size_t)p.cap[dir];
     const size_t budget = kMaxSmem - kStaticSmem - 1024;
-    L.rows = want_rows && base + rows_b <= budget;
-    L.graph = want_graph && base + (L.rows ? rows_b : 0) + graph_b <= budget;
-    L.o_rows = (int)o; o = align16(o + (L.rows ? rows_b : 0));
+    const size_t rows_b = align16(4 * (size_t)rc * p.Bp);
+    const size_t graph_b = (dir == 0 ? 12 : 16) * (size_t)p.cap[dir] + 48;
+    // finish operands: forward state + drives; backward G, A, H, dOut + two sums
+    const size_t stage_b = (dir == 0 ? 2 : 4) * rows_b + align16(8 * (size_t)rc) + align16(4 * (size_t)rc);
+    L.rows = o + rows_b <= budget;
+    if (L.rows) o += rows_b;
+    L.o_rows = (int)(o - (L.rows ? rows_b : 0));
+    L.graph = want_graph && o + graph_b <= budget;
     L.o_cw = (int)o; o = align16(o + (L.graph ? 8 * (size_t)p.cap[dir] : 0));
     L.o_row = (int)o; o = align16(o + (L.graph ? 4 * (size_t)p.cap[dir] : 0));
     L.o_dw = (int)o; o = align16(o + (L.graph && dir == 1 ? 4 * (size_t)p.cap[dir] : 0));
+    L.stage = want_stage && o + stage_b <= budget;
+    const size_t sb = L.stage ? rows_b : 0;
+    L.o_st0 = (int)o; o += sb;
+    L.o_st1 = (int)o; o += sb;
+    L.o_st2 = (int)o; o += dir == 1 ? sb : 0;
+    L.o_st3 = (int)o; o += dir == 1 ? sb : 0;
+    L.o_acc = (int)o; o = align16(o + (L.stage ? 8 * (size_t)rc : 0));
+    L.o_inp = (int)o; o = align16(o + (L.stage ? 4 * (size_t)rc : 0));
     L.bytes = o;
     return L;
 }
@@ -770,6 +887,13 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.o_cw = L.o_cw;
     k.o_row = L.o_row;
     k.o_dw = L.o_dw;
+    k.stage = L.stage ? 1 : 0;
+    k.o_st0 = L.o_st0;
+    k.o_st1 = L.o_st1;
+    k.o_st2 = L.o_st2;
+    k.o_st3 = L.o_st3;
+    k.o_inp = L.o_inp;
+    k.o_acc = L.o_acc;
     k.slot = g->slot;
     char *sc = (char *)scratch;
     k.bar = (unsigned *)(sc + p.off_ctrl);
@@ -787,7 +911,7 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
 
 ck_status launch_all(KArgs &k, const Plan &p, bool bwd, cudaStream_t s, int64_t *launches) {
     const SmemLayout &L = bwd ? p.lay_bwd : p.lay_fwd;
-    KernelFn fn = pick_kernel(p.threads, p.NC, L.graph, bwd);
+    KernelFn fn = pick_kernel(p.NC, L.graph, bwd);
     cudaError_t e = cudaFuncSetAttribute((const void *)fn,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
@@ -850,7 +974,7 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     q.M = (int)M;
     q.S = (int)(T * M);
     q.P = g->num_sms;
-    q.threads = options().threads == 1024 ? 1024 : 512;
+    q.threads = kThreads;
     q.warps = q.threads / 32;
     q.groups = q.warps * q.EPW;
     for (int d = 0; d < 2; ++d) {
@@ -858,8 +982,9 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
         q.rows_cap[d] = g->max_rows[d] + 3;
     }
     const bool want_graph = options().graph_in_smem && options().persistent;
-    q.lay_fwd = smem_layout(q, 0, want_graph, true);
-    q.lay_bwd = smem_layout(q, 1, want_graph, true);
+    const bool want_stage = options().persistent != 0;
+    q.lay_fwd = smem_layout(q, 0, want_graph, want_stage);
+    q.lay_bwd = smem_layout(q, 1, want_graph, want_stage);
     if (q.lay_fwd.bytes > (size_t)(kMaxSmem - kStaticSmem) ||
         q.lay_bwd.bytes > (size_t)(kMaxSmem - kStaticSmem))
         return fail(CK_ERR_UNSUPPORTED, "per-CTA tables exceed shared memory (rows per SM too many)");

@@ -42,13 +42,17 @@ def test_status_strings(lib):
 def test_options_validate(lib):
     from sparse_graph_recurrent_gb300 import _ck
     assert _ck.ck_get_option(_ck.OPT_PERSISTENT) == 1
-    assert _ck.ck_get_option(_ck.OPT_THREADS) == 512
+    assert _ck.ck_get_option(_ck.OPT_GRAPH_IN_SMEM) == 1
     with pytest.raises(_ck.CKError) as e:
-        _ck.ck_set_option(_ck.OPT_THREADS, 300)
-    assert e.value.name == "CK_ERR_INVALID_ARG"
-    with pytest.raises(_ck.CKError):
         _ck.ck_set_option(_ck.OPT_BARRIER_TIMEOUT_NS, 10)
-    assert _ck.ck_get_option(_ck.OPT_THREADS) == 512
+    assert e.value.name == "CK_ERR_INVALID_ARG"
+    with pytest.raises(_ck.CKError) as e:
+        _ck.ck_set_option(_ck.OPT_TEST_BARRIER_EXTRA, -1)
+    assert e.value.name == "CK_ERR_INVALID_ARG"
+    with pytest.raises(_ck.CKError) as e:
+        _ck.ck_set_option(17, 1)
+    assert e.value.name == "CK_ERR_INVALID_ARG"
+    assert _ck.ck_get_option(_ck.OPT_BARRIER_TIMEOUT_NS) == 4_000_000_000
 
 
 def test_graph_create_rejects_bad_sizes_before_cuda(lib):
