@@ -276,8 +276,45 @@ __device__ __forceinline__ int group_of(const Cta &c, int G, int k) {
 // ------------------------------------------------------------ part A
 
 // Walk this lane group's edges: gather rows[col[k]] * w[k] into per-row sums.
-// Backward: also add each edge's dot product with the state h_{s-1} of its
-// source row into the edge-gradient accumulator.
+// Batches of UNR edges are double-buffered: the gathers of the next batch are
+// in flight while the current one is summed.  Backward: also add each edge's
+// dot product with the state h_{s-1} of its source row into the edge-gradient
+// accumulator; that source row stays in registers, and the next row's is
+// fetched as soon as the current one starts.
+template <int NC, int UNR>
+struct Batch {
+    int rid[UNR];
+    float w[UNR];
+    float4 v[UNR][NC];
+};
+
+// Sum of d over the LPE lanes of each group.  With LPE == UNR (a power of two)
+// one exchange per halving leaves lane lig holding the total of item lig;
+// otherwise each item is reduced by a tree and lane 0 holds it.
+template <int UNR>
+__device__ __forceinline__ void group_dots(float (&d)[UNR], int lig, int lpe, int lpe_p2) {
+    if (lpe == UNR && (UNR & (UNR - 1)) == 0) {
+#pragma unroll
+        for (int o = UNR / 2; o >= 1; o >>= 1) {
+#pragma unroll
+            for (int j = 0; j < o; ++j) {
+                const bool hi = (lig & o) != 0;
+                const float keep = hi ? d[j + o] : d[j];
+                const float send = hi ? d[j] : d[j + o];
+                d[j] = keep + __shfl_xor_sync(kFull, send, o);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < UNR; ++q) {
+            for (int o = lpe_p2 >> 1; o >= 1; o >>= 1) {
+                const float y = __shfl_down_sync(kFull, d[q], o);
+                if (lig + o < lpe) d[q] += y;
+            }
+        }
+    }
+}
+
 template <int NC, bool SMEMG, bool BWD, int UNR>
 __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int gam, int lig,
                                              bool active, const float *__restrict__ rows,
@@ -291,11 +328,31 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     }
     const int len = k1 - k0;
     const int trips = (__reduce_max_sync(kFull, (unsigned)len) + UNR - 1) / UNR;
-    int cur = -1;
-    if (len > 0) cur = SMEMG ? c.srow[k0 - c.e0] : __ldg(a.rowid + k0);
+    auto row_at = [&](int k) -> int { return SMEMG ? c.srow[k - c.e0] : __ldg(a.rowid + k); };
+    int cur = len > 0 ? row_at(k0) : -1;
     float4 acc[NC];
 #pragma unroll
     for (int ch = 0; ch < NC; ++ch) acc[ch] = zero4();
+
+    // backward: own-row state of the current and the next source row
+    float4 hcur[BWD ? NC : 1], hnext[BWD ? NC : 1];
+    int nxt = -1;
+    auto load_h = [&](float4(&h)[BWD ? NC : 1], int row) {
+        const float *hp = hprev + (size_t)(row < 0 ? 0 : row) * Bp + lig * 4;
+#pragma unroll
+        for (int ch = 0; ch < (BWD ? NC : 1); ++ch)
+            h[ch] = row >= 0 ? __ldg(reinterpret_cast<const float4 *>(hp + ch * CW)) : zero4();
+    };
+    auto next_row = [&](int row) -> int {  // the row after `row` that has edges in [k0, k1)
+        const int pos = c.srp[row - c.r0 + 1];
+        return pos < k1 ? row_at(pos) : -1;
+    };
+    if (BWD) {
+        load_h(hcur, cur);
+        nxt = cur >= 0 ? next_row(cur) : -1;
+        load_h(hnext, nxt);
+    }
+
     auto flush = [&](int row) {
         const int i = row - c.r0;
         if (i >= 0 && i < c.nrows) {
@@ -308,65 +365,89 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
 #pragma unroll
         for (int ch = 0; ch < NC; ++ch) acc[ch] = zero4();
     };
-    int k = k0;
-    for (int it = 0; it < trips; ++it, k += UNR) {
-        int rid[UNR];
-        float wq[UNR];
-        float4 v[UNR][NC];
-        float4 hq[BWD ? UNR : 1][NC];
+    auto load = [&](Batch<NC, UNR> &bt, int kb) {
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
-            const int kk = k + q;
+            const int kk = kb + q;
             const bool ok = kk < k1;
             int cc = 0;
-            rid[q] = cur;
-            wq[q] = 0.f;
+            bt.rid[q] = -2;
+            bt.w[q] = 0.f;
             if (ok) {
                 if (SMEMG) {
                     const int2 cw = c.scw[kk - c.e0];
                     cc = cw.x;
-                    wq[q] = __int_as_float(cw.y);
-                    rid[q] = c.srow[kk - c.e0];
+                    bt.w[q] = __int_as_float(cw.y);
+                    bt.rid[q] = c.srow[kk - c.e0];
                 } else {
                     cc = __ldg(a.col + kk);
-                    wq[q] = __ldcg(a.wperm + kk);
-                    rid[q] = __ldg(a.rowid + kk);
+                    bt.w[q] = __ldcg(a.wperm + kk);
+                    bt.rid[q] = __ldg(a.rowid + kk);
                 }
             }
             const float *rp = rows + (size_t)cc * Bp + lig * 4;
-            const float *hp = hprev + (size_t)rid[q] * Bp + lig * 4;
 #pragma unroll
-            for (int ch = 0; ch < NC; ++ch) {
-                v[q][ch] = ok ? __ldcg(reinterpret_cast<const float4 *>(rp + ch * CW)) : zero4();
-                if (BWD)
-                    hq[BWD ? q : 0][ch] =
-                        ok ? __ldg(reinterpret_cast<const float4 *>(hp + ch * CW)) : zero4();
-            }
+            for (int ch = 0; ch < NC; ++ch)
+                bt.v[q][ch] = ok ? __ldca(reinterpret_cast<const float4 *>(rp + ch * CW)) : zero4();
         }
+    };
+    auto consume = [&](const Batch<NC, UNR> &bt, int kb) {
+        float d[UNR];
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
-            if (k + q < k1 && rid[q] != cur) {
+            d[q] = 0.f;
+            if (bt.rid[q] != -2 && bt.rid[q] != cur) {
                 flush(cur);
-                cur = rid[q];
+                cur = bt.rid[q];
+                if (BWD) {
+                    if (cur == nxt) {
+#pragma unroll
+                        for (int ch = 0; ch < (BWD ? NC : 1); ++ch) hcur[ch] = hnext[ch];
+                    } else {
+                        load_h(hcur, cur);
+                    }
+                    nxt = next_row(cur);
+                    load_h(hnext, nxt);
+                }
             }
 #pragma unroll
-            for (int ch = 0; ch < NC; ++ch) fma4(acc[ch], wq[q], v[q][ch]);
+            for (int ch = 0; ch < NC; ++ch) fma4(acc[ch], bt.w[q], bt.v[q][ch]);
+            if (BWD) {
+#pragma unroll
+                for (int ch = 0; ch < NC; ++ch) d[q] = dot4(bt.v[q][ch], hcur[BWD ? ch : 0], d[q]);
+            }
         }
         if (BWD) {
-#pragma unroll
-            for (int q = 0; q < UNR; ++q) {
-                float d = 0.f;
-#pragma unroll
-                for (int ch = 0; ch < NC; ++ch) d = dot4(v[q][ch], hq[BWD ? q : 0][ch], d);
-                for (int o = a.LPE_P2 >> 1; o >= 1; o >>= 1) {
-                    const float y = __shfl_down_sync(kFull, d, o);
-                    if (lig + o < a.LPE) d += y;
+            group_dots<UNR>(d, lig, a.LPE, a.LPE_P2);
+            if (a.LPE == UNR && (UNR & (UNR - 1)) == 0) {
+                const int kk = kb + lig;
+                if (kk < k1) {
+                    if (SMEMG) c.sdw[kk - c.e0] += d[0];
+                    else a.dwperm[kk] += d[0];
                 }
-                if (lig == 0 && k + q < k1) {
-                    if (SMEMG) c.sdw[k + q - c.e0] += d;
-                    else a.dwperm[k + q] += d;
+            } else if (lig == 0) {
+#pragma unroll
+                for (int q = 0; q < UNR; ++q) {
+                    const int kk = kb + q;
+                    if (kk < k1) {
+                        if (SMEMG) c.sdw[kk - c.e0] += d[q];
+                        else a.dwperm[kk] += d[q];
+                    }
                 }
             }
+        }
+    };
+
+    Batch<NC, UNR> b0, b1;
+    if (trips > 0) load(b0, k0);
+    for (int it = 0; it < trips; it += 2) {
+        const int kb0 = k0 + it * UNR, kb1 = kb0 + UNR;
+        const bool two = it + 1 < trips;
+        if (two) load(b1, kb1);
+        consume(b0, kb0);
+        if (two) {
+            if (it + 2 < trips) load(b0, kb1 + UNR);
+            consume(b1, kb1);
         }
     }
     if (active) {
@@ -603,7 +684,7 @@ __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsi
 
 template <int THREADS, int NC, bool SMEMG, bool BWD>
 __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
-    constexpr int UNR = BWD ? (NC == 2 ? 4 : 2) : (NC == 2 ? 8 : 4);
+    constexpr int UNR = BWD ? (NC == 2 ? 4 : 2) : (NC == 2 ? 4 : 2);
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_ok, s_meta[8];
 
