@@ -245,7 +245,7 @@ ck_status ck_query_status(const void *scratch, void *stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "pending CUDA error");
     int word = 0;
-    e = cudaMemcpy(&word, (const char *)scratch + 4, sizeof(int), cudaMemcpyDeviceToHost);
+    e = cudaMemcpy(&word, (const char *)scratch + kStatusOffset, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy (status word)");
     if (word == kDevTimeout) return fail(CK_ERR_TIMEOUT, "a device-side wait timed out");
     if (word != kDevOk) return fail(CK_ERR_INTERNAL, "device status word %d", word);

@@ -34,6 +34,12 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
 // Device-side status words written by the recurrence kernels.
 enum : int { kDevOk = 0, kDevTimeout = 1, kDevInternal = 2 };
 
+// Control block at the start of scratch: the barrier's top counter, its group
+// counters (one 128-byte line each), then the status word.
+constexpr int kBarGroups = 8;
+constexpr size_t kStatusOffset = 4 * 32 * (1 + kBarGroups);
+constexpr size_t kCtrlBytes = 4 * 32 * (2 + kBarGroups);
+
 // Shared-memory layout of one direction's kernel (byte offsets).
 struct SmemLayout {
     int o_srp, o_prm, o_slot, o_grp, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;

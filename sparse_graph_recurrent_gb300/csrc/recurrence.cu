@@ -121,16 +121,27 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Grid-wide barrier, bounded by a.timeout_ns.  Returns false for the whole
-// CTA once any CTA has recorded an error, so every CTA leaves together.
+// Grid-wide barrier, bounded by a.timeout_ns.  Two levels, so few arrivals
+// meet on any one address: CTA c adds to the counter of group c % kBarGroups;
+// the last arrival of a group adds to the top counter, which every CTA polls.
+// Counters only grow within a call, so barrier idx waits for known totals.
+// Returns false for the whole CTA once any CTA has recorded an error, so every
+// CTA leaves together.
 __device__ bool grid_sync(const KArgs &a, unsigned idx, int *s_ok) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned target = (a.bar_base + idx + 1u) * (unsigned)a.P + a.bar_extra;
-        red_release_add(a.bar, 1u);
+        const unsigned P = (unsigned)a.P, gi = blockIdx.x % kBarGroups;
+        const unsigned ng = P < kBarGroups ? P : kBarGroups;
+        const unsigned gsize = P / kBarGroups + (gi < P % kBarGroups ? 1u : 0u);
+        unsigned *top = a.bar, *grp = a.bar + 32 * (1 + gi);
+        const unsigned n = a.bar_base + idx + 1u;
+        unsigned old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(grp) : "memory");
+        if (old + 1u == n * gsize) red_release_add(top, 1u);
+        const unsigned target = n * ng + a.bar_extra;
         const unsigned long long t0 = globaltimer();
         int e = 0;
-        while (ld_acquire(a.bar) < target) {
+        while (ld_acquire(top) < target) {
             if ((e = ld_err(a.err)) != 0) break;
             if (globaltimer() - t0 > a.timeout_ns) {
                 atomicCAS(a.err, 0, kDevTimeout);
@@ -246,6 +257,7 @@ struct Cta {
     int n_inp;
     int r0, nrows, e0, e1, c_lo;
     bool publish;
+    bool glob;  // row r0 also sums carries published by earlier CTAs
 };
 
 __device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc) {
@@ -491,10 +503,10 @@ __device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
 }
 
 // Forward finish of rows: pre-activation, tanh, leak blend, saved copies.
-template <int THREADS>
-__device__ void finish_fwd(const KArgs &a, const Cta &c, int s, unsigned phase_id) {
-    constexpr int U = THREADS / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Rows [lo, hi) of the batch starting at row i0 (RB rows) are finished.
+__device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, int s, unsigned phase_id, int i0,
+                                 int lo, int hi) {
+    const int lane = threadIdx.x & 31;
     const int Bp = a.Bp, B = a.B, N = a.N;
     const int t = s / a.M;
     const size_t NBp = (size_t)N * Bp;
@@ -505,7 +517,7 @@ __device__ void finish_fwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
     const int cpb = NCH < 4 ? NCH : 4;
     const int RB = 4 / cpb;
     const int CB = (NCH + cpb - 1) / cpb;
-    for (int i0 = warp * RB; i0 < c.nrows; i0 += U * RB) {
+    {
         for (int cb = 0; cb < CB; ++cb) {
             float x[4], hp[4], dr[4];
             int bcol[4], irow[4];
@@ -514,7 +526,7 @@ __device__ void finish_fwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
             for (int el = 0; el < 4; ++el) {
                 const int ri = el / cpb, ci = el - ri * cpb;
                 const int i = i0 + ri, cc = cb * cpb + ci, b = cc * 32 + lane;
-                ok[el] = ri < RB && i < c.nrows && cc < NCH && b < Bp;
+                ok[el] = ri < RB && i >= lo && i < hi && cc < NCH && b < Bp;
                 irow[el] = i;
                 bcol[el] = b;
                 x[el] = hp[el] = dr[el] = 0.f;
@@ -536,7 +548,7 @@ __device__ void finish_fwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
             for (int el = 0; el < 4; ++el) {
                 // warp-uniform: every lane of an element slot shares its row
                 const int ri = el / cpb;
-                const bool row_ok = ri < RB && irow[el] < c.nrows;
+                const bool row_ok = ri < RB && irow[el] >= lo && irow[el] < hi;
                 if (row_ok) x[el] = row_total(a, c, irow[el], ok[el] ? bcol[el] : 0, phase_id, false);
             }
 #pragma unroll
@@ -555,14 +567,25 @@ __device__ void finish_fwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
     }
 }
 
+template <int THREADS>
+__device__ void finish_fwd(const KArgs &a, const Cta &c, int s, unsigned phase_id) {
+    constexpr int U = THREADS / 32;
+    const int warp = threadIdx.x >> 5;
+    const int NCH = (a.Bp + 31) >> 5;
+    const int RB = 4 / (NCH < 4 ? NCH : 4);
+    // a first row that waits for earlier CTAs' carries goes last, to the last warp
+    const int lo = c.glob ? 1 : 0;
+    for (int i0 = warp * RB; i0 < c.nrows; i0 += U * RB) finish_fwd_batch(a, c, s, phase_id, i0, lo, c.nrows);
+    if (c.glob && warp == U - 1) finish_fwd_batch(a, c, s, phase_id, 0, 0, 1);
+}
+
 // Backward finish of rows for microstep s: G_{s-1} = G_s (1 - leak) + row
 // total (+ dOut of the step ending at s-1), then the elementwise terms of
 // microstep q = s-1.  s == S is the prologue (G_{S-1} = dOut[T-1]); s == 0
 // leaves G_{-1} in G for the final transpose into d_state0.
-template <int THREADS>
-__device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_id) {
-    constexpr int U = THREADS / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, int s, unsigned phase_id, int i0,
+                                 int lo, int hi) {
+    const int lane = threadIdx.x & 31;
     const int Bp = a.Bp, B = a.B, N = a.N, M = a.M;
     const size_t NBp = (size_t)N * Bp;
     const bool pro = s == a.S;
@@ -577,7 +600,7 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
     const int cpb = NCH < 4 ? NCH : 4;
     const int RB = 4 / cpb;
     const int CB = (NCH + cpb - 1) / cpb;
-    for (int i0 = warp * RB; i0 < c.nrows; i0 += U * RB) {
+    {
         float dl[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
         for (int cb = 0; cb < CB; ++cb) {
             float x[4], gv[4], ov[4], av[4], hv[4];
@@ -587,7 +610,7 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
             for (int el = 0; el < 4; ++el) {
                 const int ri = el / cpb, ci = el - ri * cpb;
                 const int i = i0 + ri, cc = cb * cpb + ci, b = cc * 32 + lane;
-                ok[el] = ri < RB && i < c.nrows && cc < NCH && b < Bp;
+                ok[el] = ri < RB && i >= lo && i < hi && cc < NCH && b < Bp;
                 irow[el] = i;
                 bcol[el] = b;
                 x[el] = gv[el] = ov[el] = av[el] = hv[el] = 0.f;
@@ -612,7 +635,7 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
 #pragma unroll
             for (int el = 0; el < 4; ++el) {
                 const int ri = el / cpb;
-                const bool row_ok = ri < RB && irow[el] < c.nrows;
+                const bool row_ok = ri < RB && irow[el] >= lo && irow[el] < hi;
                 if (row_ok) x[el] = row_total(a, c, irow[el], ok[el] ? bcol[el] : 0, phase_id, pro);
             }
 #pragma unroll
@@ -646,8 +669,9 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
             for (int ri = 0; ri < 4; ++ri) {
                 if (ri >= RB) break;
                 const int i = i0 + ri;
-                if (i >= c.nrows) break;
+                if (i >= hi) break;
                 const float sl = warp_sum(dl[ri]), sb = warp_sum(db[ri]);
+                if (i < lo) continue;
                 if (lane == 0) {
                     const int r = c.r0 + i;
                     if (c.stage) {
@@ -664,6 +688,18 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_i
             }
         }
     }
+}
+
+template <int THREADS>
+__device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_id) {
+    constexpr int U = THREADS / 32;
+    const int warp = threadIdx.x >> 5;
+    const int NCH = (a.Bp + 31) >> 5;
+    const int RB = 4 / (NCH < 4 ? NCH : 4);
+    const bool defer = c.glob && s != a.S;  // the prologue has no carries to wait for
+    const int lo = defer ? 1 : 0;
+    for (int i0 = warp * RB; i0 < c.nrows; i0 += U * RB) finish_bwd_batch(a, c, s, phase_id, i0, lo, c.nrows);
+    if (defer && warp == U - 1) finish_bwd_batch(a, c, s, phase_id, 0, 0, 1);
 }
 
 // Publish this CTA's carry for the row its piece ends inside (row r0 + nrows):
@@ -741,6 +777,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     c.e1 = s_meta[3];
     c.c_lo = s_meta[4];
     c.publish = s_meta[5] != 0;
+    c.glob = c.c_lo < cta && c.nrows > 0;
     c.rows = a.rs_smem ? reinterpret_cast<float *>(smem + a.o_rows) : a.rowsum_g + (size_t)c.r0 * Bp;
     if (c.nrows + 2 > a.rows_cap || (SMEMG && c.e1 - c.e0 > a.cap)) {
         if (tid == 0) atomicCAS(a.err, 0, kDevInternal);
@@ -978,7 +1015,7 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.slot = g->slot;
     char *sc = (char *)scratch;
     k.bar = (unsigned *)(sc + p.off_ctrl);
-    k.err = (int *)(sc + p.off_ctrl + 4);
+    k.err = (int *)(sc + p.off_ctrl + kStatusOffset);
     k.carry = (unsigned long long *)(sc + p.off_carry);
     k.wperm = (float *)(sc + p.off_wperm);
     k.dwperm = (float *)(sc + p.off_dwperm);
@@ -1073,7 +1110,7 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     const size_t E1 = (size_t)(q.E > 0 ? q.E : 1);
     size_t off = 0;
     q.off_ctrl = off;
-    q.ctrl_bytes = 256;
+    q.ctrl_bytes = kCtrlBytes;
     off += q.ctrl_bytes;
     q.off_carry = off;
     off = align256(off + 8 * (size_t)q.P * q.Bp);
