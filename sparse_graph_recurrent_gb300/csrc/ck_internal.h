@@ -34,11 +34,10 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
 // Device-side status words written by the recurrence kernels.
 enum : int { kDevOk = 0, kDevTimeout = 1, kDevInternal = 2 };
 
-// Control block at the start of scratch: the barrier's top counter, its group
-// counters (one 128-byte line each), then the status word.
-constexpr int kBarGroups = 8;
-constexpr size_t kStatusOffset = 4 * 32 * (1 + kBarGroups);
-constexpr size_t kCtrlBytes = 4 * 32 * (2 + kBarGroups);
+// Control block at the start of scratch: the barrier counter and, on its own
+// 128-byte line, the status word.
+constexpr size_t kStatusOffset = 128;
+constexpr size_t kCtrlBytes = 256;
 
 // Shared-memory layout of one direction's kernel (byte offsets).
 struct SmemLayout {

@@ -121,27 +121,19 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Grid-wide barrier, bounded by a.timeout_ns.  Two levels, so few arrivals
-// meet on any one address: CTA c adds to the counter of group c % kBarGroups;
-// the last arrival of a group adds to the top counter, which every CTA polls.
-// Counters only grow within a call, so barrier idx waits for known totals.
-// Returns false for the whole CTA once any CTA has recorded an error, so every
-// CTA leaves together.
+// Grid-wide barrier, bounded by a.timeout_ns.  Each CTA adds one to a
+// counter that only grows within a call; barrier idx waits for its total.
+// (A two-level tree of counters measured slower here: its extra returning
+// atomic costs more than the contention it removes.)  Returns false for the
+// whole CTA once any CTA has recorded an error, so every CTA leaves together.
 __device__ bool grid_sync(const KArgs &a, unsigned idx, int *s_ok) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned P = (unsigned)a.P, gi = blockIdx.x % kBarGroups;
-        const unsigned ng = P < kBarGroups ? P : kBarGroups;
-        const unsigned gsize = P / kBarGroups + (gi < P % kBarGroups ? 1u : 0u);
-        unsigned *top = a.bar, *grp = a.bar + 32 * (1 + gi);
-        const unsigned n = a.bar_base + idx + 1u;
-        unsigned old;
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(grp) : "memory");
-        if (old + 1u == n * gsize) red_release_add(top, 1u);
-        const unsigned target = n * ng + a.bar_extra;
+        const unsigned target = (a.bar_base + idx + 1u) * (unsigned)a.P + a.bar_extra;
+        red_release_add(a.bar, 1u);
         const unsigned long long t0 = globaltimer();
         int e = 0;
-        while (ld_acquire(top) < target) {
+        while (ld_acquire(a.bar) < target) {
             if ((e = ld_err(a.err)) != 0) break;
             if (globaltimer() - t0 > a.timeout_ns) {
                 atomicCAS(a.err, 0, kDevTimeout);
