@@ -225,32 +225,45 @@ __device__ void from_rows(float *__restrict__ dst, const float *__restrict__ src
     }
 }
 
-// Per-CTA view of its piece of the work, in shared memory.
+// Per-CTA view of its piece of the work.  Its tables live in shared memory at
+// offsets fixed per launch; the accessors below recompute their addresses
+// from the shared-memory base instead of holding them in registers.
+//   srp    row_ptr[r0 + i], i < nrows + 2 (clamped at N)
+//   prm    {leak, bias} of rows r0 + i;  sslot: their input slots
+//   sgrp   groups [ga, gb) whose carries belong to row r0 + i, ga << 16 | gb
+//   scarry [G][Bp] group carries;  tile: [32][33] transpose tile
+//   scw, srow, sdw   {col, w bits}, row and edge-gradient sum of the CTA's edges
+//   stage mode, rows r0 + i:
+//     forward:  st0 = current state (resident), st1 = drives of the CTA's
+//               input rows for the current input step (row inp[i])
+//     backward: st0 = G (resident), st1 = A[q], st2 = H[q], st3 = dOut[t(q)],
+//               acc = {d_leak, d_bias} running sums (resident)
 struct Cta {
-    int *srp;       // row_ptr[r0 + i], i < nrows + 2 (clamped at N)
-    float2 *prm;    // {leak, bias} of rows r0 + i
-    int *sslot;     // slot of rows r0 + i
-    int *sgrp;      // groups [ga, gb) whose carries belong to row r0 + i, packed ga << 16 | gb
-    float *scarry;  // [G][Bp]
-    float *rows;    // [nrows][Bp] row slots (shared or global)
-    float *tile;    // [32][33]
-    int2 *scw;      // {col, bits of w} of the CTA's edges
-    int *srow;      // row of the CTA's edges
-    float *sdw;     // edge-gradient accumulators of the CTA's edges
-    // Staged finish operands (stage mode), rows r0 + i:
-    //   forward:  st0 = current state (resident across microsteps), st1 = drives
-    //             of the CTA's input rows for the current input step (row inp[i])
-    //   backward: st0 = G (resident), st1 = A[q], st2 = H[q], st3 = dOut[t(q)],
-    //             acc = {d_leak, d_bias} running sums (resident)
-    float *st0, *st1, *st2, *st3;
-    int *inp;
-    float2 *acc;
+    float *rows;  // [nrows][Bp] row slots (shared or global)
     bool stage;
     int n_inp;
     int r0, nrows, e0, e1, c_lo;
     bool publish;
     bool glob;  // row r0 also sums carries published by earlier CTAs
 };
+
+extern __shared__ __align__(16) unsigned char ck_smem[];
+__device__ __forceinline__ int *S_srp(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_srp); }
+__device__ __forceinline__ float2 *S_prm(const KArgs &a) { return reinterpret_cast<float2 *>(ck_smem + a.o_prm); }
+__device__ __forceinline__ int *S_sslot(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_slot); }
+__device__ __forceinline__ int *S_sgrp(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_grp); }
+__device__ __forceinline__ float *S_scarry(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_carry); }
+__device__ __forceinline__ float *S_tile(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_tile); }
+__device__ __forceinline__ int2 *S_scw(const KArgs &a) { return reinterpret_cast<int2 *>(ck_smem + a.o_cw); }
+__device__ __forceinline__ int *S_srow(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_row); }
+__device__ __forceinline__ float *S_sdw(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_dw); }
+__device__ __forceinline__ float *S_st0(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st0); }
+__device__ __forceinline__ float *S_st1(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st1); }
+__device__ __forceinline__ float *S_st2(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st2); }
+__device__ __forceinline__ float *S_st3(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st3); }
+__device__ __forceinline__ int *S_inp(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_inp); }
+__device__ __forceinline__ float2 *S_acc(const KArgs &a) { return reinterpret_cast<float2 *>(ck_smem + a.o_acc); }
+
 
 __device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc) {
     const unsigned sa = (unsigned)__cvta_generic_to_shared(sdst);
@@ -279,9 +292,9 @@ __device__ __forceinline__ int group_of(const Cta &c, int G, int k) {
 
 // ------------------------------------------------------------ part A
 
-// Walk this lane group's edges: gather rows[col[k]] * w[k] into per-row sums.
-// Batches of UNR edges are double-buffered: the gathers of the next batch are
-// in flight while the current one is summed.  Backward: also add each edge's
+// Walk this lane group's edges: gather rows[col[k]] * w[k] into per-row sums,
+// UNR edges per batch with all of a batch's gathers issued before any is used.
+// Backward: also add each edge's
 // dot product with the state h_{s-1} of its source row into the edge-gradient
 // accumulator; that source row stays in registers, and the next row's is
 // fetched as soon as the current one starts.
@@ -332,7 +345,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     }
     const int len = k1 - k0;
     const int trips = (__reduce_max_sync(kFull, (unsigned)len) + UNR - 1) / UNR;
-    auto row_at = [&](int k) -> int { return SMEMG ? c.srow[k - c.e0] : __ldg(a.rowid + k); };
+    auto row_at = [&](int k) -> int { return SMEMG ? S_srow(a)[k - c.e0] : __ldg(a.rowid + k); };
     int cur = len > 0 ? row_at(k0) : -1;
     float4 acc[NC];
 #pragma unroll
@@ -348,7 +361,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             h[ch] = row >= 0 ? __ldg(reinterpret_cast<const float4 *>(hp + ch * CW)) : zero4();
     };
     auto next_row = [&](int row) -> int {  // the row after `row` that has edges in [k0, k1)
-        const int pos = c.srp[row - c.r0 + 1];
+        const int pos = S_srp(a)[row - c.r0 + 1];
         return pos < k1 ? row_at(pos) : -1;
     };
     if (BWD) {
@@ -379,10 +392,10 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             bt.w[q] = 0.f;
             if (ok) {
                 if (SMEMG) {
-                    const int2 cw = c.scw[kk - c.e0];
+                    const int2 cw = S_scw(a)[kk - c.e0];
                     cc = cw.x;
                     bt.w[q] = __int_as_float(cw.y);
-                    bt.rid[q] = c.srow[kk - c.e0];
+                    bt.rid[q] = S_srow(a)[kk - c.e0];
                 } else {
                     cc = __ldg(a.col + kk);
                     bt.w[q] = __ldcg(a.wperm + kk);
@@ -426,7 +439,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             if (a.LPE == UNR && (UNR & (UNR - 1)) == 0) {
                 const int kk = kb + lig;
                 if (kk < k1) {
-                    if (SMEMG) c.sdw[kk - c.e0] += d[0];
+                    if (SMEMG) S_sdw(a)[kk - c.e0] += d[0];
                     else a.dwperm[kk] += d[0];
                 }
             } else if (lig == 0) {
@@ -434,7 +447,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                 for (int q = 0; q < UNR; ++q) {
                     const int kk = kb + q;
                     if (kk < k1) {
-                        if (SMEMG) c.sdw[kk - c.e0] += d[q];
+                        if (SMEMG) S_sdw(a)[kk - c.e0] += d[q];
                         else a.dwperm[kk] += d[q];
                     }
                 }
@@ -442,25 +455,19 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
         }
     };
 
-    Batch<NC, UNR> b0, b1;
-    if (trips > 0) load(b0, k0);
-    for (int it = 0; it < trips; it += 2) {
-        const int kb0 = k0 + it * UNR, kb1 = kb0 + UNR;
-        const bool two = it + 1 < trips;
-        if (two) load(b1, kb1);
-        consume(b0, kb0);
-        if (two) {
-            if (it + 2 < trips) load(b0, kb1 + UNR);
-            consume(b1, kb1);
-        }
+    Batch<NC, UNR> bt;
+    for (int it = 0; it < trips; ++it) {
+        const int kb = k0 + it * UNR;
+        load(bt, kb);
+        consume(bt, kb);
     }
     if (active) {
         // the row this group stops in: finished here if its last edge is ours
         // and its row end belongs to this CTA, else a carry
         const bool fin = len > 0 && cur >= c.r0 && cur < c.r0 + c.nrows &&
-                         c.srp[cur - c.r0 + 1] == k1;
+                         S_srp(a)[cur - c.r0 + 1] == k1;
         if (fin) flush(cur);
-        float *dst = c.scarry + (size_t)gam * Bp + lig * 4;
+        float *dst = S_scarry(a) + (size_t)gam * Bp + lig * 4;
 #pragma unroll
         for (int ch = 0; ch < NC; ++ch) *reinterpret_cast<float4 *>(dst + ch * CW) = acc[ch];
     }
@@ -468,23 +475,57 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
 
 // ------------------------------------------------------------ part B
 
-// Sum of row i's partial sums for column b: its slot (the part summed by the
-// group holding its last edge), then the carries of the groups holding its
-// earlier edges in this CTA, then those published by earlier CTAs (which can
-// only reach the CTA's first row).
-__device__ __forceinline__ float row_total(const KArgs &a, const Cta &c, int i, int b,
-                                           unsigned phase_id, bool pro) {
-    if (pro) return 0.f;
-    const int gr = c.sgrp[i];
+// Element layout of part B: a warp finishes RB rows at a time, lane = batch
+// column, NCH 32-column chunks per row, at most four (row, chunk) elements per
+// lane per batch.  Fixed per launch.
+struct PB {
+    int NCH, cpb, RB, CB;
+    int ri[4], ci[4];
+};
+
+__device__ __forceinline__ PB make_pb(int Bp) {
+    PB p;
+    p.NCH = (Bp + 31) >> 5;
+    p.cpb = p.NCH < 4 ? p.NCH : 4;
+    p.RB = 4 / p.cpb;
+    p.CB = (p.NCH + p.cpb - 1) / p.cpb;
+#pragma unroll
+    for (int el = 0; el < 4; ++el) {
+        p.ri[el] = el / p.cpb;
+        p.ci[el] = el - p.ri[el] * p.cpb;
+    }
+    return p;
+}
+
+// Fold the carries of the groups that hold a row's earlier edges into its
+// slot, for every row of the CTA, in group order; rows with no edges here get
+// 0.  All threads of the CTA take part.
+template <int THREADS>
+__device__ __forceinline__ void fold_carries(const KArgs &a, const Cta &c) {
+    const int Bp = a.Bp, n = c.nrows * Bp;
+    for (int x = threadIdx.x; x < n; x += THREADS) {
+        const int i = x / Bp, b = x - i * Bp;
+        const int gr = S_sgrp(a)[i];
+        float *slot = c.rows + (size_t)i * Bp + b;
+        if (gr < 0) {
+            *slot = 0.f;
+        } else {
+            const int ga = gr >> 16, gb = gr & 0xffff;
+            if (ga < gb) {
+                float v = a.rs_smem ? *slot : __ldcg(slot);
+                for (int u = ga; u < gb; ++u) v += S_scarry(a)[(size_t)u * Bp + b];
+                *slot = v;
+            }
+        }
+    }
+}
+
+// Carries published by earlier CTAs for column b of the CTA's first row.
+__device__ __forceinline__ float global_carry(const KArgs &a, const Cta &c, int b,
+                                              unsigned phase_id) {
     float x = 0.f;
-    if (gr >= 0) {
-        x = a.rs_smem ? c.rows[(size_t)i * a.Bp + b] : __ldcg(c.rows + (size_t)i * a.Bp + b);
-        for (int u = gr >> 16, ue = gr & 0xffff; u < ue; ++u) x += c.scarry[(size_t)u * a.Bp + b];
-    }
-    if (i == 0 && c.srp[0] < c.e0) {
-        for (int cc = c.c_lo; cc < (int)blockIdx.x; ++cc)
-            x += wait_carry(a, a.carry + (size_t)cc * a.Bp + b, phase_id);
-    }
+    for (int cc = c.c_lo; cc < (int)blockIdx.x; ++cc)
+        x += wait_carry(a, a.carry + (size_t)cc * a.Bp + b, phase_id);
     return x;
 }
 
@@ -494,215 +535,208 @@ __device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes & ~15u) : "memory");
 }
 
-// Forward finish of rows: pre-activation, tanh, leak blend, saved copies.
-// Rows [lo, hi) of the batch starting at row i0 (RB rows) are finished.
-__device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, int s, unsigned phase_id, int i0,
-                                 int lo, int hi) {
+// Forward finish of rows [lo, hi) among the batch starting at row i0:
+// pre-activation, tanh, leak blend, saved copies.  Straight-line over the
+// batch's elements so their loads and tanh evaluations overlap.
+__device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, const PB &pb,
+                                                 int s, unsigned phase_id, int i0, int lo,
+                                                 int hi) {
     const int lane = threadIdx.x & 31;
-    const int Bp = a.Bp, B = a.B, N = a.N;
+    const int Bp = a.Bp, B = a.B;
     const int t = s / a.M;
-    const size_t NBp = (size_t)N * Bp;
+    const size_t NBp = (size_t)a.N * Bp;
     const float *hin = a.H + (size_t)s * NBp;
     float *hout = a.H + (size_t)(s + 1) * NBp;
     float *aout = a.A + (size_t)s * NBp;
-    const int NCH = (Bp + 31) >> 5;
-    const int cpb = NCH < 4 ? NCH : 4;
-    const int RB = 4 / cpb;
-    const int CB = (NCH + cpb - 1) / cpb;
-    {
-        for (int cb = 0; cb < CB; ++cb) {
-            float x[4], hp[4], dr[4];
-            int bcol[4], irow[4];
-            bool ok[4];
+    for (int cb = 0; cb < pb.CB; ++cb) {
+        int ii[4], bb[4];
+        bool ok[4];
+        float x[4], hp[4], dr[4];
+        float2 pr[4];
 #pragma unroll
-            for (int el = 0; el < 4; ++el) {
-                const int ri = el / cpb, ci = el - ri * cpb;
-                const int i = i0 + ri, cc = cb * cpb + ci, b = cc * 32 + lane;
-                ok[el] = ri < RB && i >= lo && i < hi && cc < NCH && b < Bp;
-                irow[el] = i;
-                bcol[el] = b;
-                x[el] = hp[el] = dr[el] = 0.f;
-                if (ok[el]) {
-                    const int r = c.r0 + i;
-                    if (c.stage) {
-                        hp[el] = c.st0[(size_t)i * Bp + b];
-                        const int j = c.inp[i];
-                        if (j >= 0 && b < B) dr[el] = c.st1[(size_t)j * Bp + b];
-                    } else {
-                        hp[el] = __ldcg(hin + (size_t)r * Bp + b);
-                        const int sl = c.sslot[i];
-                        if (sl >= 0 && b < B)
-                            dr[el] = __ldg(a.drives + ((size_t)t * a.n_in + sl) * B + b);
-                    }
-                }
+        for (int el = 0; el < 4; ++el) {
+            const int i = i0 + pb.ri[el], cc = cb * pb.cpb + pb.ci[el], b = cc * 32 + lane;
+            ok[el] = pb.ri[el] < pb.RB && i >= lo && i < hi && cc < pb.NCH && b < Bp;
+            ii[el] = ok[el] ? i : lo;
+            bb[el] = ok[el] ? b : 0;
+        }
+#pragma unroll
+        for (int el = 0; el < 4; ++el) {
+            const size_t o = (size_t)ii[el] * Bp + bb[el];
+            x[el] = a.rs_smem ? c.rows[o] : __ldcg(c.rows + o);
+            pr[el] = S_prm(a)[ii[el]];
+            hp[el] = c.stage ? S_st0(a)[o] : __ldcg(hin + (size_t)c.r0 * Bp + o);
+            dr[el] = 0.f;
+            if (c.stage) {
+                const int j = S_inp(a)[ii[el]];
+                if (j >= 0 && bb[el] < B) dr[el] = S_st1(a)[(size_t)j * Bp + bb[el]];
+            } else {
+                const int sl = S_sslot(a)[ii[el]];
+                if (sl >= 0 && bb[el] < B)
+                    dr[el] = __ldg(a.drives + ((size_t)t * a.n_in + sl) * B + bb[el]);
             }
+        }
+        if (lo == 0 && i0 == 0 && c.glob) {
 #pragma unroll
-            for (int el = 0; el < 4; ++el) {
-                // warp-uniform: every lane of an element slot shares its row
-                const int ri = el / cpb;
-                const bool row_ok = ri < RB && irow[el] >= lo && irow[el] < hi;
-                if (row_ok) x[el] = row_total(a, c, irow[el], ok[el] ? bcol[el] : 0, phase_id, false);
-            }
+            for (int el = 0; el < 4; ++el)
+                if (pb.ri[el] == 0 && pb.RB > 0) x[el] += global_carry(a, c, bb[el], phase_id);
+        }
+        float av[4], th[4];
 #pragma unroll
-            for (int el = 0; el < 4; ++el) {
-                if (!ok[el]) continue;
-                const int i = irow[el], r = c.r0 + i, b = bcol[el];
-                const float2 pr = c.prm[i];
-                float av = x[el] + pr.y + dr[el], hv = 0.f;
-                if (b < B) hv = fmaf(pr.x, tanhf(av), (1.f - pr.x) * hp[el]);
-                else av = 0.f;
-                if (c.stage) c.st0[(size_t)i * Bp + b] = hv;
-                hout[(size_t)r * Bp + b] = hv;
-                __stcs(aout + (size_t)r * Bp + b, av);
+        for (int el = 0; el < 4; ++el) av[el] = x[el] + pr[el].y + dr[el];
+#pragma unroll
+        for (int el = 0; el < 4; ++el) th[el] = tanhf(av[el]);
+#pragma unroll
+        for (int el = 0; el < 4; ++el) {
+            const bool live = bb[el] < B;
+            const float hv = live ? fmaf(pr[el].x, th[el], (1.f - pr[el].x) * hp[el]) : 0.f;
+            const float a0 = live ? av[el] : 0.f;
+            if (ok[el]) {
+                const size_t o = (size_t)ii[el] * Bp + bb[el];
+                if (c.stage) S_st0(a)[o] = hv;
+                hout[(size_t)c.r0 * Bp + o] = hv;
+                __stcs(aout + (size_t)c.r0 * Bp + o, a0);
             }
         }
     }
 }
 
 template <int THREADS>
-__device__ void finish_fwd(const KArgs &a, const Cta &c, int s, unsigned phase_id) {
+__device__ void finish_fwd(const KArgs &a, const Cta &c, const PB &pb, int s, unsigned phase_id) {
     constexpr int U = THREADS / 32;
     const int warp = threadIdx.x >> 5;
-    const int NCH = (a.Bp + 31) >> 5;
-    const int RB = 4 / (NCH < 4 ? NCH : 4);
     // a first row that waits for earlier CTAs' carries goes last, to the last warp
     const int lo = c.glob ? 1 : 0;
-    for (int i0 = warp * RB; i0 < c.nrows; i0 += U * RB) finish_fwd_batch(a, c, s, phase_id, i0, lo, c.nrows);
-    if (c.glob && warp == U - 1) finish_fwd_batch(a, c, s, phase_id, 0, 0, 1);
+    for (int i0 = warp * pb.RB; i0 < c.nrows; i0 += U * pb.RB)
+        finish_fwd_batch(a, c, pb, s, phase_id, i0, lo, c.nrows);
+    if (c.glob && warp == U - 1) finish_fwd_batch(a, c, pb, s, phase_id, 0, 0, 1);
 }
 
-// Backward finish of rows for microstep s: G_{s-1} = G_s (1 - leak) + row
-// total (+ dOut of the step ending at s-1), then the elementwise terms of
-// microstep q = s-1.  s == S is the prologue (G_{S-1} = dOut[T-1]); s == 0
-// leaves G_{-1} in G for the final transpose into d_state0.
-__device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, int s, unsigned phase_id, int i0,
-                                 int lo, int hi) {
+// Backward finish of rows [lo, hi) among the batch at i0, for microstep s:
+// G_{s-1} = G_s (1 - leak) + row total (+ dOut of the step ending at s-1),
+// then the elementwise terms of microstep q = s-1.  s == S is the prologue
+// (G_{S-1} = dOut[T-1]); s == 0 leaves G_{-1} for the transpose into d_state0.
+__device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, const PB &pb,
+                                                 int s, unsigned phase_id, int i0, int lo,
+                                                 int hi) {
     const int lane = threadIdx.x & 31;
-    const int Bp = a.Bp, B = a.B, N = a.N, M = a.M;
-    const size_t NBp = (size_t)N * Bp;
+    const int Bp = a.Bp, B = a.B, M = a.M;
+    const size_t NBp = (size_t)a.N * Bp;
     const bool pro = s == a.S;
     const int q = s - 1;
     const int tq = q >= 0 ? q / M : 0;
     const bool step_end = q >= 0 && q - tq * M == M - 1;
-    const float *Aq = a.A + (size_t)(q >= 0 ? q : 0) * NBp;
-    const float *Hq = a.H + (size_t)(q >= 0 ? q : 0) * NBp;
-    const float *dO = a.doutT + (size_t)tq * NBp;
-    float *daq = a.da + (size_t)(q & 1) * NBp;
-    const int NCH = (Bp + 31) >> 5;
-    const int cpb = NCH < 4 ? NCH : 4;
-    const int RB = 4 / cpb;
-    const int CB = (NCH + cpb - 1) / cpb;
-    {
-        float dl[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int cb = 0; cb < CB; ++cb) {
-            float x[4], gv[4], ov[4], av[4], hv[4];
-            int bcol[4], irow[4];
-            bool ok[4];
+    const bool first = q >= 0 && q - tq * M == M - 1;  // first visit of step tq going backwards
+    const size_t ro = (size_t)c.r0 * Bp;
+    const float *Aq = a.A + (size_t)(q >= 0 ? q : 0) * NBp + ro;
+    const float *Hq = a.H + (size_t)(q >= 0 ? q : 0) * NBp + ro;
+    const float *dO = a.doutT + (size_t)tq * NBp + ro;
+    float *daq = a.da + (size_t)(q & 1) * NBp + ro;
+    float dl[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int cb = 0; cb < pb.CB; ++cb) {
+        int ii[4], bb[4];
+        bool ok[4];
+        float x[4], gv[4], ov[4], av[4], hv[4], lam[4];
 #pragma unroll
-            for (int el = 0; el < 4; ++el) {
-                const int ri = el / cpb, ci = el - ri * cpb;
-                const int i = i0 + ri, cc = cb * cpb + ci, b = cc * 32 + lane;
-                ok[el] = ri < RB && i >= lo && i < hi && cc < NCH && b < Bp;
-                irow[el] = i;
-                bcol[el] = b;
-                x[el] = gv[el] = ov[el] = av[el] = hv[el] = 0.f;
-                if (ok[el] && c.stage) {
-                    const size_t o = (size_t)i * Bp + b;
-                    if (!pro) gv[el] = c.st0[o];
-                    if (step_end) ov[el] = c.st3[o];
-                    if (q >= 0) {
-                        av[el] = c.st1[o];
-                        hv[el] = c.st2[o];
-                    }
-                } else if (ok[el]) {
-                    const size_t o = (size_t)(c.r0 + i) * Bp + b;
-                    if (!pro) gv[el] = __ldcg(a.G_ + o);
-                    if (step_end) ov[el] = __ldcg(dO + o);
-                    if (q >= 0) {
-                        av[el] = __ldcs(Aq + o);
-                        hv[el] = __ldg(Hq + o);
-                    }
-                }
-            }
+        for (int el = 0; el < 4; ++el) {
+            const int i = i0 + pb.ri[el], cc = cb * pb.cpb + pb.ci[el], b = cc * 32 + lane;
+            ok[el] = pb.ri[el] < pb.RB && i >= lo && i < hi && cc < pb.NCH && b < Bp;
+            ii[el] = ok[el] ? i : lo;
+            bb[el] = ok[el] ? b : 0;
+        }
 #pragma unroll
-            for (int el = 0; el < 4; ++el) {
-                const int ri = el / cpb;
-                const bool row_ok = ri < RB && irow[el] >= lo && irow[el] < hi;
-                if (row_ok) x[el] = row_total(a, c, irow[el], ok[el] ? bcol[el] : 0, phase_id, pro);
-            }
-#pragma unroll
-            for (int el = 0; el < 4; ++el) {
-                if (!ok[el]) continue;
-                const int i = irow[el], r = c.r0 + i, b = bcol[el];
-                const size_t o = (size_t)r * Bp + b;
-                const float lam = c.prm[i].x;
-                float gn = fmaf(gv[el], 1.f - lam, x[el]) + ov[el];
-                if (b >= B) gn = 0.f;
-                if (c.stage) c.st0[(size_t)i * Bp + b] = gn;
-                else a.G_[o] = gn;
-                if (q < 0) continue;
-                float d = 0.f;
-                if (b < B) {
-                    const float p = tanhf(av[el]);
-                    d = gn * lam * (1.f - p * p);
-                    dl[el / cpb] = fmaf(gn, p - hv[el], dl[el / cpb]);
-                    db[el / cpb] += d;
-                    const int sl = c.sslot[i];
-                    if (sl >= 0) {
-                        float *dd = a.ddrives + ((size_t)tq * a.n_in + sl) * B + b;
-                        *dd = (q - tq * M == M - 1) ? d : *dd + d;
-                    }
-                }
-                daq[o] = d;
+        for (int el = 0; el < 4; ++el) {
+            const size_t o = (size_t)ii[el] * Bp + bb[el];
+            lam[el] = S_prm(a)[ii[el]].x;
+            x[el] = pro ? 0.f : (a.rs_smem ? c.rows[o] : __ldcg(c.rows + o));
+            if (c.stage) {
+                gv[el] = pro ? 0.f : S_st0(a)[o];
+                ov[el] = step_end ? S_st3(a)[o] : 0.f;
+                av[el] = q >= 0 ? S_st1(a)[o] : 0.f;
+                hv[el] = q >= 0 ? S_st2(a)[o] : 0.f;
+            } else {
+                gv[el] = pro ? 0.f : __ldcg(a.G_ + ro + o);
+                ov[el] = step_end ? __ldcg(dO + o) : 0.f;
+                av[el] = q >= 0 ? __ldcs(Aq + o) : 0.f;
+                hv[el] = q >= 0 ? __ldg(Hq + o) : 0.f;
             }
         }
-        if (q >= 0) {
+        if (!pro && lo == 0 && i0 == 0 && c.glob) {
 #pragma unroll
-            for (int ri = 0; ri < 4; ++ri) {
-                if (ri >= RB) break;
-                const int i = i0 + ri;
-                if (i >= hi) break;
-                const float sl = warp_sum(dl[ri]), sb = warp_sum(db[ri]);
-                if (i < lo) continue;
-                if (lane == 0) {
-                    const int r = c.r0 + i;
-                    if (c.stage) {
-                        const float2 o = q == a.S - 1 ? make_float2(0.f, 0.f) : c.acc[i];
-                        c.acc[i] = make_float2(o.x + sl, o.y + sb);
-                    } else if (q == a.S - 1) {
-                        a.dleak[r] = sl;
-                        a.dbias[r] = sb;
-                    } else {
-                        a.dleak[r] += sl;
-                        a.dbias[r] += sb;
-                    }
+            for (int el = 0; el < 4; ++el)
+                if (pb.ri[el] == 0) x[el] += global_carry(a, c, bb[el], phase_id);
+        }
+        float gn[4], p[4];
+#pragma unroll
+        for (int el = 0; el < 4; ++el) {
+            gn[el] = fmaf(gv[el], 1.f - lam[el], x[el]) + ov[el];
+            if (bb[el] >= B) gn[el] = 0.f;
+        }
+#pragma unroll
+        for (int el = 0; el < 4; ++el) p[el] = q >= 0 ? tanhf(av[el]) : 0.f;
+#pragma unroll
+        for (int el = 0; el < 4; ++el) {
+            if (!ok[el]) continue;
+            const size_t o = (size_t)ii[el] * Bp + bb[el];
+            if (c.stage) S_st0(a)[o] = gn[el];
+            else a.G_[ro + o] = gn[el];
+            if (q < 0) continue;
+            const bool live = bb[el] < B;
+            const float d = live ? gn[el] * lam[el] * (1.f - p[el] * p[el]) : 0.f;
+            if (live) {
+                dl[pb.ri[el]] = fmaf(gn[el], p[el] - hv[el], dl[pb.ri[el]]);
+                db[pb.ri[el]] += d;
+                const int sl = S_sslot(a)[ii[el]];
+                if (sl >= 0) {
+                    float *dd = a.ddrives + ((size_t)tq * a.n_in + sl) * B + bb[el];
+                    *dd = first ? d : *dd + d;
                 }
+            }
+            daq[o] = d;
+        }
+    }
+    if (q >= 0) {
+#pragma unroll
+        for (int ri = 0; ri < 4; ++ri) {
+            if (ri >= pb.RB) break;
+            const int i = i0 + ri;
+            if (i >= hi) break;
+            const float sl = warp_sum(dl[ri]), sb = warp_sum(db[ri]);
+            if (i < lo || lane != 0) continue;
+            if (c.stage) {
+                const float2 o = q == a.S - 1 ? make_float2(0.f, 0.f) : S_acc(a)[i];
+                S_acc(a)[i] = make_float2(o.x + sl, o.y + sb);
+            } else if (q == a.S - 1) {
+                a.dleak[c.r0 + i] = sl;
+                a.dbias[c.r0 + i] = sb;
+            } else {
+                a.dleak[c.r0 + i] += sl;
+                a.dbias[c.r0 + i] += sb;
             }
         }
     }
 }
 
 template <int THREADS>
-__device__ void finish_bwd(const KArgs &a, const Cta &c, int s, unsigned phase_id) {
+__device__ void finish_bwd(const KArgs &a, const Cta &c, const PB &pb, int s, unsigned phase_id) {
     constexpr int U = THREADS / 32;
     const int warp = threadIdx.x >> 5;
-    const int NCH = (a.Bp + 31) >> 5;
-    const int RB = 4 / (NCH < 4 ? NCH : 4);
     const bool defer = c.glob && s != a.S;  // the prologue has no carries to wait for
     const int lo = defer ? 1 : 0;
-    for (int i0 = warp * RB; i0 < c.nrows; i0 += U * RB) finish_bwd_batch(a, c, s, phase_id, i0, lo, c.nrows);
-    if (defer && warp == U - 1) finish_bwd_batch(a, c, s, phase_id, 0, 0, 1);
+    for (int i0 = warp * pb.RB; i0 < c.nrows; i0 += U * pb.RB)
+        finish_bwd_batch(a, c, pb, s, phase_id, i0, lo, c.nrows);
+    if (defer && warp == U - 1) finish_bwd_batch(a, c, pb, s, phase_id, 0, 0, 1);
 }
 
 // Publish this CTA's carry for the row its piece ends inside (row r0 + nrows):
 // the carries of the groups holding that row's edges here, in group order.
 __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsigned phase_id) {
     const int lane = threadIdx.x & 31;
-    const int ka = c.srp[c.nrows] > c.e0 ? c.srp[c.nrows] : c.e0;
+    const int ka = S_srp(a)[c.nrows] > c.e0 ? S_srp(a)[c.nrows] : c.e0;
     const int ga = ka < c.e1 ? group_of(c, a.G, ka) : a.G;
     for (int b = lane; b < a.Bp; b += 32) {
         float x = 0.f;
-        for (int u = ga; u < a.G; ++u) x += c.scarry[(size_t)u * a.Bp + b];
+        for (int u = ga; u < a.G; ++u) x += S_scarry(a)[(size_t)u * a.Bp + b];
         st_relaxed64(a.carry + (size_t)blockIdx.x * a.Bp + b,
                      ((unsigned long long)phase_id << 32) | __float_as_uint(x));
     }
@@ -712,8 +746,7 @@ __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsi
 
 template <int THREADS, int NC, bool SMEMG, bool BWD>
 __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
-    constexpr int UNR = BWD ? (NC == 2 ? 4 : 2) : (NC == 2 ? 4 : 2);
-    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int UNR = BWD ? (NC == 2 ? 4 : 2) : (NC == 2 ? 8 : 4);
     __shared__ int s_ok, s_meta[8];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -724,23 +757,9 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     const bool active = g < a.EPW;
     const int gam = warp * a.EPW + g;  // this lane's group in the CTA (if active)
 
+    const PB pb = make_pb(Bp);
     Cta c;
-    c.srp = reinterpret_cast<int *>(smem + a.o_srp);
-    c.prm = reinterpret_cast<float2 *>(smem + a.o_prm);
-    c.sslot = reinterpret_cast<int *>(smem + a.o_slot);
-    c.sgrp = reinterpret_cast<int *>(smem + a.o_grp);
-    c.scarry = reinterpret_cast<float *>(smem + a.o_carry);
-    c.tile = reinterpret_cast<float *>(smem + a.o_tile);
-    c.scw = reinterpret_cast<int2 *>(smem + a.o_cw);
-    c.srow = reinterpret_cast<int *>(smem + a.o_row);
-    c.sdw = reinterpret_cast<float *>(smem + a.o_dw);
     c.stage = a.stage != 0;
-    c.st0 = reinterpret_cast<float *>(smem + a.o_st0);
-    c.st1 = reinterpret_cast<float *>(smem + a.o_st1);
-    c.st2 = reinterpret_cast<float *>(smem + a.o_st2);
-    c.st3 = reinterpret_cast<float *>(smem + a.o_st3);
-    c.inp = reinterpret_cast<int *>(smem + a.o_inp);
-    c.acc = reinterpret_cast<float2 *>(smem + a.o_acc);
 
     // ---- this CTA's piece of the merge path of (row ends, edges)
     const long long items = (long long)N + a.E;
@@ -770,16 +789,16 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     c.c_lo = s_meta[4];
     c.publish = s_meta[5] != 0;
     c.glob = c.c_lo < cta && c.nrows > 0;
-    c.rows = a.rs_smem ? reinterpret_cast<float *>(smem + a.o_rows) : a.rowsum_g + (size_t)c.r0 * Bp;
+    c.rows = a.rs_smem ? reinterpret_cast<float *>(ck_smem + a.o_rows) : a.rowsum_g + (size_t)c.r0 * Bp;
     if (c.nrows + 2 > a.rows_cap || (SMEMG && c.e1 - c.e0 > a.cap)) {
         if (tid == 0) atomicCAS(a.err, 0, kDevInternal);
         return;  // every other CTA sees the error word at its next wait
     }
-    for (int i = tid; i < c.nrows + 2; i += THREADS) c.srp[i] = __ldg(a.row_ptr + min(c.r0 + i, N));
+    for (int i = tid; i < c.nrows + 2; i += THREADS) S_srp(a)[i] = __ldg(a.row_ptr + min(c.r0 + i, N));
     for (int i = tid; i < c.nrows; i += THREADS) {
         const int r = c.r0 + i;
-        c.prm[i] = make_float2(__ldg(a.leak + r), BWD ? 0.f : __ldg(a.bias + r));
-        c.sslot[i] = __ldg(a.slot + r);
+        S_prm(a)[i] = make_float2(__ldg(a.leak + r), BWD ? 0.f : __ldg(a.bias + r));
+        S_sslot(a)[i] = __ldg(a.slot + r);
         // a row's last edge lies in this CTA iff it has edges here: then its slot
         // holds the tail, and the groups holding its earlier edges carry the rest
         const int rs = __ldg(a.row_ptr + r), re = __ldg(a.row_ptr + r + 1);
@@ -789,13 +808,13 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
             const int gb = group_of(c, a.G, re - 1);
             gr = (ga << 16) | gb;
         }
-        c.sgrp[i] = gr;
+        S_sgrp(a)[i] = gr;
     }
     for (int k = c.e0 + tid; k < c.e1; k += THREADS) {
         if (SMEMG) {
-            c.scw[k - c.e0] = make_int2(__ldg(a.col + k), __float_as_int(__ldg(a.w + __ldg(a.perm + k))));
-            c.srow[k - c.e0] = __ldg(a.rowid + k);
-            if (BWD) c.sdw[k - c.e0] = 0.f;
+            S_scw(a)[k - c.e0] = make_int2(__ldg(a.col + k), __float_as_int(__ldg(a.w + __ldg(a.perm + k))));
+            S_srow(a)[k - c.e0] = __ldg(a.rowid + k);
+            if (BWD) S_sdw(a)[k - c.e0] = 0.f;
         } else if (a.do_prologue) {
             a.wperm[k] = __ldg(a.w + __ldg(a.perm + k));
             if (BWD) a.dwperm[k] = 0.f;
@@ -806,7 +825,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         // index of each input row among this CTA's input rows (their drives are staged)
         if (tid == 0) {
             int n = 0;
-            for (int i = 0; i < c.nrows; ++i) c.inp[i] = c.sslot[i] >= 0 ? n++ : -1;
+            for (int i = 0; i < c.nrows; ++i) S_inp(a)[i] = S_sslot(a)[i] >= 0 ? n++ : -1;
             s_meta[6] = n;
         }
         __syncthreads();
@@ -816,24 +835,24 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     unsigned nbar = 0;
     if (a.do_prologue) {
         if (!BWD) {
-            to_rows<THREADS>(a.H, a.state0, c.r0, c.r0 + c.nrows, a.B, Bp, N, c.tile);
+            to_rows<THREADS>(a.H, a.state0, c.r0, c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
             if (c.stage) {
                 for (int j = tid; j < c.nrows * Bp; j += THREADS)
-                    c.st0[j] = __ldcg(a.H + (size_t)c.r0 * Bp + j);
+                    S_st0(a)[j] = __ldcg(a.H + (size_t)c.r0 * Bp + j);
             }
         } else {
             for (int t = 0; t < a.T; ++t)
                 to_rows<THREADS>(a.doutT + (size_t)t * NBp, a.dout + (size_t)t * a.B * N, c.r0,
-                                 c.r0 + c.nrows, a.B, Bp, N, c.tile);
+                                 c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
             if (c.stage) {
                 const size_t ro = (size_t)c.r0 * Bp;
-                stage_rows<THREADS>(c.st1, a.A + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
-                stage_rows<THREADS>(c.st2, a.H + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
-                stage_rows<THREADS>(c.st3, a.doutT + (size_t)(a.T - 1) * NBp + ro, c.nrows, Bp);
+                stage_rows<THREADS>(S_st1(a), a.A + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
+                stage_rows<THREADS>(S_st2(a), a.H + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
+                stage_rows<THREADS>(S_st3(a), a.doutT + (size_t)(a.T - 1) * NBp + ro, c.nrows, Bp);
                 cp_async_wait_all();
             }
             __syncthreads();
-            finish_bwd<THREADS>(a, c, a.S, 0u);
+            finish_bwd<THREADS>(a, c, pb, a.S, 0u);
         }
         if (!grid_sync(a, nbar++, &s_ok)) return;
     }
@@ -847,18 +866,18 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
             const size_t ro = (size_t)c.r0 * Bp;
             if (BWD && s > 0) {
                 const int q = s - 1, tq = q / a.M;
-                stage_rows<THREADS>(c.st1, a.A + (size_t)q * NBp + ro, c.nrows, Bp);
-                stage_rows<THREADS>(c.st2, a.H + (size_t)q * NBp + ro, c.nrows, Bp);
+                stage_rows<THREADS>(S_st1(a), a.A + (size_t)q * NBp + ro, c.nrows, Bp);
+                stage_rows<THREADS>(S_st2(a), a.H + (size_t)q * NBp + ro, c.nrows, Bp);
                 if (q - tq * a.M == a.M - 1)
-                    stage_rows<THREADS>(c.st3, a.doutT + (size_t)tq * NBp + ro, c.nrows, Bp);
+                    stage_rows<THREADS>(S_st3(a), a.doutT + (size_t)tq * NBp + ro, c.nrows, Bp);
             } else if (!BWD && c.n_inp > 0 && s % a.M == 0) {
                 const int t = s / a.M;
                 for (int j = tid; j < c.nrows * a.B; j += THREADS) {
                     const int i = j / a.B, b = j - i * a.B;
-                    const int ii = c.inp[i];
+                    const int ii = S_inp(a)[i];
                     if (ii >= 0)
-                        cp_async4(c.st1 + (size_t)ii * Bp + b,
-                                  a.drives + ((size_t)t * a.n_in + c.sslot[i]) * a.B + b);
+                        cp_async4(S_st1(a) + (size_t)ii * Bp + b,
+                                  a.drives + ((size_t)t * a.n_in + S_sslot(a)[i]) * a.B + b);
                 }
             }
             cp_async_commit();
@@ -881,8 +900,10 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         if (c.stage) cp_async_wait_all();
         __syncthreads();
         if (warp == 0 && c.publish) publish_carry(a, c, phase_id);
-        if (BWD) finish_bwd<THREADS>(a, c, s, phase_id);
-        else finish_fwd<THREADS>(a, c, s, phase_id);
+        fold_carries<THREADS>(a, c);
+        __syncthreads();
+        if (BWD) finish_bwd<THREADS>(a, c, pb, s, phase_id);
+        else finish_fwd<THREADS>(a, c, pb, s, phase_id);
         if (it + 1 < a.s_count)
             if (!grid_sync(a, nbar++, &s_ok)) return;
     }
@@ -892,19 +913,19 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         if (!BWD) {
             for (int t = 0; t < a.T; ++t)
                 from_rows<THREADS>(a.out + (size_t)t * a.B * N, a.H + (size_t)(t + 1) * a.M * NBp,
-                                   c.r0, c.r0 + c.nrows, a.B, Bp, N, c.tile);
+                                   c.r0, c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
         } else {
             if (c.stage) {
-                for (int j = tid; j < c.nrows * Bp; j += THREADS) a.G_[(size_t)c.r0 * Bp + j] = c.st0[j];
+                for (int j = tid; j < c.nrows * Bp; j += THREADS) a.G_[(size_t)c.r0 * Bp + j] = S_st0(a)[j];
                 for (int i = tid; i < c.nrows; i += THREADS) {
-                    a.dleak[c.r0 + i] = c.acc[i].x;
-                    a.dbias[c.r0 + i] = c.acc[i].y;
+                    a.dleak[c.r0 + i] = S_acc(a)[i].x;
+                    a.dbias[c.r0 + i] = S_acc(a)[i].y;
                 }
                 __syncthreads();
             }
-            from_rows<THREADS>(a.dstate0, a.G_, c.r0, c.r0 + c.nrows, a.B, Bp, N, c.tile);
+            from_rows<THREADS>(a.dstate0, a.G_, c.r0, c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
             for (int k = c.e0 + tid; k < c.e1; k += THREADS)
-                a.dw[__ldg(a.perm + k)] = SMEMG ? c.sdw[k - c.e0] : a.dwperm[k];
+                a.dw[__ldg(a.perm + k)] = SMEMG ? S_sdw(a)[k - c.e0] : a.dwperm[k];
         }
     }
 }
