@@ -557,7 +557,7 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
         for (int el = 0; el < 4; ++el) {
             const int i = i0 + pb.ri[el], cc = cb * pb.cpb + pb.ci[el], b = cc * 32 + lane;
             ok[el] = pb.ri[el] < pb.RB && i >= lo && i < hi && cc < pb.NCH && b < Bp;
-            ii[el] = ok[el] ? i : lo;
+            ii[el] = ok[el] ? i : hi - 1;  // an initialised row, read but not used
             bb[el] = ok[el] ? b : 0;
         }
 #pragma unroll
@@ -569,10 +569,10 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
             dr[el] = 0.f;
             if (c.stage) {
                 const int j = S_inp(a)[ii[el]];
-                if (j >= 0 && bb[el] < B) dr[el] = S_st1(a)[(size_t)j * Bp + bb[el]];
+                if (ok[el] && j >= 0 && bb[el] < B) dr[el] = S_st1(a)[(size_t)j * Bp + bb[el]];
             } else {
                 const int sl = S_sslot(a)[ii[el]];
-                if (sl >= 0 && bb[el] < B)
+                if (ok[el] && sl >= 0 && bb[el] < B)
                     dr[el] = __ldg(a.drives + ((size_t)t * a.n_in + sl) * B + bb[el]);
             }
         }
@@ -641,7 +641,7 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
         for (int el = 0; el < 4; ++el) {
             const int i = i0 + pb.ri[el], cc = cb * pb.cpb + pb.ci[el], b = cc * 32 + lane;
             ok[el] = pb.ri[el] < pb.RB && i >= lo && i < hi && cc < pb.NCH && b < Bp;
-            ii[el] = ok[el] ? i : lo;
+            ii[el] = ok[el] ? i : hi - 1;  // an initialised row, read but not used
             bb[el] = ok[el] ? b : 0;
         }
 #pragma unroll
