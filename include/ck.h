@@ -165,6 +165,39 @@ ck_status ck_backward(const ck_graph *g, const float *edge_values, const float *
                       float *d_state0, void *scratch, size_t scratch_bytes, void *stream);
 
 /*
+ * ck_forward_static_scratch -- ck_forward without a scratch buffer: the
+ * temporary workspace comes from a 32 MiB array of device memory compiled into
+ * the library.  The pages have no counterpart for this call; it exists for
+ * callers that cannot allocate device memory when they run the forward, such
+ * as a plugin inside a host application whose memory manager owns the device
+ * and refuses allocations it did not make, or a control loop that must not
+ * allocate once running.  The caller still passes every input and output
+ * (including `saved`, sized by ck_workspace_size) with the meanings of
+ * ck_forward; `saved` then feeds ck_backward as usual.
+ *
+ *   - Allocates nothing and calls no allocating routine.
+ *   - Every GPU that loads the library holds the 32 MiB array until the process
+ *     exits.  The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array: two calls whose work overlaps on the GPU
+ *     (different streams, different threads) race and corrupt each other.
+ *     Each call clears the words that must start at zero; the rest of the
+ *     array keeps the previous call's contents until overwritten.
+ *   - Shapes whose forward workspace exceeds the array (control words, one
+ *     carry row per SM, one float per edge and per padded node-batch element)
+ *     are refused with CK_ERR_UNSUPPORTED and a message giving both sizes.
+ *   - Device-side wait timeouts are not reported by this call (ck_query_status
+ *     needs a caller-owned scratch buffer).
+ * Errors: CK_ERR_INVALID_ARG, CK_ERR_WORKSPACE, CK_ERR_UNSUPPORTED, CK_ERR_CUDA.
+ */
+ck_status ck_forward_static_scratch(const ck_graph *g, const float *edge_values,
+                                    const float *leak, const float *bias, const float *drives,
+                                    const float *state0, int64_t B, int64_t T,
+                                    int64_t microsteps, float *states_out, void *saved,
+                                    size_t saved_bytes, void *stream);
+
+/*
  * ck_query_status -- synchronise `stream` and report whether the last
  * ck_forward / ck_backward that used `scratch` finished every device-side wait:
  * CK_OK, or CK_ERR_TIMEOUT if a bounded wait gave up (its kernel then stopped

@@ -56,6 +56,7 @@ def load() -> ctypes.CDLL:
         "ck_backward": [p, p, p, i64, i64, i64, p, sz, p, p, p, p, p, p, p, sz, p],
         "ck_query_status": [p, p],
         "ck_set_option": [ctypes.c_int, i64],
+        "ck_forward_static_scratch": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p],
         "ck_probe_read": [p, sz, i64, p, p],
         "ck_probe_gather": [p, i64, i64, p, i64, p, p],
     }
@@ -163,6 +164,20 @@ def ck_backward(handle, edge_values, leak, B, T, microsteps, saved, d_states, d_
                               _ptr(d_drives) if d_drives is not None and d_drives.numel() else None,
                               _ptr(d_state0), _ptr(scratch),
                               scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def ck_forward_static_scratch(handle, edge_values, leak, bias, drives, state0, microsteps,
+                              states_out, saved, stream=None):
+    for t, n in ((edge_values, "edge_values"), (leak, "leak"), (bias, "bias"),
+                 (drives, "drives"), (state0, "state0"), (states_out, "states_out")):
+        _need(t, torch.float32, n)
+    B = state0.shape[0]
+    T = states_out.shape[0]
+    _check(load().ck_forward_static_scratch(
+        handle, _ptr(edge_values), _ptr(leak), _ptr(bias),
+        _ptr(drives) if drives is not None and drives.numel() else None, _ptr(state0), B, T,
+        microsteps, _ptr(states_out), _ptr(saved), saved.numel() * saved.element_size(),
+        _stream(stream)))
 
 
 def ck_query_status(scratch, stream=None):
