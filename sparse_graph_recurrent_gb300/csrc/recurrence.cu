@@ -497,27 +497,20 @@ __device__ __forceinline__ PB make_pb(int Bp) {
     return p;
 }
 
-// Fold the carries of the groups that hold a row's earlier edges into its
-// slot, for every row of the CTA, in group order; rows with no edges here get
-// 0.  All threads of the CTA take part.
-template <int THREADS>
-__device__ __forceinline__ void fold_carries(const KArgs &a, const Cta &c) {
-    const int Bp = a.Bp, n = c.nrows * Bp;
-    for (int x = threadIdx.x; x < n; x += THREADS) {
-        const int i = x / Bp, b = x - i * Bp;
-        const int gr = S_sgrp(a)[i];
-        float *slot = c.rows + (size_t)i * Bp + b;
-        if (gr < 0) {
-            *slot = 0.f;
-        } else {
-            const int ga = gr >> 16, gb = gr & 0xffff;
-            if (ga < gb) {
-                float v = a.rs_smem ? *slot : __ldcg(slot);
-                for (int u = ga; u < gb; ++u) v += S_scarry(a)[(size_t)u * Bp + b];
-                *slot = v;
-            }
-        }
-    }
+// Row i's sum for column b: its slot (the part summed by the group holding its
+// last edge here), then the carries of the groups holding its earlier edges,
+// in group order; 0 for a row with no edges in this CTA.
+__device__ __forceinline__ float row_sum(const KArgs &a, const Cta &c, int i, int b) {
+    const int gr = S_sgrp(a)[i];
+    const size_t o = (size_t)i * a.Bp + b;
+    float x = gr < 0 ? 0.f : (a.rs_smem ? c.rows[o] : __ldcg(c.rows + o));
+    const int ga = gr >> 16, gb = gr < 0 ? 0 : (gr & 0xffff);
+    const float *sc = S_scarry(a) + b;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        if (ga + u < gb) x += sc[(size_t)(ga + u) * a.Bp];
+    for (int u = ga + 8; u < gb; ++u) x += sc[(size_t)u * a.Bp];
+    return x;
 }
 
 // Carries published by earlier CTAs for column b of the CTA's first row.
@@ -563,7 +556,7 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
 #pragma unroll
         for (int el = 0; el < 4; ++el) {
             const size_t o = (size_t)ii[el] * Bp + bb[el];
-            x[el] = a.rs_smem ? c.rows[o] : __ldcg(c.rows + o);
+            x[el] = row_sum(a, c, ii[el], bb[el]);
             pr[el] = S_prm(a)[ii[el]];
             hp[el] = c.stage ? S_st0(a)[o] : __ldcg(hin + (size_t)c.r0 * Bp + o);
             dr[el] = 0.f;
@@ -648,7 +641,7 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
         for (int el = 0; el < 4; ++el) {
             const size_t o = (size_t)ii[el] * Bp + bb[el];
             lam[el] = S_prm(a)[ii[el]].x;
-            x[el] = pro ? 0.f : (a.rs_smem ? c.rows[o] : __ldcg(c.rows + o));
+            x[el] = pro ? 0.f : row_sum(a, c, ii[el], bb[el]);
             if (c.stage) {
                 gv[el] = pro ? 0.f : S_st0(a)[o];
                 ov[el] = step_end ? S_st3(a)[o] : 0.f;
@@ -696,12 +689,33 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
         }
     }
     if (q >= 0) {
+        // sum the eight values {dl, db} x 4 rows over the warp: three halving
+        // exchanges (lane bits 4, 3, 2) split the values among lanes, two more
+        // (bits 1, 0) finish the sums
+        float v[8] = {dl[0], dl[1], dl[2], dl[3], db[0], db[1], db[2], db[3]};
+#pragma unroll
+        for (int o = 4, m = 16; o >= 1; o >>= 1, m >>= 1) {
+#pragma unroll
+            for (int j = 0; j < o; ++j) {
+                const bool up = (lane & m) != 0;
+                const float keep = up ? v[j + o] : v[j];
+                const float send = up ? v[j] : v[j + o];
+                v[j] = keep + __shfl_xor_sync(kFull, send, m);
+            }
+        }
+        v[0] += __shfl_xor_sync(kFull, v[0], 2);
+        v[0] += __shfl_xor_sync(kFull, v[0], 1);
+        // lane l now holds value 4 bit4(l) + 2 bit3(l) + bit2(l)
+        float tot[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            tot[j] = __shfl_sync(kFull, v[0], ((j & 4) << 2) | ((j & 2) << 2) | ((j & 1) << 2));
 #pragma unroll
         for (int ri = 0; ri < 4; ++ri) {
             if (ri >= pb.RB) break;
             const int i = i0 + ri;
             if (i >= hi) break;
-            const float sl = warp_sum(dl[ri]), sb = warp_sum(db[ri]);
+            const float sl = tot[ri], sb = tot[4 + ri];
             if (i < lo || lane != 0) continue;
             if (c.stage) {
                 const float2 o = q == a.S - 1 ? make_float2(0.f, 0.f) : S_acc(a)[i];
@@ -899,9 +913,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         stream_piece<NC, SMEMG, BWD, UNR>(a, c, gam, lig, active, rows, a.H + (size_t)s * NBp);
         if (c.stage) cp_async_wait_all();
         __syncthreads();
-        if (warp == 0 && c.publish) publish_carry(a, c, phase_id);
-        fold_carries<THREADS>(a, c);
-        __syncthreads();
+        if (warp == THREADS / 32 - 2 && c.publish) publish_carry(a, c, phase_id);
         if (BWD) finish_bwd<THREADS>(a, c, pb, s, phase_id);
         else finish_fwd<THREADS>(a, c, pb, s, phase_id);
         if (it + 1 < a.s_count)
