@@ -115,11 +115,6 @@ __device__ __forceinline__ float dot4(const float4 &a, const float4 &b, float d)
     d = fmaf(a.z, b.z, d);
     return fmaf(a.w, b.w, d);
 }
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
-}
 
 // Grid-wide barrier, bounded by a.timeout_ns.  Each CTA adds one to a
 // counter that only grows within a call; barrier idx waits for its total.
@@ -504,7 +499,7 @@ __device__ __forceinline__ float row_sum(const KArgs &a, const Cta &c, int i, in
     const int gr = S_sgrp(a)[i];
     const size_t o = (size_t)i * a.Bp + b;
     float x = gr < 0 ? 0.f : (a.rs_smem ? c.rows[o] : __ldcg(c.rows + o));
-    const int ga = gr >> 16, gb = gr < 0 ? 0 : (gr & 0xffff);
+    const int ga = gr < 0 ? 0 : gr >> 16, gb = gr < 0 ? 0 : (gr & 0xffff);
     const float *sc = S_scarry(a) + b;
 #pragma unroll
     for (int u = 0; u < 8; ++u)
