@@ -40,6 +40,7 @@
 // once per call; otherwise it streams from global memory every microstep.
 #include <algorithm>
 #include <cstring>
+#include <type_traits>
 
 #include "ck_internal.h"
 
@@ -495,10 +496,11 @@ __device__ __forceinline__ PB make_pb(int Bp) {
 // Row i's sum for column b: its slot (the part summed by the group holding its
 // last edge here), then the carries of the groups holding its earlier edges,
 // in group order; 0 for a row with no edges in this CTA.
+template <bool RS>
 __device__ __forceinline__ float row_sum(const KArgs &a, const Cta &c, int i, int b) {
     const int gr = S_sgrp(a)[i];
     const size_t o = (size_t)i * a.Bp + b;
-    float x = gr < 0 ? 0.f : (a.rs_smem ? c.rows[o] : __ldcg(c.rows + o));
+    float x = gr < 0 ? 0.f : (RS ? c.rows[o] : __ldcg(c.rows + o));
     const int ga = gr < 0 ? 0 : gr >> 16, gb = gr < 0 ? 0 : (gr & 0xffff);
     const float *sc = S_scarry(a) + b;
 #pragma unroll
@@ -523,9 +525,25 @@ __device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes & ~15u) : "memory");
 }
 
+// Call f with the staging and row-sum placement as compile-time flags, so the
+// finish code has no per-element branches on them.
+template <class F>
+__device__ __forceinline__ void dispatch_modes(bool stage, bool rs, F &&f) {
+    using T = std::true_type;
+    using Fl = std::false_type;
+    if (stage) {
+        if (rs) f(T{}, T{});
+        else f(T{}, Fl{});
+    } else {
+        if (rs) f(Fl{}, T{});
+        else f(Fl{}, Fl{});
+    }
+}
+
 // Forward finish of rows [lo, hi) among the batch starting at row i0:
 // pre-activation, tanh, leak blend, saved copies.  Straight-line over the
 // batch's elements so their loads and tanh evaluations overlap.
+template <bool ST, bool RS>
 __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, const PB &pb,
                                                  int s, unsigned phase_id, int i0, int lo,
                                                  int hi) {
@@ -551,11 +569,11 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
 #pragma unroll
         for (int el = 0; el < 4; ++el) {
             const size_t o = (size_t)ii[el] * Bp + bb[el];
-            x[el] = row_sum(a, c, ii[el], bb[el]);
+            x[el] = row_sum<RS>(a, c, ii[el], bb[el]);
             pr[el] = S_prm(a)[ii[el]];
-            hp[el] = c.stage ? S_st0(a)[o] : __ldcg(hin + (size_t)c.r0 * Bp + o);
+            hp[el] = ST ? S_st0(a)[o] : __ldcg(hin + (size_t)c.r0 * Bp + o);
             dr[el] = 0.f;
-            if (c.stage) {
+            if (ST) {
                 const int j = S_inp(a)[ii[el]];
                 if (ok[el] && j >= 0 && bb[el] < B) dr[el] = S_st1(a)[(size_t)j * Bp + bb[el]];
             } else {
@@ -581,7 +599,7 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
             const float a0 = live ? av[el] : 0.f;
             if (ok[el]) {
                 const size_t o = (size_t)ii[el] * Bp + bb[el];
-                if (c.stage) S_st0(a)[o] = hv;
+                if (ST) S_st0(a)[o] = hv;
                 hout[(size_t)c.r0 * Bp + o] = hv;
                 __stcs(aout + (size_t)c.r0 * Bp + o, a0);
             }
@@ -595,15 +613,20 @@ __device__ void finish_fwd(const KArgs &a, const Cta &c, const PB &pb, int s, un
     const int warp = threadIdx.x >> 5;
     // a first row that waits for earlier CTAs' carries goes last, to the last warp
     const int lo = c.glob ? 1 : 0;
-    for (int i0 = warp * pb.RB; i0 < c.nrows; i0 += U * pb.RB)
-        finish_fwd_batch(a, c, pb, s, phase_id, i0, lo, c.nrows);
-    if (c.glob && warp == U - 1) finish_fwd_batch(a, c, pb, s, phase_id, 0, 0, 1);
+    auto run = [&](auto st, auto rs) {
+        constexpr bool ST = decltype(st)::value, RS = decltype(rs)::value;
+        for (int i0 = warp * pb.RB; i0 < c.nrows; i0 += U * pb.RB)
+            finish_fwd_batch<ST, RS>(a, c, pb, s, phase_id, i0, lo, c.nrows);
+        if (c.glob && warp == U - 1) finish_fwd_batch<ST, RS>(a, c, pb, s, phase_id, 0, 0, 1);
+    };
+    dispatch_modes(c.stage, a.rs_smem != 0, run);
 }
 
 // Backward finish of rows [lo, hi) among the batch at i0, for microstep s:
 // G_{s-1} = G_s (1 - leak) + row total (+ dOut of the step ending at s-1),
 // then the elementwise terms of microstep q = s-1.  s == S is the prologue
 // (G_{S-1} = dOut[T-1]); s == 0 leaves G_{-1} for the transpose into d_state0.
+template <bool ST, bool RS>
 __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, const PB &pb,
                                                  int s, unsigned phase_id, int i0, int lo,
                                                  int hi) {
@@ -636,8 +659,8 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
         for (int el = 0; el < 4; ++el) {
             const size_t o = (size_t)ii[el] * Bp + bb[el];
             lam[el] = S_prm(a)[ii[el]].x;
-            x[el] = pro ? 0.f : row_sum(a, c, ii[el], bb[el]);
-            if (c.stage) {
+            x[el] = pro ? 0.f : row_sum<RS>(a, c, ii[el], bb[el]);
+            if (ST) {
                 gv[el] = pro ? 0.f : S_st0(a)[o];
                 ov[el] = step_end ? S_st3(a)[o] : 0.f;
                 av[el] = q >= 0 ? S_st1(a)[o] : 0.f;
@@ -666,7 +689,7 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
         for (int el = 0; el < 4; ++el) {
             if (!ok[el]) continue;
             const size_t o = (size_t)ii[el] * Bp + bb[el];
-            if (c.stage) S_st0(a)[o] = gn[el];
+            if (ST) S_st0(a)[o] = gn[el];
             else a.G_[ro + o] = gn[el];
             if (q < 0) continue;
             const bool live = bb[el] < B;
@@ -712,7 +735,7 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
             if (i >= hi) break;
             const float sl = tot[ri], sb = tot[4 + ri];
             if (i < lo || lane != 0) continue;
-            if (c.stage) {
+            if (ST) {
                 const float2 o = q == a.S - 1 ? make_float2(0.f, 0.f) : S_acc(a)[i];
                 S_acc(a)[i] = make_float2(o.x + sl, o.y + sb);
             } else if (q == a.S - 1) {
@@ -732,9 +755,13 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, const PB &pb, int s, un
     const int warp = threadIdx.x >> 5;
     const bool defer = c.glob && s != a.S;  // the prologue has no carries to wait for
     const int lo = defer ? 1 : 0;
-    for (int i0 = warp * pb.RB; i0 < c.nrows; i0 += U * pb.RB)
-        finish_bwd_batch(a, c, pb, s, phase_id, i0, lo, c.nrows);
-    if (defer && warp == U - 1) finish_bwd_batch(a, c, pb, s, phase_id, 0, 0, 1);
+    auto run = [&](auto st, auto rs) {
+        constexpr bool ST = decltype(st)::value, RS = decltype(rs)::value;
+        for (int i0 = warp * pb.RB; i0 < c.nrows; i0 += U * pb.RB)
+            finish_bwd_batch<ST, RS>(a, c, pb, s, phase_id, i0, lo, c.nrows);
+        if (defer && warp == U - 1) finish_bwd_batch<ST, RS>(a, c, pb, s, phase_id, 0, 0, 1);
+    };
+    dispatch_modes(c.stage, a.rs_smem != 0, run);
 }
 
 // Publish this CTA's carry for the row its piece ends inside (row r0 + nrows):
