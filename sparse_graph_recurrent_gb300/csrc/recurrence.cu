@@ -228,7 +228,7 @@ __device__ void from_rows(float *__restrict__ dst, const float *__restrict__ src
 //   prm    {leak, bias} of rows r0 + i;  sslot: their input slots
 //   sgrp   groups [ga, gb) whose carries belong to row r0 + i, ga << 16 | gb
 //   scarry [G][Bp] group carries;  tile: [32][33] transpose tile
-//   rec    one 16-byte record per edge of the CTA: {col, w bits, row, edge-gradient sum bits}
+//   scw, srow, sdw   {col, w bits}, row and edge-gradient sum of the CTA's edges
 //   stage mode, rows r0 + i:
 //     forward:  st0 = current state (resident), st1 = drives of the CTA's
 //               input rows for the current input step (row inp[i])
@@ -250,7 +250,9 @@ __device__ __forceinline__ int *S_sslot(const KArgs &a) { return reinterpret_cas
 __device__ __forceinline__ int *S_sgrp(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_grp); }
 __device__ __forceinline__ float *S_scarry(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_carry); }
 __device__ __forceinline__ float *S_tile(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_tile); }
-__device__ __forceinline__ int4 *S_rec(const KArgs &a) { return reinterpret_cast<int4 *>(ck_smem + a.o_cw); }
+__device__ __forceinline__ int2 *S_scw(const KArgs &a) { return reinterpret_cast<int2 *>(ck_smem + a.o_cw); }
+__device__ __forceinline__ int *S_srow(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_row); }
+__device__ __forceinline__ float *S_sdw(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_dw); }
 __device__ __forceinline__ float *S_st0(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st0); }
 __device__ __forceinline__ float *S_st1(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st1); }
 __device__ __forceinline__ float *S_st2(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st2); }
@@ -299,37 +301,22 @@ struct Batch {
     float4 v[UNR][NC];
 };
 
-// Sum of d over the LPE lanes of each group.  When LPE is a power of two that
-// divides UNR, each block of LPE values is reduced by one exchange per
-// halving, leaving lane lig with the total of item (block * LPE + lig) in
-// d[block]; otherwise each item is reduced by a tree and lane 0 holds it.
-template <int UNR>
-__device__ __forceinline__ bool butterfly_ok(int lpe) {
-    return (lpe & (lpe - 1)) == 0 && lpe <= UNR && UNR % lpe == 0;
-}
-
+// Sum of d over the LPE lanes of each group.  With LPE == UNR (a power of two)
+// one exchange per halving leaves lane lig holding the total of item lig;
+// otherwise each item is reduced by a tree and lane 0 holds it.
 template <int UNR>
 __device__ __forceinline__ void group_dots(float (&d)[UNR], int lig, int lpe, int lpe_p2) {
-    if (butterfly_ok<UNR>(lpe)) {
-        // blocks of lpe values; o runs over lpe/2 .. 1
+    if (lpe == UNR && (UNR & (UNR - 1)) == 0) {
 #pragma unroll
         for (int o = UNR / 2; o >= 1; o >>= 1) {
-            if (o >= lpe) continue;
 #pragma unroll
-            for (int blk = 0; blk < UNR; blk += 2 * o) {
-                // within the block starting at blk (size lpe), values j and j + o
-#pragma unroll
-                for (int j = 0; j < o; ++j) {
-                    const int lo_i = blk + j, hi_i = blk + j + o;
-                    if (hi_i >= UNR) continue;
-                    const bool hi = (lig & o) != 0;
-                    const float keep = hi ? d[hi_i] : d[lo_i];
-                    const float send = hi ? d[lo_i] : d[hi_i];
-                    d[lo_i] = keep + __shfl_xor_sync(kFull, send, o);
-                }
+            for (int j = 0; j < o; ++j) {
+                const bool hi = (lig & o) != 0;
+                const float keep = hi ? d[j + o] : d[j];
+                const float send = hi ? d[j] : d[j + o];
+                d[j] = keep + __shfl_xor_sync(kFull, send, o);
             }
         }
-        // the total of item (block * lpe + lig) is now in d[block * lpe]
     } else {
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
@@ -354,7 +341,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     }
     const int len = k1 - k0;
     const int trips = (__reduce_max_sync(kFull, (unsigned)len) + UNR - 1) / UNR;
-    auto row_at = [&](int k) -> int { return SMEMG ? S_rec(a)[k - c.e0].z : __ldg(a.rowid + k); };
+    auto row_at = [&](int k) -> int { return SMEMG ? S_srow(a)[k - c.e0] : __ldg(a.rowid + k); };
     int cur = len > 0 ? row_at(k0) : -1;
     float4 acc[NC];
 #pragma unroll
@@ -401,10 +388,10 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             bt.w[q] = 0.f;
             if (ok) {
                 if (SMEMG) {
-                    const int4 r = S_rec(a)[kk - c.e0];
-                    cc = r.x;
-                    bt.w[q] = __int_as_float(r.y);
-                    bt.rid[q] = r.z;
+                    const int2 cw = S_scw(a)[kk - c.e0];
+                    cc = cw.x;
+                    bt.w[q] = __int_as_float(cw.y);
+                    bt.rid[q] = S_srow(a)[kk - c.e0];
                 } else {
                     cc = __ldg(a.col + kk);
                     bt.w[q] = __ldcg(a.wperm + kk);
@@ -445,22 +432,18 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
         }
         if (BWD) {
             group_dots<UNR>(d, lig, a.LPE, a.LPE_P2);
-            if (butterfly_ok<UNR>(a.LPE)) {
-#pragma unroll
-                for (int blk = 0; blk < UNR; blk += 1) {
-                    if (blk % a.LPE != 0) continue;
-                    const int kk = kb + blk + lig;
-                    if (kk < k1) {
-                        if (SMEMG) reinterpret_cast<float *>(&S_rec(a)[kk - c.e0].w)[0] += d[blk];
-                        else a.dwperm[kk] += d[blk];
-                    }
+            if (a.LPE == UNR && (UNR & (UNR - 1)) == 0) {
+                const int kk = kb + lig;
+                if (kk < k1) {
+                    if (SMEMG) S_sdw(a)[kk - c.e0] += d[0];
+                    else a.dwperm[kk] += d[0];
                 }
             } else if (lig == 0) {
 #pragma unroll
                 for (int q = 0; q < UNR; ++q) {
                     const int kk = kb + q;
                     if (kk < k1) {
-                        if (SMEMG) reinterpret_cast<float *>(&S_rec(a)[kk - c.e0].w)[0] += d[q];
+                        if (SMEMG) S_sdw(a)[kk - c.e0] += d[q];
                         else a.dwperm[kk] += d[q];
                     }
                 }
@@ -865,8 +848,9 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     }
     for (int k = c.e0 + tid; k < c.e1; k += THREADS) {
         if (SMEMG) {
-            S_rec(a)[k - c.e0] = make_int4(__ldg(a.col + k), __float_as_int(__ldg(a.w + __ldg(a.perm + k))),
-                                           __ldg(a.rowid + k), 0);
+            S_scw(a)[k - c.e0] = make_int2(__ldg(a.col + k), __float_as_int(__ldg(a.w + __ldg(a.perm + k))));
+            S_srow(a)[k - c.e0] = __ldg(a.rowid + k);
+            if (BWD) S_sdw(a)[k - c.e0] = 0.f;
         } else if (a.do_prologue) {
             a.wperm[k] = __ldg(a.w + __ldg(a.perm + k));
             if (BWD) a.dwperm[k] = 0.f;
@@ -975,7 +959,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
             }
             from_rows<THREADS>(a.dstate0, a.G_, c.r0, c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
             for (int k = c.e0 + tid; k < c.e1; k += THREADS)
-                a.dw[__ldg(a.perm + k)] = SMEMG ? __int_as_float(S_rec(a)[k - c.e0].w) : a.dwperm[k];
+                a.dw[__ldg(a.perm + k)] = SMEMG ? S_sdw(a)[k - c.e0] : a.dwperm[k];
         }
     }
 }
@@ -1017,15 +1001,16 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     L.o_tile = (int)o; o = align16(o + 4 * 32 * 33);
     const size_t budget = kMaxSmem - kStaticSmem - 1024;
     const size_t rows_b = align16(4 * (size_t)rc * p.Bp);
-    const size_t graph_b = 16 * (size_t)p.cap[dir] + 48;
+    const size_t graph_b = (dir == 0 ? 12 : 16) * (size_t)p.cap[dir] + 48;
     // finish operands: forward state + drives; backward G, A, H, dOut + two sums
     const size_t stage_b = (dir == 0 ? 2 : 4) * rows_b + align16(8 * (size_t)rc) + align16(4 * (size_t)rc);
     L.rows = o + rows_b <= budget;
     if (L.rows) o += rows_b;
     L.o_rows = (int)(o - (L.rows ? rows_b : 0));
     L.graph = want_graph && o + graph_b <= budget;
-    L.o_cw = (int)o; o = align16(o + (L.graph ? 16 * (size_t)p.cap[dir] : 0));
-    L.o_row = L.o_dw = (int)o;
+    L.o_cw = (int)o; o = align16(o + (L.graph ? 8 * (size_t)p.cap[dir] : 0));
+    L.o_row = (int)o; o = align16(o + (L.graph ? 4 * (size_t)p.cap[dir] : 0));
+    L.o_dw = (int)o; o = align16(o + (L.graph && dir == 1 ? 4 * (size_t)p.cap[dir] : 0));
     L.stage = want_stage && o + stage_b <= budget;
     const size_t sb = L.stage ? rows_b : 0;
     L.o_st0 = (int)o; o += sb;
