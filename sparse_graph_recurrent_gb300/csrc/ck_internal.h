@@ -68,7 +68,6 @@ struct Plan {
     size_t off_G;       // float [N][Bp]
     size_t off_da;      // float [2][N][Bp]
     size_t off_rowsum;  // float [N][Bp]
-    size_t off_doutT;   // float [T][N][Bp]
     size_t scratch_bytes;
     size_t saved_bytes; // float [(S+1) + S][N][Bp]
 };

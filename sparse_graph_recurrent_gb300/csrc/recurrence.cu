@@ -17,7 +17,8 @@
 //   A[s][N][Bp]    pre-activation of microstep s
 //   G[N][Bp]       running state gradient (backward)
 //   da[2][N][Bp]   d(loss)/d(pre-activation), ping-pong between microsteps
-//   dOutT[T][N][Bp]  dOut transposed once at the start of the backward
+// The caller's [T][B][N] outputs and output gradients are read and written one
+// input step at a time, transposed through shared memory when staging is on.
 //
 // Work split.  One CTA per SM and one persistent cooperative launch per call;
 // microsteps are separated by a grid-wide barrier whose wait is bounded.  CTA
@@ -66,7 +67,6 @@ struct KArgs {
     float *out;
     float *H, *A;
     const float *dout;
-    float *doutT;
     float *dw, *dleak, *dbias, *ddrives, *dstate0;
     float *G_, *da, *rowsum_g;
     unsigned *bar;
@@ -230,10 +230,12 @@ __device__ void from_rows(float *__restrict__ dst, const float *__restrict__ src
 //   scarry [G][Bp] group carries;  tile: [32][33] transpose tile
 //   scw, srow, sdw   {col, w bits}, row and edge-gradient sum of the CTA's edges
 //   stage mode, rows r0 + i:
-//     forward:  st0 = current state (resident), st1 = drives of the CTA's
-//               input rows for the current input step (row inp[i])
-//     backward: st0 = G (resident), st1 = A[q], st2 = H[q], st3 = dOut[t(q)],
-//               acc = {d_leak, d_bias} running sums (resident)
+//     forward:  st0 = current state (resident, row stride Bp + 1), st1 =
+//               drives of the CTA's input rows for the current input step
+//               (row inp[i])
+//     backward: st0 = G (resident), st1 = A[q], st2 = H[q], st3 = dOut[t(q)]
+//               (row stride Bp + 1), acc = {d_leak, d_bias} running sums
+//               (resident)
 struct Cta {
     float *rows;  // [nrows][Bp] row slots (shared or global)
     bool stage;
@@ -259,6 +261,10 @@ __device__ __forceinline__ float *S_st2(const KArgs &a) { return reinterpret_cas
 __device__ __forceinline__ float *S_st3(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st3); }
 __device__ __forceinline__ int *S_inp(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_inp); }
 __device__ __forceinline__ float2 *S_acc(const KArgs &a) { return reinterpret_cast<float2 *>(ck_smem + a.o_acc); }
+// Row stride of the staged arrays that are also read or written across rows
+// (forward st0, backward st3): Bp + 1 words, so a warp walking down a column
+// touches 32 distinct banks as well as one walking along a row.
+__device__ __forceinline__ int pstride(const KArgs &a) { return a.Bp + 1; }
 
 
 __device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc) {
@@ -277,6 +283,29 @@ template <int THREADS>
 __device__ __forceinline__ void stage_rows(float *sdst, const float *gsrc, int nrows, int Bp) {
     const int n16 = nrows * Bp / 4;
     for (int j = threadIdx.x; j < n16; j += THREADS) cp_async16(sdst + 4 * j, gsrc + 4 * j);
+}
+
+// Copy dOut of input step t for this CTA's rows (a [B][N] slab, rows r0 + i
+// contiguous per column) into st3 as rows of stride Bp + 1: consecutive
+// threads read consecutive nodes of one column.
+template <int THREADS>
+__device__ __forceinline__ void stage_dout(const KArgs &a, const Cta &c, int t) {
+    const float *src = a.dout + (size_t)t * a.B * a.N + c.r0;
+    for (int j = threadIdx.x; j < c.nrows * a.B; j += THREADS) {
+        const int b = j / c.nrows, i = j - b * c.nrows;
+        cp_async4(S_st3(a) + i * pstride(a) + b, src + (size_t)b * a.N + i);
+    }
+}
+
+// Write the state held in st0 to output step t ([B][N] slab): consecutive
+// threads write consecutive nodes of one column.
+template <int THREADS>
+__device__ __forceinline__ void write_out(const KArgs &a, const Cta &c, int t) {
+    float *dst = a.out + (size_t)t * a.B * a.N + c.r0;
+    for (int j = threadIdx.x; j < c.nrows * a.B; j += THREADS) {
+        const int b = j / c.nrows, i = j - b * c.nrows;
+        __stcs(dst + (size_t)b * a.N + i, S_st0(a)[i * pstride(a) + b]);
+    }
 }
 
 // The lane group whose edge sub-range holds edge k of the CTA (n = e1 - e0 > 0).
@@ -542,7 +571,9 @@ __device__ __forceinline__ void dispatch_modes(bool stage, bool rs, F &&f) {
 
 // Forward finish of rows [lo, hi) among the batch starting at row i0:
 // pre-activation, tanh, leak blend, saved copies.  Straight-line over the
-// batch's elements so their loads and tanh evaluations overlap.
+// batch's elements so their loads and tanh evaluations overlap.  Without
+// staging, the state that ends an input step is also written to the output
+// here; with staging it is copied out of st0 during the next microstep.
 template <bool ST, bool RS>
 __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, const PB &pb,
                                                  int s, unsigned phase_id, int i0, int lo,
@@ -550,6 +581,7 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
     const int lane = threadIdx.x & 31;
     const int Bp = a.Bp, B = a.B;
     const int t = s / a.M;
+    const bool step_end = s - t * a.M == a.M - 1;
     const size_t NBp = (size_t)a.N * Bp;
     const float *hin = a.H + (size_t)s * NBp;
     float *hout = a.H + (size_t)(s + 1) * NBp;
@@ -571,7 +603,7 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
             const size_t o = (size_t)ii[el] * Bp + bb[el];
             x[el] = row_sum<RS>(a, c, ii[el], bb[el]);
             pr[el] = S_prm(a)[ii[el]];
-            hp[el] = ST ? S_st0(a)[o] : __ldcg(hin + (size_t)c.r0 * Bp + o);
+            hp[el] = ST ? S_st0(a)[ii[el] * pstride(a) + bb[el]] : __ldcg(hin + (size_t)c.r0 * Bp + o);
             dr[el] = 0.f;
             if (ST) {
                 const int j = S_inp(a)[ii[el]];
@@ -599,7 +631,9 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
             const float a0 = live ? av[el] : 0.f;
             if (ok[el]) {
                 const size_t o = (size_t)ii[el] * Bp + bb[el];
-                if (ST) S_st0(a)[o] = hv;
+                if (ST) S_st0(a)[ii[el] * pstride(a) + bb[el]] = hv;
+                else if (step_end && live)
+                    __stcs(a.out + ((size_t)t * B + bb[el]) * a.N + c.r0 + ii[el], hv);
                 hout[(size_t)c.r0 * Bp + o] = hv;
                 __stcs(aout + (size_t)c.r0 * Bp + o, a0);
             }
@@ -641,7 +675,7 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
     const size_t ro = (size_t)c.r0 * Bp;
     const float *Aq = a.A + (size_t)(q >= 0 ? q : 0) * NBp + ro;
     const float *Hq = a.H + (size_t)(q >= 0 ? q : 0) * NBp + ro;
-    const float *dO = a.doutT + (size_t)tq * NBp + ro;
+    const float *dO = a.dout + (size_t)tq * B * a.N + c.r0;  // [B][N] slab of step tq
     float *daq = a.da + (size_t)(q & 1) * NBp + ro;
     float dl[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
     for (int cb = 0; cb < pb.CB; ++cb) {
@@ -662,12 +696,12 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
             x[el] = pro ? 0.f : row_sum<RS>(a, c, ii[el], bb[el]);
             if (ST) {
                 gv[el] = pro ? 0.f : S_st0(a)[o];
-                ov[el] = step_end ? S_st3(a)[o] : 0.f;
+                ov[el] = step_end && bb[el] < B ? S_st3(a)[ii[el] * pstride(a) + bb[el]] : 0.f;
                 av[el] = q >= 0 ? S_st1(a)[o] : 0.f;
                 hv[el] = q >= 0 ? S_st2(a)[o] : 0.f;
             } else {
                 gv[el] = pro ? 0.f : __ldcg(a.G_ + ro + o);
-                ov[el] = step_end ? __ldcg(dO + o) : 0.f;
+                ov[el] = step_end && bb[el] < B ? __ldg(dO + (size_t)bb[el] * a.N + ii[el]) : 0.f;
                 av[el] = q >= 0 ? __ldcs(Aq + o) : 0.f;
                 hv[el] = q >= 0 ? __ldg(Hq + o) : 0.f;
             }
@@ -873,18 +907,17 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         if (!BWD) {
             to_rows<THREADS>(a.H, a.state0, c.r0, c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
             if (c.stage) {
-                for (int j = tid; j < c.nrows * Bp; j += THREADS)
-                    S_st0(a)[j] = __ldcg(a.H + (size_t)c.r0 * Bp + j);
+                for (int j = tid; j < c.nrows * Bp; j += THREADS) {
+                    const int i = j / Bp, b = j - i * Bp;
+                    S_st0(a)[i * pstride(a) + b] = __ldcg(a.H + (size_t)c.r0 * Bp + j);
+                }
             }
         } else {
-            for (int t = 0; t < a.T; ++t)
-                to_rows<THREADS>(a.doutT + (size_t)t * NBp, a.dout + (size_t)t * a.B * N, c.r0,
-                                 c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
             if (c.stage) {
                 const size_t ro = (size_t)c.r0 * Bp;
                 stage_rows<THREADS>(S_st1(a), a.A + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
                 stage_rows<THREADS>(S_st2(a), a.H + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
-                stage_rows<THREADS>(S_st3(a), a.doutT + (size_t)(a.T - 1) * NBp + ro, c.nrows, Bp);
+                stage_dout<THREADS>(a, c, a.T - 1);
                 cp_async_wait_all();
             }
             __syncthreads();
@@ -904,8 +937,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
                 const int q = s - 1, tq = q / a.M;
                 stage_rows<THREADS>(S_st1(a), a.A + (size_t)q * NBp + ro, c.nrows, Bp);
                 stage_rows<THREADS>(S_st2(a), a.H + (size_t)q * NBp + ro, c.nrows, Bp);
-                if (q - tq * a.M == a.M - 1)
-                    stage_rows<THREADS>(S_st3(a), a.doutT + (size_t)tq * NBp + ro, c.nrows, Bp);
+                if (q - tq * a.M == a.M - 1) stage_dout<THREADS>(a, c, tq);
             } else if (!BWD && c.n_inp > 0 && s % a.M == 0) {
                 const int t = s / a.M;
                 for (int j = tid; j < c.nrows * a.B; j += THREADS) {
@@ -917,6 +949,8 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
                 }
             }
             cp_async_commit();
+            // the state that ended the previous input step, still in st0
+            if (!BWD && s > 0 && s % a.M == 0) write_out<THREADS>(a, c, s / a.M - 1);
         } else if (tid == 0 && c.nrows > 0) {
             // part B's operands of this CTA's rows, fetched into L2 during part A
             const unsigned rb = (unsigned)((size_t)c.nrows * Bp * 4);
@@ -925,8 +959,6 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
                 if (s > 0) {
                     prefetch_l2(a.A + (size_t)(s - 1) * NBp + ro, rb);
                     prefetch_l2(a.H + (size_t)(s - 1) * NBp + ro, rb);
-                    const int q = s - 1, tq = q / a.M;
-                    if (q - tq * a.M == a.M - 1) prefetch_l2(a.doutT + (size_t)tq * NBp + ro, rb);
                 }
             } else {
                 prefetch_l2(a.H + (size_t)s * NBp + ro, rb);
@@ -945,9 +977,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     if (a.do_epilogue) {
         __syncthreads();
         if (!BWD) {
-            for (int t = 0; t < a.T; ++t)
-                from_rows<THREADS>(a.out + (size_t)t * a.B * N, a.H + (size_t)(t + 1) * a.M * NBp,
-                                   c.r0, c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
+            if (c.stage) write_out<THREADS>(a, c, a.T - 1);
         } else {
             if (c.stage) {
                 for (int j = tid; j < c.nrows * Bp; j += THREADS) a.G_[(size_t)c.r0 * Bp + j] = S_st0(a)[j];
@@ -1001,9 +1031,10 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     L.o_tile = (int)o; o = align16(o + 4 * 32 * 33);
     const size_t budget = kMaxSmem - kStaticSmem - 1024;
     const size_t rows_b = align16(4 * (size_t)rc * p.Bp);
+    const size_t rows_pb = align16(4 * (size_t)rc * (p.Bp + 1));  // row stride Bp + 1
     const size_t graph_b = (dir == 0 ? 12 : 16) * (size_t)p.cap[dir] + 48;
     // finish operands: forward state + drives; backward G, A, H, dOut + two sums
-    const size_t stage_b = (dir == 0 ? 2 : 4) * rows_b + align16(8 * (size_t)rc) + align16(4 * (size_t)rc);
+    const size_t stage_b = (dir == 0 ? 1 : 3) * rows_b + rows_pb + align16(8 * (size_t)rc) + align16(4 * (size_t)rc);
     L.rows = o + rows_b <= budget;
     if (L.rows) o += rows_b;
     L.o_rows = (int)(o - (L.rows ? rows_b : 0));
@@ -1012,11 +1043,11 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     L.o_row = (int)o; o = align16(o + (L.graph ? 4 * (size_t)p.cap[dir] : 0));
     L.o_dw = (int)o; o = align16(o + (L.graph && dir == 1 ? 4 * (size_t)p.cap[dir] : 0));
     L.stage = want_stage && o + stage_b <= budget;
-    const size_t sb = L.stage ? rows_b : 0;
-    L.o_st0 = (int)o; o += sb;
+    const size_t sb = L.stage ? rows_b : 0, spb = L.stage ? rows_pb : 0;
+    L.o_st0 = (int)o; o += dir == 0 ? spb : sb;
     L.o_st1 = (int)o; o += sb;
     L.o_st2 = (int)o; o += dir == 1 ? sb : 0;
-    L.o_st3 = (int)o; o += dir == 1 ? sb : 0;
+    L.o_st3 = (int)o; o += dir == 1 ? spb : 0;
     L.o_acc = (int)o; o = align16(o + (L.stage ? 8 * (size_t)rc : 0));
     L.o_inp = (int)o; o = align16(o + (L.stage ? 4 * (size_t)rc : 0));
     L.bytes = o;
@@ -1069,7 +1100,6 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.G_ = (float *)(sc + p.off_G);
     k.da = (float *)(sc + p.off_da);
     k.rowsum_g = (float *)(sc + p.off_rowsum);
-    k.doutT = (float *)(sc + p.off_doutT);
     k.bar_extra = (unsigned)options().barrier_extra;
     k.timeout_ns = (unsigned long long)options().timeout_ns;
 }
@@ -1171,8 +1201,6 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     off = align256(off + 8 * NBp);
     q.off_rowsum = off;
     off = align256(off + 4 * NBp);
-    q.off_doutT = off;
-    off = align256(off + 4 * NBp * (size_t)q.T);
     q.scratch_bytes = off;
     q.saved_bytes = 4 * NBp * (size_t)(2 * q.S + 1);
     *p = q;
