@@ -122,11 +122,15 @@ __device__ __forceinline__ float dot4(const float4 &a, const float4 &b, float d)
 // (A two-level tree of counters measured slower here: its extra returning
 // atomic costs more than the contention it removes.)  Returns false for the
 // whole CTA once any CTA has recorded an error, so every CTA leaves together.
-__device__ bool grid_sync(const KArgs &a, unsigned idx, int *s_ok) {
+// `during` runs on every thread between the arrival and the wait: work that
+// other CTAs do not depend on (output copies, staging of the next operands).
+template <class F>
+__device__ bool grid_sync(const KArgs &a, unsigned idx, int *s_ok, F &&during) {
     __syncthreads();
+    const unsigned target = (a.bar_base + idx + 1u) * (unsigned)a.P + a.bar_extra;
+    if (threadIdx.x == 0) red_release_add(a.bar, 1u);
+    during();
     if (threadIdx.x == 0) {
-        const unsigned target = (a.bar_base + idx + 1u) * (unsigned)a.P + a.bar_extra;
-        red_release_add(a.bar, 1u);
         const unsigned long long t0 = globaltimer();
         int e = 0;
         while (ld_acquire(a.bar) < target) {
@@ -141,6 +145,9 @@ __device__ bool grid_sync(const KArgs &a, unsigned idx, int *s_ok) {
     }
     __syncthreads();
     return *s_ok != 0;
+}
+__device__ bool grid_sync(const KArgs &a, unsigned idx, int *s_ok) {
+    return grid_sync(a, idx, s_ok, [] {});
 }
 
 // Another CTA's published carry for column b: a 64-bit word whose high half
@@ -926,32 +933,36 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         if (!grid_sync(a, nbar++, &s_ok)) return;
     }
 
-    for (int it = 0; it < a.s_count; ++it) {
-        const int s = BWD ? a.s_first - it : a.s_first + it;
-        const unsigned phase_id = BWD ? (unsigned)(a.S - s) : (unsigned)(s + 1);
-        const float *rows = BWD ? a.da + (size_t)(s & 1) * NBp : a.H + (size_t)s * NBp;
-        if (c.stage) {
-            // part B's operands copied into shared memory while part A runs
-            const size_t ro = (size_t)c.r0 * Bp;
-            if (BWD && s > 0) {
+    // stage mode: issue the copies of microstep s's part-B operands into
+    // shared memory; they land while part A runs
+    auto stage_for = [&](int s) {
+        const size_t ro = (size_t)c.r0 * Bp;
+        if (BWD) {
+            if (s > 0) {
                 const int q = s - 1, tq = q / a.M;
                 stage_rows<THREADS>(S_st1(a), a.A + (size_t)q * NBp + ro, c.nrows, Bp);
                 stage_rows<THREADS>(S_st2(a), a.H + (size_t)q * NBp + ro, c.nrows, Bp);
                 if (q - tq * a.M == a.M - 1) stage_dout<THREADS>(a, c, tq);
-            } else if (!BWD && c.n_inp > 0 && s % a.M == 0) {
-                const int t = s / a.M;
-                for (int j = tid; j < c.nrows * a.B; j += THREADS) {
-                    const int i = j / a.B, b = j - i * a.B;
-                    const int ii = S_inp(a)[i];
-                    if (ii >= 0)
-                        cp_async4(S_st1(a) + (size_t)ii * Bp + b,
-                                  a.drives + ((size_t)t * a.n_in + S_sslot(a)[i]) * a.B + b);
-                }
             }
-            cp_async_commit();
-            // the state that ended the previous input step, still in st0
-            if (!BWD && s > 0 && s % a.M == 0) write_out<THREADS>(a, c, s / a.M - 1);
-        } else if (tid == 0 && c.nrows > 0) {
+        } else if (c.n_inp > 0 && s % a.M == 0) {
+            const int t = s / a.M;
+            for (int j = tid; j < c.nrows * a.B; j += THREADS) {
+                const int i = j / a.B, b = j - i * a.B;
+                const int ii = S_inp(a)[i];
+                if (ii >= 0)
+                    cp_async4(S_st1(a) + (size_t)ii * Bp + b,
+                              a.drives + ((size_t)t * a.n_in + S_sslot(a)[i]) * a.B + b);
+            }
+        }
+        cp_async_commit();
+    };
+    if (c.stage && a.s_count > 0) stage_for(a.s_first);
+
+    for (int it = 0; it < a.s_count; ++it) {
+        const int s = BWD ? a.s_first - it : a.s_first + it;
+        const unsigned phase_id = BWD ? (unsigned)(a.S - s) : (unsigned)(s + 1);
+        const float *rows = BWD ? a.da + (size_t)(s & 1) * NBp : a.H + (size_t)s * NBp;
+        if (!c.stage && tid == 0 && c.nrows > 0) {
             // part B's operands of this CTA's rows, fetched into L2 during part A
             const unsigned rb = (unsigned)((size_t)c.nrows * Bp * 4);
             const size_t ro = (size_t)c.r0 * Bp;
@@ -970,8 +981,20 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         if (warp == THREADS / 32 - 2 && c.publish) publish_carry(a, c, phase_id);
         if (BWD) finish_bwd<THREADS>(a, c, pb, s, phase_id);
         else finish_fwd<THREADS>(a, c, pb, s, phase_id);
-        if (it + 1 < a.s_count)
-            if (!grid_sync(a, nbar++, &s_ok)) return;
+        if (it + 1 < a.s_count) {
+            // while other CTAs finish: copy out the state that ended an input
+            // step, and stage the next microstep's operands (this microstep's
+            // part B has read the old ones)
+            auto between = [&]() {
+                if (!c.stage) return;
+                if (!BWD && s % a.M == a.M - 1) write_out<THREADS>(a, c, s / a.M);
+                stage_for(BWD ? s - 1 : s + 1);
+            };
+            if (!grid_sync(a, nbar++, &s_ok, between)) {
+                cp_async_wait_all();
+                return;
+            }
+        }
     }
 
     if (a.do_epilogue) {
