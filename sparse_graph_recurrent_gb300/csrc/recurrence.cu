@@ -31,7 +31,10 @@
 //      a batch are issued before any is used, whatever rows they belong to.
 //      When the row id changes, the group's running sum of the row that ended
 //      goes to that row's slot in shared memory; the partial sum of the row it
-//      stops inside goes to the group's carry slot.
+//      stops inside goes to the group's carry slot, after the groups of a warp
+//      that carry the same row have added theirs together (a segmented sum
+//      over shuffles), so a row split over many groups leaves one carry per
+//      warp.
 //   B  after a CTA barrier, warps finish the CTA's rows, lane = batch column,
 //      up to four rows at a time: row slot, plus the carries of the groups
 //      that hold the row's earlier edges (and, for the CTA's first row, the
@@ -493,12 +496,42 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
         load(bt, kb);
         consume(bt, kb);
     }
+    // the row this group stops in: finished here if its last edge is ours and
+    // its row end belongs to this CTA (the carry is then 0), else a carry
+    int lab = -2;  // row of this group's carry; never equal for inactive lanes
     if (active) {
-        // the row this group stops in: finished here if its last edge is ours
-        // and its row end belongs to this CTA, else a carry
         const bool fin = len > 0 && cur >= c.r0 && cur < c.r0 + c.nrows &&
                          S_srp(a)[cur - c.r0 + 1] == k1;
         if (fin) flush(cur);
+        // an empty group sits at edge k0 < e1 (n > 0): it takes that edge's row
+        lab = len > 0 ? cur : (k0 < c.e1 ? row_at(k0) : -1);
+    }
+    // Segmented suffix sums over the warp's groups: a group adds the carry of
+    // the group d places on while both carry the same row (labels do not
+    // decrease along the groups, so equal ends mean an equal run).  Afterwards
+    // the first group of each run in the warp holds the run's total, and a row
+    // spread over many groups needs one carry read per warp it crosses.
+    const int g = (threadIdx.x & 31) / a.LPE;
+    for (int d = 1; d < a.EPW; d <<= 1) {
+        const int sh = d * a.LPE;
+        const int lo = __shfl_down_sync(kFull, lab, sh);
+        const bool take = g + d < a.EPW && lo == lab;
+#pragma unroll
+        for (int ch = 0; ch < NC; ++ch) {
+            float4 o;
+            o.x = __shfl_down_sync(kFull, acc[ch].x, sh);
+            o.y = __shfl_down_sync(kFull, acc[ch].y, sh);
+            o.z = __shfl_down_sync(kFull, acc[ch].z, sh);
+            o.w = __shfl_down_sync(kFull, acc[ch].w, sh);
+            if (take) {
+                acc[ch].x += o.x;
+                acc[ch].y += o.y;
+                acc[ch].z += o.z;
+                acc[ch].w += o.w;
+            }
+        }
+    }
+    if (active) {
         float *dst = S_scarry(a) + (size_t)gam * Bp + lig * 4;
 #pragma unroll
         for (int ch = 0; ch < NC; ++ch) *reinterpret_cast<float4 *>(dst + ch * CW) = acc[ch];
@@ -529,21 +562,32 @@ __device__ __forceinline__ PB make_pb(int Bp) {
     return p;
 }
 
+// Column b of the carries of groups [ga, gb), all of one row, after part A's
+// per-warp run sums: group ga's entry covers the row's groups in ga's warp,
+// and the first group of every later warp below gb covers that warp's.  The
+// first two reads are unconditional (clamped, masked) so they issue without
+// waiting on branches.
+__device__ __forceinline__ float carry_sum(const KArgs &a, const float *sc, int ga, int gb) {
+    const int h1 = (ga / a.EPW + 1) * a.EPW;
+    const float v0 = sc[(size_t)min(ga, a.G - 1) * a.Bp];
+    const float v1 = sc[(size_t)min(h1, a.G - 1) * a.Bp];
+    float x = ga < gb ? v0 : 0.f;
+    x += h1 < gb ? v1 : 0.f;
+    for (int h = h1 + a.EPW; h < gb; h += a.EPW) x += sc[(size_t)h * a.Bp];
+    return x;
+}
+
 // Row i's sum for column b: its slot (the part summed by the group holding its
-// last edge here), then the carries of the groups holding its earlier edges,
-// in group order; 0 for a row with no edges in this CTA.
+// last edge here) plus the carries of the groups holding its earlier edges; 0
+// for a row with no edges in this CTA.
 template <bool RS>
 __device__ __forceinline__ float row_sum(const KArgs &a, const Cta &c, int i, int b) {
     const int gr = S_sgrp(a)[i];
     const size_t o = (size_t)i * a.Bp + b;
-    float x = gr < 0 ? 0.f : (RS ? c.rows[o] : __ldcg(c.rows + o));
+    const float slot = RS ? c.rows[o] : __ldcg(c.rows + o);
     const int ga = gr < 0 ? 0 : gr >> 16, gb = gr < 0 ? 0 : (gr & 0xffff);
-    const float *sc = S_scarry(a) + b;
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-        if (ga + u < gb) x += sc[(size_t)(ga + u) * a.Bp];
-    for (int u = ga + 8; u < gb; ++u) x += sc[(size_t)u * a.Bp];
-    return x;
+    const float x = gr < 0 ? 0.f : slot;
+    return x + carry_sum(a, S_scarry(a) + b, ga, gb);
 }
 
 // Carries published by earlier CTAs for column b of the CTA's first row.
@@ -806,14 +850,13 @@ __device__ void finish_bwd(const KArgs &a, const Cta &c, const PB &pb, int s, un
 }
 
 // Publish this CTA's carry for the row its piece ends inside (row r0 + nrows):
-// the carries of the groups holding that row's edges here, in group order.
+// the sum of the carries of the groups holding that row's edges here.
 __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsigned phase_id) {
     const int lane = threadIdx.x & 31;
     const int ka = S_srp(a)[c.nrows] > c.e0 ? S_srp(a)[c.nrows] : c.e0;
     const int ga = ka < c.e1 ? group_of(c, a.G, ka) : a.G;
     for (int b = lane; b < a.Bp; b += 32) {
-        float x = 0.f;
-        for (int u = ga; u < a.G; ++u) x += S_scarry(a)[(size_t)u * a.Bp + b];
+        const float x = carry_sum(a, S_scarry(a) + b, ga, a.G);
         st_relaxed64(a.carry + (size_t)blockIdx.x * a.Bp + b,
                      ((unsigned long long)phase_id << 32) | __float_as_uint(x));
     }
