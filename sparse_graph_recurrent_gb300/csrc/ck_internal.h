@@ -46,7 +46,7 @@ struct SmemLayout {
     bool graph;  // the CTA's slice of the graph lives in shared memory
     bool rows;   // row sums live in shared memory (else in global scratch)
     bool stage;  // finish operands staged in shared memory
-    int o_st0, o_st1, o_st2, o_st3, o_inp, o_acc;
+    int o_st0, o_st1, o_st2, o_st3, o_st4, o_inp, o_acc;
 };
 
 // Launch description of one ck_forward / ck_backward call (recurrence.cu).

@@ -64,7 +64,7 @@ struct KArgs {
     // dynamic shared memory layout (byte offsets)
     int o_srp, o_prm, o_slot, o_grp, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;
     int stage;  // finish operands staged in shared memory (see Cta)
-    int o_st0, o_st1, o_st2, o_st3, o_inp, o_acc;
+    int o_st0, o_st1, o_st2, o_st3, o_st4, o_inp, o_acc;
     const int *row_ptr, *col, *perm, *slot, *rowid;
     const float *w, *leak, *bias, *drives, *state0;
     float *out;
@@ -244,8 +244,9 @@ __device__ void from_rows(float *__restrict__ dst, const float *__restrict__ src
 //               drives of the CTA's input rows for the current input step
 //               (row inp[i])
 //     backward: st0 = G (resident), st1 = A[q], st2 = H[q], st3 = dOut[t(q)]
-//               (row stride Bp + 1), acc = {d_leak, d_bias} running sums
-//               (resident)
+//               (row stride Bp + 1), st4 = H[s] (rows r0 .. r0 + nrows: the
+//               source rows part A meets), acc = {d_leak, d_bias} running
+//               sums (resident)
 struct Cta {
     float *rows;  // [nrows][Bp] row slots (shared or global)
     bool stage;
@@ -269,6 +270,7 @@ __device__ __forceinline__ float *S_st0(const KArgs &a) { return reinterpret_cas
 __device__ __forceinline__ float *S_st1(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st1); }
 __device__ __forceinline__ float *S_st2(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st2); }
 __device__ __forceinline__ float *S_st3(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st3); }
+__device__ __forceinline__ float *S_st4(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st4); }
 __device__ __forceinline__ int *S_inp(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_inp); }
 __device__ __forceinline__ float2 *S_acc(const KArgs &a) { return reinterpret_cast<float2 *>(ck_smem + a.o_acc); }
 // Row stride of the staged arrays that are also read or written across rows
@@ -287,6 +289,8 @@ __device__ __forceinline__ void cp_async4(void *sdst, const void *gsrc) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// all but the most recently committed group have landed
+__device__ __forceinline__ void cp_async_wait_but_last() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Copy this CTA's rows [r0, r0 + nrows) of a node-major array into shared memory.
 template <int THREADS>
@@ -367,7 +371,7 @@ __device__ __forceinline__ void group_dots(float (&d)[UNR], int lig, int lpe, in
     }
 }
 
-template <int NC, bool SMEMG, bool BWD, int UNR>
+template <int NC, bool SMEMG, bool BWD, int UNR, bool HS>
 __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int gam, int lig,
                                              bool active, const float *__restrict__ rows,
                                              const float *__restrict__ hprev) {
@@ -386,14 +390,26 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
 #pragma unroll
     for (int ch = 0; ch < NC; ++ch) acc[ch] = zero4();
 
-    // backward: own-row state of the current and the next source row
-    float4 hcur[BWD ? NC : 1], hnext[BWD ? NC : 1];
+    // backward: own-row state of the current source row and, when it is read
+    // from global memory (HS false), of the next one, fetched ahead; with HS
+    // the CTA's rows of h_{s-1} are staged in shared memory (st4)
+    constexpr int HN = BWD ? NC : 1;
+    float4 hcur[HN], hnext[HS ? 1 : HN];
     int nxt = -1;
-    auto load_h = [&](float4(&h)[BWD ? NC : 1], int row) {
-        const float *hp = hprev + (size_t)(row < 0 ? 0 : row) * Bp + lig * 4;
+    auto load_h = [&](float4(&h)[HN], int row) {
+        if (HS) {
+            const int i = row - c.r0;
+            const bool in = row >= 0 && i <= c.nrows;  // always, for a valid graph
+            const float *hp = S_st4(a) + (size_t)(in ? i : 0) * Bp + lig * 4;
 #pragma unroll
-        for (int ch = 0; ch < (BWD ? NC : 1); ++ch)
-            h[ch] = row >= 0 ? __ldg(reinterpret_cast<const float4 *>(hp + ch * CW)) : zero4();
+            for (int ch = 0; ch < HN; ++ch)
+                h[ch] = in ? *reinterpret_cast<const float4 *>(hp + ch * CW) : zero4();
+        } else {
+            const float *hp = hprev + (size_t)(row < 0 ? 0 : row) * Bp + lig * 4;
+#pragma unroll
+            for (int ch = 0; ch < HN; ++ch)
+                h[ch] = row >= 0 ? __ldg(reinterpret_cast<const float4 *>(hp + ch * CW)) : zero4();
+        }
     };
     auto next_row = [&](int row) -> int {  // the row after `row` that has edges in [k0, k1)
         const int pos = S_srp(a)[row - c.r0 + 1];
@@ -401,8 +417,10 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     };
     if (BWD) {
         load_h(hcur, cur);
-        nxt = cur >= 0 ? next_row(cur) : -1;
-        load_h(hnext, nxt);
+        if (!HS) {
+            nxt = cur >= 0 ? next_row(cur) : -1;
+            load_h(reinterpret_cast<float4(&)[HN]>(hnext), nxt);
+        }
     }
 
     auto flush = [&](int row) {
@@ -452,14 +470,18 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                 flush(cur);
                 cur = bt.rid[q];
                 if (BWD) {
-                    if (cur == nxt) {
-#pragma unroll
-                        for (int ch = 0; ch < (BWD ? NC : 1); ++ch) hcur[ch] = hnext[ch];
-                    } else {
+                    if (HS) {
                         load_h(hcur, cur);
+                    } else {
+                        if (cur == nxt) {
+#pragma unroll
+                            for (int ch = 0; ch < HN; ++ch) hcur[ch] = hnext[HS ? 0 : ch];
+                        } else {
+                            load_h(hcur, cur);
+                        }
+                        nxt = next_row(cur);
+                        load_h(reinterpret_cast<float4(&)[HN]>(hnext), nxt);
                     }
-                    nxt = next_row(cur);
-                    load_h(hnext, nxt);
                 }
             }
 #pragma unroll
@@ -981,6 +1003,10 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     auto stage_for = [&](int s) {
         const size_t ro = (size_t)c.r0 * Bp;
         if (BWD) {
+            // part A's source rows: r0 .. r0 + nrows (the last one only if it exists)
+            stage_rows<THREADS>(S_st4(a), a.H + (size_t)s * NBp + ro,
+                                c.r0 + c.nrows < N ? c.nrows + 1 : c.nrows, Bp);
+            cp_async_commit();  // its own group: part A waits for it alone
             if (s > 0) {
                 const int q = s - 1, tq = q / a.M;
                 stage_rows<THREADS>(S_st1(a), a.A + (size_t)q * NBp + ro, c.nrows, Bp);
@@ -1018,7 +1044,15 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
                 prefetch_l2(a.H + (size_t)s * NBp + ro, rb);
             }
         }
-        stream_piece<NC, SMEMG, BWD, UNR>(a, c, gam, lig, active, rows, a.H + (size_t)s * NBp);
+        if (BWD && c.stage) {
+            // st4 (h_{s-1} rows) must have landed before part A reads it; the
+            // finish operands committed after it may still be in flight
+            cp_async_wait_but_last();
+            __syncthreads();
+            stream_piece<NC, SMEMG, BWD, UNR, true>(a, c, gam, lig, active, rows, a.H + (size_t)s * NBp);
+        } else {
+            stream_piece<NC, SMEMG, BWD, UNR, false>(a, c, gam, lig, active, rows, a.H + (size_t)s * NBp);
+        }
         if (c.stage) cp_async_wait_all();
         __syncthreads();
         if (warp == THREADS / 32 - 2 && c.publish) publish_carry(a, c, phase_id);
@@ -1100,7 +1134,7 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     const size_t rows_pb = align16(4 * (size_t)rc * (p.Bp + 1));  // row stride Bp + 1
     const size_t graph_b = (dir == 0 ? 12 : 16) * (size_t)p.cap[dir] + 48;
     // finish operands: forward state + drives; backward G, A, H, dOut + two sums
-    const size_t stage_b = (dir == 0 ? 1 : 3) * rows_b + rows_pb + align16(8 * (size_t)rc) + align16(4 * (size_t)rc);
+    const size_t stage_b = (dir == 0 ? 1 : 4) * rows_b + rows_pb + align16(8 * (size_t)rc) + align16(4 * (size_t)rc);
     L.rows = o + rows_b <= budget;
     if (L.rows) o += rows_b;
     L.o_rows = (int)(o - (L.rows ? rows_b : 0));
@@ -1114,6 +1148,7 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     L.o_st1 = (int)o; o += sb;
     L.o_st2 = (int)o; o += dir == 1 ? sb : 0;
     L.o_st3 = (int)o; o += dir == 1 ? spb : 0;
+    L.o_st4 = (int)o; o += dir == 1 ? sb : 0;
     L.o_acc = (int)o; o = align16(o + (L.stage ? 8 * (size_t)rc : 0));
     L.o_inp = (int)o; o = align16(o + (L.stage ? 4 * (size_t)rc : 0));
     L.bytes = o;
@@ -1154,6 +1189,7 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.o_st1 = L.o_st1;
     k.o_st2 = L.o_st2;
     k.o_st3 = L.o_st3;
+    k.o_st4 = L.o_st4;
     k.o_inp = L.o_inp;
     k.o_acc = L.o_acc;
     k.slot = g->slot;
