@@ -103,9 +103,11 @@ ck_status ck_graph_export(const ck_graph *g, int32_t *row_ptr, int32_t *col, int
  * ck_workspace_size -- bytes of the two caller-owned buffers for batch B,
  * T input steps and `microsteps` microsteps per step, on the current device.
  *   saved_bytes    activations kept from ck_forward for ck_backward: the state
- *                  and pre-activation after every microstep plus the initial
- *                  state (connectome-kernels page, "Design notes": 2 x T x M x
- *                  N x B floats saved), rows padded to a multiple of 8 floats
+ *                  and the proposal tanh(pre-activation) after every microstep,
+ *                  plus the initial state (connectome-kernels page, "Design
+ *                  notes": 2 x T x M x N x B floats saved; the proposal stands in
+ *                  for the pre-activation, which the backward needs only through
+ *                  its tanh), rows padded to a multiple of 8 floats
  *   scratch_bytes  temporary device memory for one ck_forward or ck_backward
  *                  call; one scratch buffer may serve both, but two calls that
  *                  run at the same time need two buffers

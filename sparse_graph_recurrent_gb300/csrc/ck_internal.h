@@ -68,6 +68,7 @@ struct Plan {
     size_t off_G;       // float [N][Bp]
     size_t off_da;      // float [2][N][Bp]
     size_t off_rowsum;  // float [N][Bp]
+    size_t off_lacc;    // float2 [N][32] per-lane d_leak / d_bias partials
     size_t scratch_bytes;
     size_t saved_bytes; // float [(S+1) + S][N][Bp]
 };

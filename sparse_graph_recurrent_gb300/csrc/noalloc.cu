@@ -83,7 +83,7 @@ extern "C" ck_status ck_forward_static_scratch(const ck_graph *g, const float *e
     off = up256(off + 4 * (size_t)(q.E > 0 ? q.E : 1));
     q.off_rowsum = off;
     off = up256(off + 4 * (size_t)q.N * q.Bp);
-    q.off_dwperm = q.off_G = q.off_da = 0;  // backward-only regions, unused here
+    q.off_dwperm = q.off_G = q.off_da = q.off_lacc = 0;  // backward-only regions, unused here
     q.scratch_bytes = off;
     if (off > kStaticScratchBytes)
         return fail(CK_ERR_UNSUPPORTED,

@@ -14,7 +14,9 @@
 //
 // Layout in device memory (fp32, rows padded to Bp = B rounded up to 8):
 //   H[s+1][N][Bp]  state after microstep s; H[0] = state0 transposed
-//   A[s][N][Bp]    pre-activation of microstep s
+//   Pr[s][N][Bp]   proposal tanh(pre-activation) of microstep s (the backward
+//                  needs only the proposal, so it is saved instead of the
+//                  pre-activation and the backward evaluates no tanh)
 //   G[N][Bp]       running state gradient (backward)
 //   da[2][N][Bp]   d(loss)/d(pre-activation), ping-pong between microsteps
 // The caller's [T][B][N] outputs and output gradients are read and written one
@@ -68,10 +70,11 @@ struct KArgs {
     const int *row_ptr, *col, *perm, *slot, *rowid;
     const float *w, *leak, *bias, *drives, *state0;
     float *out;
-    float *H, *A;
+    float *H, *Pr;  // saved states and proposals
     const float *dout;
     float *dw, *dleak, *dbias, *ddrives, *dstate0;
     float *G_, *da, *rowsum_g;
+    float2 *lacc;  // [N][32] per-lane {d_leak, d_bias} partials (backward, unstaged)
     unsigned *bar;
     int *err;
     unsigned long long *carry;  // [P][Bp] {float bits, phase id} words
@@ -236,17 +239,18 @@ __device__ void from_rows(float *__restrict__ dst, const float *__restrict__ src
 // from the shared-memory base instead of holding them in registers.
 //   srp    row_ptr[r0 + i], i < nrows + 2 (clamped at N)
 //   prm    {leak, bias} of rows r0 + i;  sslot: their input slots
-//   sgrp   groups [ga, gb) whose carries belong to row r0 + i, ga << 16 | gb
+//   sgrp   groups [ga, gb) whose carries belong to row r0 + i, {ga << 16 | gb,
+//          first group of the next warp after ga's}
 //   scarry [G][Bp] group carries;  tile: [32][33] transpose tile
 //   scw, srow, sdw   {col, w bits}, row and edge-gradient sum of the CTA's edges
 //   stage mode, rows r0 + i:
 //     forward:  st0 = current state (resident, row stride Bp + 1), st1 =
 //               drives of the CTA's input rows for the current input step
 //               (row inp[i])
-//     backward: st0 = G (resident), st1 = A[q], st2 = H[q], st3 = dOut[t(q)]
+//     backward: st0 = G (resident), st1 = Pr[q], st2 = H[q], st3 = dOut[t(q)]
 //               (row stride Bp + 1), st4 = H[s] (rows r0 .. r0 + nrows: the
 //               source rows part A meets), acc = {d_leak, d_bias} running
-//               sums (resident)
+//               sums per row and lane, [rows][32] (resident)
 struct Cta {
     float *rows;  // [nrows][Bp] row slots (shared or global)
     bool stage;
@@ -260,7 +264,7 @@ extern __shared__ __align__(16) unsigned char ck_smem[];
 __device__ __forceinline__ int *S_srp(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_srp); }
 __device__ __forceinline__ float2 *S_prm(const KArgs &a) { return reinterpret_cast<float2 *>(ck_smem + a.o_prm); }
 __device__ __forceinline__ int *S_sslot(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_slot); }
-__device__ __forceinline__ int *S_sgrp(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_grp); }
+__device__ __forceinline__ int2 *S_sgrp(const KArgs &a) { return reinterpret_cast<int2 *>(ck_smem + a.o_grp); }
 __device__ __forceinline__ float *S_scarry(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_carry); }
 __device__ __forceinline__ float *S_tile(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_tile); }
 __device__ __forceinline__ int2 *S_scw(const KArgs &a) { return reinterpret_cast<int2 *>(ck_smem + a.o_cw); }
@@ -394,32 +398,37 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     // from global memory (HS false), of the next one, fetched ahead; with HS
     // the CTA's rows of h_{s-1} are staged in shared memory (st4)
     constexpr int HN = BWD ? NC : 1;
-    float4 hcur[HN], hnext[HS ? 1 : HN];
-    int nxt = -1;
-    auto load_h = [&](float4(&h)[HN], int row) {
+    struct HRow {
+        float4 v[HN];
+    };
+    auto load_h = [&](int row) -> HRow {
+        HRow h;
         if (HS) {
             const int i = row - c.r0;
             const bool in = row >= 0 && i <= c.nrows;  // always, for a valid graph
             const float *hp = S_st4(a) + (size_t)(in ? i : 0) * Bp + lig * 4;
 #pragma unroll
             for (int ch = 0; ch < HN; ++ch)
-                h[ch] = in ? *reinterpret_cast<const float4 *>(hp + ch * CW) : zero4();
+                h.v[ch] = in ? *reinterpret_cast<const float4 *>(hp + ch * CW) : zero4();
         } else {
             const float *hp = hprev + (size_t)(row < 0 ? 0 : row) * Bp + lig * 4;
 #pragma unroll
             for (int ch = 0; ch < HN; ++ch)
-                h[ch] = row >= 0 ? __ldg(reinterpret_cast<const float4 *>(hp + ch * CW)) : zero4();
+                h.v[ch] = row >= 0 ? __ldg(reinterpret_cast<const float4 *>(hp + ch * CW)) : zero4();
         }
+        return h;
     };
+    HRow hcur, hnext;
+    int nxt = -1;
     auto next_row = [&](int row) -> int {  // the row after `row` that has edges in [k0, k1)
         const int pos = S_srp(a)[row - c.r0 + 1];
         return pos < k1 ? row_at(pos) : -1;
     };
     if (BWD) {
-        load_h(hcur, cur);
+        hcur = load_h(cur);
         if (!HS) {
             nxt = cur >= 0 ? next_row(cur) : -1;
-            load_h(reinterpret_cast<float4(&)[HN]>(hnext), nxt);
+            hnext = load_h(nxt);
         }
     }
 
@@ -471,16 +480,11 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                 cur = bt.rid[q];
                 if (BWD) {
                     if (HS) {
-                        load_h(hcur, cur);
+                        hcur = load_h(cur);
                     } else {
-                        if (cur == nxt) {
-#pragma unroll
-                            for (int ch = 0; ch < HN; ++ch) hcur[ch] = hnext[HS ? 0 : ch];
-                        } else {
-                            load_h(hcur, cur);
-                        }
+                        hcur = cur == nxt ? hnext : load_h(cur);
                         nxt = next_row(cur);
-                        load_h(reinterpret_cast<float4(&)[HN]>(hnext), nxt);
+                        hnext = load_h(nxt);
                     }
                 }
             }
@@ -488,7 +492,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             for (int ch = 0; ch < NC; ++ch) fma4(acc[ch], bt.w[q], bt.v[q][ch]);
             if (BWD) {
 #pragma unroll
-                for (int ch = 0; ch < NC; ++ch) d[q] = dot4(bt.v[q][ch], hcur[BWD ? ch : 0], d[q]);
+                for (int ch = 0; ch < NC; ++ch) d[q] = dot4(bt.v[q][ch], hcur.v[BWD ? ch : 0], d[q]);
             }
         }
         if (BWD) {
@@ -589,8 +593,8 @@ __device__ __forceinline__ PB make_pb(int Bp) {
 // and the first group of every later warp below gb covers that warp's.  The
 // first two reads are unconditional (clamped, masked) so they issue without
 // waiting on branches.
-__device__ __forceinline__ float carry_sum(const KArgs &a, const float *sc, int ga, int gb) {
-    const int h1 = (ga / a.EPW + 1) * a.EPW;
+__device__ __forceinline__ int next_warp_group(const KArgs &a, int ga) { return (ga / a.EPW + 1) * a.EPW; }
+__device__ __forceinline__ float carry_sum(const KArgs &a, const float *sc, int ga, int gb, int h1) {
     const float v0 = sc[(size_t)min(ga, a.G - 1) * a.Bp];
     const float v1 = sc[(size_t)min(h1, a.G - 1) * a.Bp];
     float x = ga < gb ? v0 : 0.f;
@@ -604,12 +608,13 @@ __device__ __forceinline__ float carry_sum(const KArgs &a, const float *sc, int 
 // for a row with no edges in this CTA.
 template <bool RS>
 __device__ __forceinline__ float row_sum(const KArgs &a, const Cta &c, int i, int b) {
-    const int gr = S_sgrp(a)[i];
+    const int2 g2 = S_sgrp(a)[i];
+    const int gr = g2.x;
     const size_t o = (size_t)i * a.Bp + b;
     const float slot = RS ? c.rows[o] : __ldcg(c.rows + o);
     const int ga = gr < 0 ? 0 : gr >> 16, gb = gr < 0 ? 0 : (gr & 0xffff);
     const float x = gr < 0 ? 0.f : slot;
-    return x + carry_sum(a, S_scarry(a) + b, ga, gb);
+    return x + carry_sum(a, S_scarry(a) + b, ga, gb, g2.y);
 }
 
 // Carries published by earlier CTAs for column b of the CTA's first row.
@@ -658,7 +663,7 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
     const size_t NBp = (size_t)a.N * Bp;
     const float *hin = a.H + (size_t)s * NBp;
     float *hout = a.H + (size_t)(s + 1) * NBp;
-    float *aout = a.A + (size_t)s * NBp;
+    float *pout = a.Pr + (size_t)s * NBp;
     for (int cb = 0; cb < pb.CB; ++cb) {
         int ii[4], bb[4];
         bool ok[4];
@@ -701,14 +706,14 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
         for (int el = 0; el < 4; ++el) {
             const bool live = bb[el] < B;
             const float hv = live ? fmaf(pr[el].x, th[el], (1.f - pr[el].x) * hp[el]) : 0.f;
-            const float a0 = live ? av[el] : 0.f;
+            const float p0 = live ? th[el] : 0.f;
             if (ok[el]) {
                 const size_t o = (size_t)ii[el] * Bp + bb[el];
                 if (ST) S_st0(a)[ii[el] * pstride(a) + bb[el]] = hv;
                 else if (step_end && live)
                     __stcs(a.out + ((size_t)t * B + bb[el]) * a.N + c.r0 + ii[el], hv);
                 hout[(size_t)c.r0 * Bp + o] = hv;
-                __stcs(aout + (size_t)c.r0 * Bp + o, a0);
+                __stcs(pout + (size_t)c.r0 * Bp + o, p0);
             }
         }
     }
@@ -746,15 +751,16 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
     const bool step_end = q >= 0 && q - tq * M == M - 1;
     const bool first = q >= 0 && q - tq * M == M - 1;  // first visit of step tq going backwards
     const size_t ro = (size_t)c.r0 * Bp;
-    const float *Aq = a.A + (size_t)(q >= 0 ? q : 0) * NBp + ro;
+    const float *Pq = a.Pr + (size_t)(q >= 0 ? q : 0) * NBp + ro;
     const float *Hq = a.H + (size_t)(q >= 0 ? q : 0) * NBp + ro;
     const float *dO = a.dout + (size_t)tq * B * a.N + c.r0;  // [B][N] slab of step tq
     float *daq = a.da + (size_t)(q & 1) * NBp + ro;
+    // d_leak, d_bias terms summed per element slot over the column chunks
     float dl[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
     for (int cb = 0; cb < pb.CB; ++cb) {
         int ii[4], bb[4];
         bool ok[4];
-        float x[4], gv[4], ov[4], av[4], hv[4], lam[4];
+        float x[4], gv[4], ov[4], p[4], hv[4], lam[4];
 #pragma unroll
         for (int el = 0; el < 4; ++el) {
             const int i = i0 + pb.ri[el], cc = cb * pb.cpb + pb.ci[el], b = cc * 32 + lane;
@@ -770,12 +776,12 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
             if (ST) {
                 gv[el] = pro ? 0.f : S_st0(a)[o];
                 ov[el] = step_end && bb[el] < B ? S_st3(a)[ii[el] * pstride(a) + bb[el]] : 0.f;
-                av[el] = q >= 0 ? S_st1(a)[o] : 0.f;
+                p[el] = q >= 0 ? S_st1(a)[o] : 0.f;
                 hv[el] = q >= 0 ? S_st2(a)[o] : 0.f;
             } else {
                 gv[el] = pro ? 0.f : __ldcg(a.G_ + ro + o);
                 ov[el] = step_end && bb[el] < B ? __ldg(dO + (size_t)bb[el] * a.N + ii[el]) : 0.f;
-                av[el] = q >= 0 ? __ldcs(Aq + o) : 0.f;
+                p[el] = q >= 0 ? __ldcs(Pq + o) : 0.f;
                 hv[el] = q >= 0 ? __ldg(Hq + o) : 0.f;
             }
         }
@@ -784,14 +790,12 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
             for (int el = 0; el < 4; ++el)
                 if (pb.ri[el] == 0) x[el] += global_carry(a, c, bb[el], phase_id);
         }
-        float gn[4], p[4];
+        float gn[4];
 #pragma unroll
         for (int el = 0; el < 4; ++el) {
             gn[el] = fmaf(gv[el], 1.f - lam[el], x[el]) + ov[el];
             if (bb[el] >= B) gn[el] = 0.f;
         }
-#pragma unroll
-        for (int el = 0; el < 4; ++el) p[el] = q >= 0 ? tanhf(av[el]) : 0.f;
 #pragma unroll
         for (int el = 0; el < 4; ++el) {
             if (!ok[el]) continue;
@@ -802,8 +806,8 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
             const bool live = bb[el] < B;
             const float d = live ? gn[el] * lam[el] * (1.f - p[el] * p[el]) : 0.f;
             if (live) {
-                dl[pb.ri[el]] = fmaf(gn[el], p[el] - hv[el], dl[pb.ri[el]]);
-                db[pb.ri[el]] += d;
+                dl[el] = fmaf(gn[el], p[el] - hv[el], dl[el]);
+                db[el] += d;
                 const int sl = S_sslot(a)[ii[el]];
                 if (sl >= 0) {
                     float *dd = a.ddrives + ((size_t)tq * a.n_in + sl) * B + bb[el];
@@ -814,44 +818,25 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
         }
     }
     if (q >= 0) {
-        // sum the eight values {dl, db} x 4 rows over the warp: three halving
-        // exchanges (lane bits 4, 3, 2) split the values among lanes, two more
-        // (bits 1, 0) finish the sums
-        float v[8] = {dl[0], dl[1], dl[2], dl[3], db[0], db[1], db[2], db[3]};
-#pragma unroll
-        for (int o = 4, m = 16; o >= 1; o >>= 1, m >>= 1) {
-#pragma unroll
-            for (int j = 0; j < o; ++j) {
-                const bool up = (lane & m) != 0;
-                const float keep = up ? v[j + o] : v[j];
-                const float send = up ? v[j] : v[j + o];
-                v[j] = keep + __shfl_xor_sync(kFull, send, m);
-            }
-        }
-        v[0] += __shfl_xor_sync(kFull, v[0], 2);
-        v[0] += __shfl_xor_sync(kFull, v[0], 1);
-        // lane l now holds value 4 bit4(l) + 2 bit3(l) + bit2(l)
-        float tot[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            tot[j] = __shfl_sync(kFull, v[0], ((j & 4) << 2) | ((j & 2) << 2) | ((j & 1) << 2));
+        // d_leak, d_bias: per-lane partial sums per row (shared memory when
+        // staged, else scratch), reduced across lanes once, in the epilogue
+        float2 *lacc = ST ? S_acc(a) : a.lacc + (size_t)c.r0 * 32;
 #pragma unroll
         for (int ri = 0; ri < 4; ++ri) {
             if (ri >= pb.RB) break;
             const int i = i0 + ri;
             if (i >= hi) break;
-            const float sl = tot[ri], sb = tot[4 + ri];
-            if (i < lo || lane != 0) continue;
-            if (ST) {
-                const float2 o = q == a.S - 1 ? make_float2(0.f, 0.f) : S_acc(a)[i];
-                S_acc(a)[i] = make_float2(o.x + sl, o.y + sb);
-            } else if (q == a.S - 1) {
-                a.dleak[c.r0 + i] = sl;
-                a.dbias[c.r0 + i] = sb;
-            } else {
-                a.dleak[c.r0 + i] += sl;
-                a.dbias[c.r0 + i] += sb;
+            if (i < lo) continue;
+            // the element slots of row ri (value selects keep dl, db in registers)
+            float sl = 0.f, sb = 0.f;
+#pragma unroll
+            for (int el = 0; el < 4; ++el) {
+                sl += pb.ri[el] == ri ? dl[el] : 0.f;
+                sb += pb.ri[el] == ri ? db[el] : 0.f;
             }
+            float2 *pa = lacc + i * 32 + lane;
+            const float2 o = q == a.S - 1 ? make_float2(0.f, 0.f) : *pa;
+            *pa = make_float2(o.x + sl, o.y + sb);
         }
     }
 }
@@ -878,7 +863,7 @@ __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsi
     const int ka = S_srp(a)[c.nrows] > c.e0 ? S_srp(a)[c.nrows] : c.e0;
     const int ga = ka < c.e1 ? group_of(c, a.G, ka) : a.G;
     for (int b = lane; b < a.Bp; b += 32) {
-        const float x = carry_sum(a, S_scarry(a) + b, ga, a.G);
+        const float x = carry_sum(a, S_scarry(a) + b, ga, a.G, next_warp_group(a, ga));
         st_relaxed64(a.carry + (size_t)blockIdx.x * a.Bp + b,
                      ((unsigned long long)phase_id << 32) | __float_as_uint(x));
     }
@@ -944,11 +929,11 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         // a row's last edge lies in this CTA iff it has edges here: then its slot
         // holds the tail, and the groups holding its earlier edges carry the rest
         const int rs = __ldg(a.row_ptr + r), re = __ldg(a.row_ptr + r + 1);
-        int gr = -1;
+        int2 gr = make_int2(-1, 0);
         if (re > rs && re - 1 >= c.e0) {
             const int ga = group_of(c, a.G, rs > c.e0 ? rs : c.e0);
             const int gb = group_of(c, a.G, re - 1);
-            gr = (ga << 16) | gb;
+            gr = make_int2((ga << 16) | gb, next_warp_group(a, ga));
         }
         S_sgrp(a)[i] = gr;
     }
@@ -987,7 +972,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         } else {
             if (c.stage) {
                 const size_t ro = (size_t)c.r0 * Bp;
-                stage_rows<THREADS>(S_st1(a), a.A + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
+                stage_rows<THREADS>(S_st1(a), a.Pr + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
                 stage_rows<THREADS>(S_st2(a), a.H + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
                 stage_dout<THREADS>(a, c, a.T - 1);
                 cp_async_wait_all();
@@ -1009,7 +994,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
             cp_async_commit();  // its own group: part A waits for it alone
             if (s > 0) {
                 const int q = s - 1, tq = q / a.M;
-                stage_rows<THREADS>(S_st1(a), a.A + (size_t)q * NBp + ro, c.nrows, Bp);
+                stage_rows<THREADS>(S_st1(a), a.Pr + (size_t)q * NBp + ro, c.nrows, Bp);
                 stage_rows<THREADS>(S_st2(a), a.H + (size_t)q * NBp + ro, c.nrows, Bp);
                 if (q - tq * a.M == a.M - 1) stage_dout<THREADS>(a, c, tq);
             }
@@ -1037,7 +1022,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
             const size_t ro = (size_t)c.r0 * Bp;
             if (BWD) {
                 if (s > 0) {
-                    prefetch_l2(a.A + (size_t)(s - 1) * NBp + ro, rb);
+                    prefetch_l2(a.Pr + (size_t)(s - 1) * NBp + ro, rb);
                     prefetch_l2(a.H + (size_t)(s - 1) * NBp + ro, rb);
                 }
             } else {
@@ -1081,11 +1066,22 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         } else {
             if (c.stage) {
                 for (int j = tid; j < c.nrows * Bp; j += THREADS) a.G_[(size_t)c.r0 * Bp + j] = S_st0(a)[j];
-                for (int i = tid; i < c.nrows; i += THREADS) {
-                    a.dleak[c.r0 + i] = S_acc(a)[i].x;
-                    a.dbias[c.r0 + i] = S_acc(a)[i].y;
-                }
                 __syncthreads();
+            }
+            // d_leak, d_bias: each row's 32 per-lane partials, summed by a fixed
+            // butterfly
+            const float2 *lacc = c.stage ? S_acc(a) : a.lacc + (size_t)c.r0 * 32;
+            for (int i = warp; i < c.nrows; i += THREADS / 32) {
+                float2 v = lacc[i * 32 + lane];
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) {
+                    v.x += __shfl_xor_sync(kFull, v.x, m);
+                    v.y += __shfl_xor_sync(kFull, v.y, m);
+                }
+                if (lane == 0) {
+                    a.dleak[c.r0 + i] = v.x;
+                    a.dbias[c.r0 + i] = v.y;
+                }
             }
             from_rows<THREADS>(a.dstate0, a.G_, c.r0, c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
             for (int k = c.e0 + tid; k < c.e1; k += THREADS)
@@ -1126,7 +1122,7 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     L.o_srp = (int)o; o = align16(o + 4 * (size_t)rc);
     L.o_prm = (int)o; o = align16(o + 8 * (size_t)rc);
     L.o_slot = (int)o; o = align16(o + 4 * (size_t)rc);
-    L.o_grp = (int)o; o = align16(o + 4 * (size_t)rc);
+    L.o_grp = (int)o; o = align16(o + 8 * (size_t)rc);
     L.o_carry = (int)o; o = align16(o + 4 * (size_t)p.groups * p.Bp);
     L.o_tile = (int)o; o = align16(o + 4 * 32 * 33);
     const size_t budget = kMaxSmem - kStaticSmem - 1024;
@@ -1134,7 +1130,8 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     const size_t rows_pb = align16(4 * (size_t)rc * (p.Bp + 1));  // row stride Bp + 1
     const size_t graph_b = (dir == 0 ? 12 : 16) * (size_t)p.cap[dir] + 48;
     // finish operands: forward state + drives; backward G, A, H, dOut + two sums
-    const size_t stage_b = (dir == 0 ? 1 : 4) * rows_b + rows_pb + align16(8 * (size_t)rc) + align16(4 * (size_t)rc);
+    const size_t stage_b = (dir == 0 ? 1 : 4) * rows_b + rows_pb + (dir == 1 ? 8 * 32 * (size_t)rc : 0) +
+                           align16(4 * (size_t)rc);
     L.rows = o + rows_b <= budget;
     if (L.rows) o += rows_b;
     L.o_rows = (int)(o - (L.rows ? rows_b : 0));
@@ -1149,7 +1146,7 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     L.o_st2 = (int)o; o += dir == 1 ? sb : 0;
     L.o_st3 = (int)o; o += dir == 1 ? spb : 0;
     L.o_st4 = (int)o; o += dir == 1 ? sb : 0;
-    L.o_acc = (int)o; o = align16(o + (L.stage ? 8 * (size_t)rc : 0));
+    L.o_acc = (int)o; o = align16(o + (L.stage && dir == 1 ? 8 * 32 * (size_t)rc : 0));
     L.o_inp = (int)o; o = align16(o + (L.stage ? 4 * (size_t)rc : 0));
     L.bytes = o;
     return L;
@@ -1202,6 +1199,7 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.G_ = (float *)(sc + p.off_G);
     k.da = (float *)(sc + p.off_da);
     k.rowsum_g = (float *)(sc + p.off_rowsum);
+    k.lacc = (float2 *)(sc + p.off_lacc);
     k.bar_extra = (unsigned)options().barrier_extra;
     k.timeout_ns = (unsigned long long)options().timeout_ns;
 }
@@ -1303,6 +1301,8 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     off = align256(off + 8 * NBp);
     q.off_rowsum = off;
     off = align256(off + 4 * NBp);
+    q.off_lacc = off;
+    off = align256(off + 8 * 32 * (size_t)q.N);
     q.scratch_bytes = off;
     q.saved_bytes = 4 * NBp * (size_t)(2 * q.S + 1);
     *p = q;
@@ -1324,7 +1324,7 @@ ck_status launch_forward(const ck_graph *g, const Plan &p, const FwdIO &io, cuda
     k.state0 = io.state0;
     k.out = io.out;
     k.H = io.saved;
-    k.A = io.saved + (size_t)(p.S + 1) * p.N * p.Bp;
+    k.Pr = io.saved + (size_t)(p.S + 1) * p.N * p.Bp;
     return launch_all(k, p, false, s, launches);
 }
 
@@ -1339,7 +1339,7 @@ ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cud
     k.w = io.w;
     k.leak = io.leak;
     k.H = const_cast<float *>(io.saved);
-    k.A = const_cast<float *>(io.saved) + (size_t)(p.S + 1) * p.N * p.Bp;
+    k.Pr = const_cast<float *>(io.saved) + (size_t)(p.S + 1) * p.N * p.Bp;
     k.dout = io.dout;
     k.dw = io.dw;
     k.dleak = io.dleak;
