@@ -873,7 +873,9 @@ __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsi
 
 template <int THREADS, int NC, bool SMEMG, bool BWD>
 __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
-    constexpr int UNR = BWD ? (NC == 2 ? 4 : 2) : (NC == 2 ? 8 : 4);
+    // edges per gather batch: more loads in flight per lane measured slower
+    // (the L2 path congests), four per batch measured fastest for NC = 2
+    constexpr int UNR = BWD ? (NC == 2 ? 4 : 2) : (NC == 2 ? 4 : 4);
     __shared__ int s_ok, s_meta[8];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
