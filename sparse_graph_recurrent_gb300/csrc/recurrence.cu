@@ -603,18 +603,39 @@ __device__ __forceinline__ float carry_sum(const KArgs &a, const float *sc, int 
     return x;
 }
 
-// Row i's sum for column b: its slot (the part summed by the group holding its
-// last edge here) plus the carries of the groups holding its earlier edges; 0
-// for a row with no edges in this CTA.
+// Row sums of four (row, column) elements: each row's slot (the part summed by
+// the group holding its last edge here) plus the carries of the groups holding
+// its earlier edges (carry_sum's terms and order); 0 for a row with no edges
+// in this CTA.  Every load of the common case (at most two carry reads) is
+// unconditional, so the four elements' loads issue together; rows that cross
+// more warps finish in a second pass.
 template <bool RS>
-__device__ __forceinline__ float row_sum(const KArgs &a, const Cta &c, int i, int b) {
-    const int2 g2 = S_sgrp(a)[i];
-    const int gr = g2.x;
-    const size_t o = (size_t)i * a.Bp + b;
-    const float slot = RS ? c.rows[o] : __ldcg(c.rows + o);
-    const int ga = gr < 0 ? 0 : gr >> 16, gb = gr < 0 ? 0 : (gr & 0xffff);
-    const float x = gr < 0 ? 0.f : slot;
-    return x + carry_sum(a, S_scarry(a) + b, ga, gb, g2.y);
+__device__ __forceinline__ void row_sums4(const KArgs &a, const Cta &c, const int (&ii)[4],
+                                          const int (&bb)[4], float (&x)[4]) {
+    const float *sc = S_scarry(a);
+    float slot[4], cs[4];
+    int gb[4], h2[4];
+#pragma unroll
+    for (int el = 0; el < 4; ++el) {
+        const int2 g2 = S_sgrp(a)[ii[el]];
+        const int gr = g2.x;
+        const size_t o = (size_t)ii[el] * a.Bp + bb[el];
+        const float sv = RS ? c.rows[o] : __ldcg(c.rows + o);
+        const int ga = gr < 0 ? 0 : gr >> 16;
+        gb[el] = gr < 0 ? 0 : (gr & 0xffff);
+        const int h1 = g2.y;
+        const float v0 = sc[(size_t)min(ga, a.G - 1) * a.Bp + bb[el]];
+        const float v1 = sc[(size_t)min(h1, a.G - 1) * a.Bp + bb[el]];
+        slot[el] = gr < 0 ? 0.f : sv;
+        cs[el] = ga < gb[el] ? v0 : 0.f;
+        cs[el] += h1 < gb[el] ? v1 : 0.f;
+        h2[el] = h1 + a.EPW;
+    }
+#pragma unroll
+    for (int el = 0; el < 4; ++el)
+        for (int h = h2[el]; h < gb[el]; h += a.EPW) cs[el] += sc[(size_t)h * a.Bp + bb[el]];
+#pragma unroll
+    for (int el = 0; el < 4; ++el) x[el] = slot[el] + cs[el];
 }
 
 // Carries published by earlier CTAs for column b of the CTA's first row.
@@ -676,20 +697,26 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
             ii[el] = ok[el] ? i : hi - 1;  // an initialised row, read but not used
             bb[el] = ok[el] ? b : 0;
         }
+        row_sums4<RS>(a, c, ii, bb, x);
 #pragma unroll
         for (int el = 0; el < 4; ++el) {
             const size_t o = (size_t)ii[el] * Bp + bb[el];
-            x[el] = row_sum<RS>(a, c, ii[el], bb[el]);
             pr[el] = S_prm(a)[ii[el]];
             hp[el] = ST ? S_st0(a)[ii[el] * pstride(a) + bb[el]] : __ldcg(hin + (size_t)c.r0 * Bp + o);
-            dr[el] = 0.f;
+            // drive: loaded from a valid address whatever the row, kept only
+            // for a live column of an input row
+            const int bl = bb[el] < B ? bb[el] : B - 1;
             if (ST) {
                 const int j = S_inp(a)[ii[el]];
-                if (ok[el] && j >= 0 && bb[el] < B) dr[el] = S_st1(a)[(size_t)j * Bp + bb[el]];
+                const float v = S_st1(a)[(size_t)(j < 0 ? 0 : j) * Bp + bl];
+                dr[el] = ok[el] && j >= 0 && bb[el] < B ? v : 0.f;
             } else {
                 const int sl = S_sslot(a)[ii[el]];
-                if (ok[el] && sl >= 0 && bb[el] < B)
-                    dr[el] = __ldg(a.drives + ((size_t)t * a.n_in + sl) * B + bb[el]);
+                dr[el] = 0.f;
+                if (a.n_in > 0) {
+                    const float v = __ldg(a.drives + ((size_t)t * a.n_in + (sl < 0 ? 0 : sl)) * B + bl);
+                    dr[el] = ok[el] && sl >= 0 && bb[el] < B ? v : 0.f;
+                }
             }
         }
         if (lo == 0 && i0 == 0 && c.glob) {
@@ -768,22 +795,31 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
             ii[el] = ok[el] ? i : hi - 1;  // an initialised row, read but not used
             bb[el] = ok[el] ? b : 0;
         }
+        // every load below is unconditional (from a valid address) and the
+        // value is selected after, so the four elements' loads issue together
+        row_sums4<RS>(a, c, ii, bb, x);
 #pragma unroll
         for (int el = 0; el < 4; ++el) {
             const size_t o = (size_t)ii[el] * Bp + bb[el];
+            const int bl = bb[el] < B ? bb[el] : B - 1;
+            float g0, o0, p0, h0;
             lam[el] = S_prm(a)[ii[el]].x;
-            x[el] = pro ? 0.f : row_sum<RS>(a, c, ii[el], bb[el]);
             if (ST) {
-                gv[el] = pro ? 0.f : S_st0(a)[o];
-                ov[el] = step_end && bb[el] < B ? S_st3(a)[ii[el] * pstride(a) + bb[el]] : 0.f;
-                p[el] = q >= 0 ? S_st1(a)[o] : 0.f;
-                hv[el] = q >= 0 ? S_st2(a)[o] : 0.f;
+                g0 = S_st0(a)[o];
+                o0 = S_st3(a)[ii[el] * pstride(a) + bl];
+                p0 = S_st1(a)[o];
+                h0 = S_st2(a)[o];
             } else {
-                gv[el] = pro ? 0.f : __ldcg(a.G_ + ro + o);
-                ov[el] = step_end && bb[el] < B ? __ldg(dO + (size_t)bb[el] * a.N + ii[el]) : 0.f;
-                p[el] = q >= 0 ? __ldcs(Pq + o) : 0.f;
-                hv[el] = q >= 0 ? __ldg(Hq + o) : 0.f;
+                g0 = __ldcg(a.G_ + ro + o);
+                o0 = __ldg(dO + (size_t)bl * a.N + ii[el]);
+                p0 = __ldcs(Pq + o);
+                h0 = __ldg(Hq + o);
             }
+            x[el] = pro ? 0.f : x[el];
+            gv[el] = pro ? 0.f : g0;
+            ov[el] = step_end && bb[el] < B ? o0 : 0.f;
+            p[el] = q >= 0 ? p0 : 0.f;
+            hv[el] = q >= 0 ? h0 : 0.f;
         }
         if (!pro && lo == 0 && i0 == 0 && c.glob) {
 #pragma unroll
