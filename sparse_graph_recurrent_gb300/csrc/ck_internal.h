@@ -19,9 +19,15 @@ struct ck_graph {
     // into num_sms equal pieces of the merge path of (row ends, edges): the
     // most rows any piece finishes and the most edges any piece holds.
     int max_rows[2], max_edges[2];
+    // piece[d][c * kPieceInts + j] for CTA c: {r0, nrows, e0, e1, c_lo, publish}
+    // (first row, rows finished, edge range, first earlier CTA whose carries
+    // reach row r0, whether the piece ends inside a row it must publish)
+    int *piece[2];
 };
 
 namespace ck {
+
+constexpr int kPieceInts = 8;
 
 // Per-thread error reporting used by every ABI entry point.
 ck_status fail(ck_status s, const char *fmt, ...);

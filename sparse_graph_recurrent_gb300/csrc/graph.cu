@@ -244,6 +244,30 @@ __global__ void k_piece_bounds(const int *__restrict__ row_ptr, int N, int E, in
     }
 }
 
+// Per-CTA description of each merge-path piece (see ck_graph::piece), from
+// the P + 1 piece bounds.  One thread per piece.
+__global__ void k_piece_meta(const int *__restrict__ row_ptr, int N, int P,
+                             const int *__restrict__ pr, const int *__restrict__ pe,
+                             int *__restrict__ meta) {
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < P; c += gridDim.x * blockDim.x) {
+        const int r0 = pr[c], r1 = pr[c + 1], e0 = pe[c], e1 = pe[c + 1];
+        int clo = c;
+        if (c > 0 && e0 > row_ptr[r0]) {  // row r0 has edges in earlier pieces
+            clo = c - 1;
+            while (clo > 0 && pr[clo] == r0) --clo;
+        }
+        int *m = meta + (size_t)c * kPieceInts;
+        m[0] = r0;
+        m[1] = r1 - r0;
+        m[2] = e0;
+        m[3] = e1;
+        m[4] = clo;
+        m[5] = (c + 1 < P && r1 < N) ? 1 : 0;
+        m[6] = 0;
+        m[7] = 0;
+    }
+}
+
 struct DevBuf {
     void *p = nullptr;
     ~DevBuf() {
@@ -363,6 +387,9 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
         for (int d = 0; d < 2; ++d) {
             k_piece_bounds<<<(P + 256) / 256, 256, 0, s>>>(rps[d], N, E, P, pr, pe);
             CK_TRY(cudaGetLastError(), "piece bounds launch");
+            CK_TRY(cudaMalloc((void **)&g->piece[d], sizeof(int) * kPieceInts * P), "cudaMalloc piece");
+            k_piece_meta<<<(P + 255) / 256, 256, 0, s>>>(rps[d], N, P, pr, pe, g->piece[d]);
+            CK_TRY(cudaGetLastError(), "piece meta launch");
             CK_TRY(cudaMemcpyAsync(hr.data(), pr, sizeof(int) * (P + 1), cudaMemcpyDeviceToHost, s),
                    "copy piece rows");
             CK_TRY(cudaMemcpyAsync(he.data(), pe, sizeof(int) * (P + 1), cudaMemcpyDeviceToHost, s),

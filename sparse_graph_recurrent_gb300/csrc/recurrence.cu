@@ -68,6 +68,7 @@ struct KArgs {
     int stage;  // finish operands staged in shared memory (see Cta)
     int o_st0, o_st1, o_st2, o_st3, o_st4, o_inp, o_acc;
     const int *row_ptr, *col, *perm, *slot, *rowid;
+    const int *piece;  // per-CTA piece description, kPieceInts ints each
     const float *w, *leak, *bias, *drives, *state0;
     float *out;
     float *H, *Pr;  // saved states and proposals
@@ -174,17 +175,6 @@ __device__ __forceinline__ float wait_carry(const KArgs &a, const unsigned long 
         } while ((unsigned)(v >> 32) != phase_id);
     }
     return __uint_as_float((unsigned)v);
-}
-
-// Merge-path split: the largest r in [0, min(d, N)] with row_ptr[r] + r <= d.
-__device__ __forceinline__ int merge_search(const int *row_ptr, int N, long long d) {
-    int lo = 0, hi = (int)(d < (long long)N ? d : (long long)N);
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if ((long long)__ldg(row_ptr + mid) + mid <= d) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
 }
 
 // Transposes between the caller's batch-major [B][N] arrays and the
@@ -926,26 +916,9 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     Cta c;
     c.stage = a.stage != 0;
 
-    // ---- this CTA's piece of the merge path of (row ends, edges)
-    const long long items = (long long)N + a.E;
-    if (tid == 0) {
-        const long long d0 = (long long)cta * items / a.P;
-        const long long d1 = (long long)(cta + 1) * items / a.P;
-        const int r0 = merge_search(a.row_ptr, N, d0);
-        const int r1 = merge_search(a.row_ptr, N, d1);
-        s_meta[0] = r0;
-        s_meta[1] = r1 - r0;
-        s_meta[2] = (int)(d0 - r0);
-        s_meta[3] = (int)(d1 - r1);
-        // earlier CTAs whose carries reach this CTA's first row
-        int clo = cta;
-        if (cta > 0 && s_meta[2] > __ldg(a.row_ptr + r0)) {
-            clo = cta - 1;
-            while (clo > 0 && merge_search(a.row_ptr, N, (long long)clo * items / a.P) == r0) --clo;
-        }
-        s_meta[4] = clo;
-        s_meta[5] = (cta + 1 < a.P && r1 < N) ? 1 : 0;
-    }
+    // ---- this CTA's piece of the merge path of (row ends, edges), computed
+    // when the graph was built
+    if (tid < 6) s_meta[tid] = __ldg(a.piece + (size_t)cta * kPieceInts + tid);
     __syncthreads();
     c.r0 = s_meta[0];
     c.nrows = s_meta[1];
@@ -975,14 +948,34 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         }
         S_sgrp(a)[i] = gr;
     }
-    for (int k = c.e0 + tid; k < c.e1; k += THREADS) {
-        if (SMEMG) {
-            S_scw(a)[k - c.e0] = make_int2(__ldg(a.col + k), __float_as_int(__ldg(a.w + __ldg(a.perm + k))));
-            S_srow(a)[k - c.e0] = __ldg(a.rowid + k);
-            if (BWD) S_sdw(a)[k - c.e0] = 0.f;
-        } else if (a.do_prologue) {
-            a.wperm[k] = __ldg(a.w + __ldg(a.perm + k));
-            if (BWD) a.dwperm[k] = 0.f;
+    // the CTA's edges: {col, w[perm[k]]} and row ids, eight edges per thread
+    // per pass so the independent loads (and then the dependent w loads) of a
+    // pass are in flight together
+    if (SMEMG || a.do_prologue) {
+        for (int kb = c.e0 + tid; kb < c.e1; kb += 8 * THREADS) {
+            int pm[8], cl[8], rw[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int k = kb + j * THREADS;
+                const int kc = k < c.e1 ? k : c.e0;  // a valid edge, result unused
+                pm[j] = __ldg(a.perm + kc);
+                cl[j] = SMEMG ? __ldg(a.col + kc) : 0;
+                rw[j] = SMEMG ? __ldg(a.rowid + kc) : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int k = kb + j * THREADS;
+                const float wv = __ldg(a.w + pm[j]);
+                if (k >= c.e1) continue;
+                if (SMEMG) {
+                    S_scw(a)[k - c.e0] = make_int2(cl[j], __float_as_int(wv));
+                    S_srow(a)[k - c.e0] = rw[j];
+                    if (BWD) S_sdw(a)[k - c.e0] = 0.f;
+                } else {
+                    a.wperm[k] = wv;
+                    if (BWD) a.dwperm[k] = 0.f;
+                }
+            }
         }
     }
     __syncthreads();
@@ -1122,8 +1115,20 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
                 }
             }
             from_rows<THREADS>(a.dstate0, a.G_, c.r0, c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
-            for (int k = c.e0 + tid; k < c.e1; k += THREADS)
-                a.dw[__ldg(a.perm + k)] = SMEMG ? S_sdw(a)[k - c.e0] : a.dwperm[k];
+            // dw back to the caller's edge order, eight edges per thread per pass
+            for (int kb = c.e0 + tid; kb < c.e1; kb += 8 * THREADS) {
+                int pm[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int k = kb + j * THREADS;
+                    pm[j] = __ldg(a.perm + (k < c.e1 ? k : c.e0));
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int k = kb + j * THREADS;
+                    if (k < c.e1) a.dw[pm[j]] = SMEMG ? S_sdw(a)[k - c.e0] : a.dwperm[k];
+                }
+            }
         }
     }
 }
@@ -1352,6 +1357,7 @@ ck_status launch_forward(const ck_graph *g, const Plan &p, const FwdIO &io, cuda
     KArgs k;
     fill_common(k, g, p, io.scratch, 0);
     k.row_ptr = g->row_ptr;
+    k.piece = g->piece[0];
     k.col = g->col;
     k.perm = g->perm;
     k.rowid = g->rowid;
@@ -1371,6 +1377,7 @@ ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cud
     KArgs k;
     fill_common(k, g, p, io.scratch, 1);
     k.row_ptr = g->rowT_ptr;
+    k.piece = g->piece[1];
     k.col = g->colT;
     k.perm = g->permT;
     k.rowid = g->rowidT;
