@@ -142,10 +142,13 @@ ck_status ck_graph_create(const int64_t *src, const int64_t *dst, int64_t E, int
 ck_status ck_graph_destroy(ck_graph *g) {
     if (!g) return CK_OK;
     cudaDeviceSynchronize();
-    int *ptrs[] = {g->row_ptr, g->col,    g->perm,  g->rowT_ptr, g->colT,    g->permT,
-                   g->slot,    g->rowid,  g->rowidT, g->piece[0], g->piece[1]};
+    int *ptrs[] = {g->row_ptr, g->col, g->perm, g->rowT_ptr, g->colT, g->permT,
+                   g->slot, g->rowid, g->rowidT};
     for (int *p : ptrs)
         if (p) cudaFree(p);
+    for (int d = 0; d < 2; ++d)
+        for (int v = 0; v < 3; ++v)
+            if (g->piece[d][v]) cudaFree(g->piece[d][v]);
     delete g;
     return CK_OK;
 }

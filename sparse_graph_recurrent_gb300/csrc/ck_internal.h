@@ -18,16 +18,26 @@ struct ck_graph {
     // Per direction (0: rows keyed by dst, 1: keyed by src), with the work cut
     // into num_sms equal pieces of the merge path of (row ends, edges): the
     // most rows any piece finishes and the most edges any piece holds.
-    int max_rows[2], max_edges[2];
-    // piece[d][c * kPieceInts + j] for CTA c: {r0, nrows, e0, e1, c_lo, publish}
-    // (first row, rows finished, edge range, first earlier CTA whose carries
-    // reach row r0, whether the piece ends inside a row it must publish)
-    int *piece[2];
+    //
+    // One cut per finish pass size v (kPassRows[v] rows finished at once by a
+    // CTA's warps): a weighted merge path, where a row end counts as w items
+    // and w is chosen so that few pieces hold more rows than one pass
+    // finishes.  piece[d][v][c * kPieceInts + j] for CTA c: {r0, nrows, e0,
+    // e1, c_lo, publish} (first row, rows finished, edge range, first earlier
+    // CTA whose carries reach row r0, whether the piece ends inside a row it
+    // must publish).
+    int max_rows[2][3], max_edges[2][3], row_weight[2][3];
+    int *piece[2][3];
 };
 
 namespace ck {
 
 constexpr int kPieceInts = 8;
+// Rows one finish pass of a CTA covers (16 warps, four (row, column-chunk)
+// elements per lane), by padded batch width: index 0 for Bp <= 32, 1 for
+// Bp <= 64, 2 above.
+constexpr int kPassRows[3] = {64, 32, 16};
+inline int pass_index(int Bp) { return Bp <= 32 ? 0 : (Bp <= 64 ? 1 : 2); }
 
 // Per-thread error reporting used by every ABI entry point.
 ck_status fail(ck_status s, const char *fmt, ...);

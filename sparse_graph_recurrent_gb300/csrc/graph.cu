@@ -229,43 +229,72 @@ __global__ void k_gather_other(const int64_t *__restrict__ other, const int *__r
 
 // First row and edge of each of P equal pieces of the merge path of
 // (row ends, edges): the largest r with row_ptr[r] + r <= floor(c (N+E) / P).
-__global__ void k_piece_bounds(const int *__restrict__ row_ptr, int N, int E, int P,
-                               int *__restrict__ out_r, int *__restrict__ out_e) {
-    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c <= P; c += gridDim.x * blockDim.x) {
-        const long long d = (long long)c * ((long long)N + E) / P;
-        int lo = 0, hi = (int)(d < N ? d : N);
+// One cut of the weighted merge path of (row ends, edges) into P pieces: a
+// row end counts as `wt` items, an edge as one.  Piece c starts at diagonal
+// d = c (E + wt N) / P: r = the rows whose ends come before d (the largest r
+// with row_ptr[r] + wt r <= d) and e = the edges before d, which lie between
+// row_ptr[r] and row_ptr[r + 1].  With wt = 1 this is the plain merge path.
+struct Cut {
+    std::vector<int> r, e;  // P + 1 bounds
+    int max_rows = 0, max_edges = 0;
+};
+
+Cut cut_pieces(const std::vector<int> &rp, int N, int E, int P, int wt) {
+    Cut k;
+    k.r.resize(P + 1);
+    k.e.resize(P + 1);
+    const long long items = (long long)E + (long long)wt * N;
+    for (int c = 0; c <= P; ++c) {
+        const long long d = (long long)c * items / P;
+        int lo = 0, hi = N;
         while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if ((long long)row_ptr[mid] + mid <= d) lo = mid;
+            const int mid = (lo + hi + 1) >> 1;
+            if ((long long)rp[mid] + (long long)wt * mid <= d) lo = mid;
             else hi = mid - 1;
         }
-        out_r[c] = lo;
-        out_e[c] = (int)(d - lo);
+        const long long e = d - (long long)wt * lo;
+        const int cap = rp[lo < N ? lo + 1 : N];
+        k.r[c] = lo;
+        k.e[c] = (int)(e < cap ? e : cap);
     }
+    for (int c = 0; c < P; ++c) {
+        k.max_rows = std::max(k.max_rows, k.r[c + 1] - k.r[c]);
+        k.max_edges = std::max(k.max_edges, k.e[c + 1] - k.e[c]);
+    }
+    return k;
 }
 
-// Per-CTA description of each merge-path piece (see ck_graph::piece), from
-// the P + 1 piece bounds.  One thread per piece.
-__global__ void k_piece_meta(const int *__restrict__ row_ptr, int N, int P,
-                             const int *__restrict__ pr, const int *__restrict__ pe,
-                             int *__restrict__ meta) {
-    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < P; c += gridDim.x * blockDim.x) {
-        const int r0 = pr[c], r1 = pr[c + 1], e0 = pe[c], e1 = pe[c + 1];
-        int clo = c;
-        if (c > 0 && e0 > row_ptr[r0]) {  // row r0 has edges in earlier pieces
-            clo = c - 1;
-            while (clo > 0 && pr[clo] == r0) --clo;
-        }
-        int *m = meta + (size_t)c * kPieceInts;
-        m[0] = r0;
-        m[1] = r1 - r0;
-        m[2] = e0;
-        m[3] = e1;
-        m[4] = clo;
-        m[5] = (c + 1 < P && r1 < N) ? 1 : 0;
-        m[6] = 0;
-        m[7] = 0;
+// Estimated time of the slowest piece, for choosing the row weight: part A
+// grows with a piece's edges, part B with the finish passes its rows need.
+double cut_cost(const Cut &k, int P, int pass_rows, double edge_us, double pass_us) {
+    double worst = 0.0;
+    for (int c = 0; c < P; ++c) {
+        const int rows = k.r[c + 1] - k.r[c], edges = k.e[c + 1] - k.e[c];
+        const int passes = (rows + pass_rows - 1) / pass_rows;
+        worst = std::max(worst, edges * edge_us + (passes > 0 ? passes : 1) * pass_us);
     }
+    return worst;
+}
+
+// Per-CTA piece descriptions (ck_graph::piece) of one cut.
+std::vector<int> piece_meta(const Cut &k, const std::vector<int> &rp, int N, int P) {
+    std::vector<int> m((size_t)P * kPieceInts, 0);
+    for (int c = 0; c < P; ++c) {
+        const int r0 = k.r[c], r1 = k.r[c + 1], e0 = k.e[c], e1 = k.e[c + 1];
+        int clo = c;
+        if (c > 0 && e0 > rp[r0]) {  // row r0 has edges in earlier pieces
+            clo = c - 1;
+            while (clo > 0 && k.r[clo] == r0) --clo;
+        }
+        int *q = m.data() + (size_t)c * kPieceInts;
+        q[0] = r0;
+        q[1] = r1 - r0;
+        q[2] = e0;
+        q[3] = e1;
+        q[4] = clo;
+        q[5] = (c + 1 < P && r1 < N) ? 1 : 0;
+    }
+    return m;
 }
 
 struct DevBuf {
@@ -378,30 +407,40 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
         CK_TRY(cudaGetLastError(), "row_ptr launch");
         // the second side reuses kb/vb; stream order already serialises it
     }
-    // piece bounds for launch sizing (one piece per SM)
+    // Pieces, one per SM, for each finish pass size.  The row weight is the
+    // one (of a few) whose slowest piece is estimated fastest: part A at about
+    // 1.5 ns per edge per 32 batch columns, a finish pass at about 0.8 us
+    // (measured on the FlyGPT-shaped graph); ties go to the smaller weight.
     {
         const int P = g->num_sms;
-        int *pr = kb, *pe = kb + (P + 1);  // kb is free now and holds >= 2 (P + 1) ints
-        std::vector<int> hr(P + 1), he(P + 1);
+        std::vector<int> rp(N + 1);
         const int *rps[2] = {g->row_ptr, g->rowT_ptr};
+        static const int weights[] = {1, 2, 3, 4, 6, 8, 12, 16};
         for (int d = 0; d < 2; ++d) {
-            k_piece_bounds<<<(P + 256) / 256, 256, 0, s>>>(rps[d], N, E, P, pr, pe);
-            CK_TRY(cudaGetLastError(), "piece bounds launch");
-            CK_TRY(cudaMalloc((void **)&g->piece[d], sizeof(int) * kPieceInts * P), "cudaMalloc piece");
-            k_piece_meta<<<(P + 255) / 256, 256, 0, s>>>(rps[d], N, P, pr, pe, g->piece[d]);
-            CK_TRY(cudaGetLastError(), "piece meta launch");
-            CK_TRY(cudaMemcpyAsync(hr.data(), pr, sizeof(int) * (P + 1), cudaMemcpyDeviceToHost, s),
-                   "copy piece rows");
-            CK_TRY(cudaMemcpyAsync(he.data(), pe, sizeof(int) * (P + 1), cudaMemcpyDeviceToHost, s),
-                   "copy piece edges");
-            CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (piece bounds)");
-            int mr = 0, me = 0;
-            for (int c = 0; c < P; ++c) {
-                mr = std::max(mr, hr[c + 1] - hr[c]);
-                me = std::max(me, he[c + 1] - he[c]);
+            CK_TRY(cudaMemcpyAsync(rp.data(), rps[d], sizeof(int) * (N + 1), cudaMemcpyDeviceToHost, s),
+                   "copy row pointers");
+            CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (row pointers)");
+            std::vector<Cut> cuts;
+            for (int wt : weights) cuts.push_back(cut_pieces(rp, (int)N, (int)E, P, wt));
+            for (int v = 0; v < 3; ++v) {
+                const double edge_us = 1.5e-3 * (v == 0 ? 1 : v == 1 ? 2 : 4);
+                int best = 0;
+                double best_cost = 0.0;
+                for (int i = 0; i < (int)cuts.size(); ++i) {
+                    const double cost = cut_cost(cuts[i], P, kPassRows[v], edge_us, 0.8);
+                    if (i == 0 || cost < best_cost) {
+                        best = i;
+                        best_cost = cost;
+                    }
+                }
+                const std::vector<int> m = piece_meta(cuts[best], rp, (int)N, P);
+                CK_TRY(cudaMalloc((void **)&g->piece[d][v], sizeof(int) * m.size()), "cudaMalloc piece");
+                CK_TRY(cudaMemcpy(g->piece[d][v], m.data(), sizeof(int) * m.size(), cudaMemcpyHostToDevice),
+                       "copy piece descriptions");
+                g->max_rows[d][v] = cuts[best].max_rows;
+                g->max_edges[d][v] = cuts[best].max_edges;
+                g->row_weight[d][v] = weights[best];
             }
-            g->max_rows[d] = mr;
-            g->max_edges[d] = me;
         }
     }
 #undef CK_TRY

@@ -1316,8 +1316,8 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     q.warps = q.threads / 32;
     q.groups = q.warps * q.EPW;
     for (int d = 0; d < 2; ++d) {
-        q.cap[d] = g->max_edges[d] + 1;
-        q.rows_cap[d] = g->max_rows[d] + 3;
+        q.cap[d] = g->max_edges[d][pass_index(q.Bp)] + 1;
+        q.rows_cap[d] = g->max_rows[d][pass_index(q.Bp)] + 3;
     }
     const bool want_graph = options().graph_in_smem && options().persistent;
     const bool want_stage = options().persistent != 0;
@@ -1357,7 +1357,7 @@ ck_status launch_forward(const ck_graph *g, const Plan &p, const FwdIO &io, cuda
     KArgs k;
     fill_common(k, g, p, io.scratch, 0);
     k.row_ptr = g->row_ptr;
-    k.piece = g->piece[0];
+    k.piece = g->piece[0][pass_index(p.Bp)];
     k.col = g->col;
     k.perm = g->perm;
     k.rowid = g->rowid;
@@ -1377,7 +1377,7 @@ ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cud
     KArgs k;
     fill_common(k, g, p, io.scratch, 1);
     k.row_ptr = g->rowT_ptr;
-    k.piece = g->piece[1];
+    k.piece = g->piece[1][pass_index(p.Bp)];
     k.col = g->colT;
     k.perm = g->permT;
     k.rowid = g->rowidT;
