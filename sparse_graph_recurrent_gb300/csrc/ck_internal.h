@@ -57,7 +57,7 @@ constexpr size_t kCtrlBytes = 256;
 
 // Shared-memory layout of one direction's kernel (byte offsets).
 struct SmemLayout {
-    int o_srp, o_prm, o_slot, o_grp, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;
+    int o_srp, o_prm, o_slot, o_grp, o_carry, o_rows, o_tile, o_cw, o_gst, o_dw;
     size_t bytes;
     bool graph;  // the CTA's slice of the graph lives in shared memory
     bool rows;   // row sums live in shared memory (else in global scratch)

@@ -64,7 +64,7 @@ struct KArgs {
     int cap, rows_cap;      // edges / rows (+2) bounds per CTA, for shared memory
     int rs_smem;            // row sums in shared memory (else in global scratch)
     // dynamic shared memory layout (byte offsets)
-    int o_srp, o_prm, o_slot, o_grp, o_carry, o_rows, o_tile, o_cw, o_row, o_dw;
+    int o_srp, o_prm, o_slot, o_grp, o_carry, o_rows, o_tile, o_cw, o_gst, o_dw;
     int stage;  // finish operands staged in shared memory (see Cta)
     int o_st0, o_st1, o_st2, o_st3, o_st4, o_inp, o_acc;
     const int *row_ptr, *col, *perm, *slot, *rowid;
@@ -258,7 +258,7 @@ __device__ __forceinline__ int2 *S_sgrp(const KArgs &a) { return reinterpret_cas
 __device__ __forceinline__ float *S_scarry(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_carry); }
 __device__ __forceinline__ float *S_tile(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_tile); }
 __device__ __forceinline__ int2 *S_scw(const KArgs &a) { return reinterpret_cast<int2 *>(ck_smem + a.o_cw); }
-__device__ __forceinline__ int *S_srow(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_row); }
+__device__ __forceinline__ int *S_gst(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_gst); }
 __device__ __forceinline__ float *S_sdw(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_dw); }
 __device__ __forceinline__ float *S_st0(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st0); }
 __device__ __forceinline__ float *S_st1(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st1); }
@@ -333,7 +333,6 @@ __device__ __forceinline__ int group_of(const Cta &c, int G, int k) {
 // fetched as soon as the current one starts.
 template <int NC, int UNR>
 struct Batch {
-    int rid[UNR];
     float w[UNR];
     float4 v[UNR][NC];
 };
@@ -378,8 +377,10 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     }
     const int len = k1 - k0;
     const int trips = (__reduce_max_sync(kFull, (unsigned)len) + UNR - 1) / UNR;
-    auto row_at = [&](int k) -> int { return SMEMG ? S_srow(a)[k - c.e0] : __ldg(a.rowid + k); };
-    int cur = len > 0 ? row_at(k0) : -1;
+    auto row_at = [&](int k) -> int { return __ldg(a.rowid + k); };
+    const int row0 = active ? S_gst(a)[gam] : -1;  // row of edge k0 (when k0 < e1), set up once
+    int cur = len > 0 ? row0 : -1;
+    int bnd = len > 0 ? S_srp(a)[cur - c.r0 + 1] : k1;  // end of cur's edges
     float4 acc[NC];
 #pragma unroll
     for (int ch = 0; ch < NC; ++ch) acc[ch] = zero4();
@@ -434,49 +435,60 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
 #pragma unroll
         for (int ch = 0; ch < NC; ++ch) acc[ch] = zero4();
     };
+    // Edges past the group's range (the warp runs to its longest group) load
+    // the CTA's first edge and weigh 0, so every load is unconditional.
     auto load = [&](Batch<NC, UNR> &bt, int kb) {
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
             const int kk = kb + q;
             const bool ok = kk < k1;
-            int cc = 0;
-            bt.rid[q] = -2;
-            bt.w[q] = 0.f;
-            if (ok) {
-                if (SMEMG) {
-                    const int2 cw = S_scw(a)[kk - c.e0];
-                    cc = cw.x;
-                    bt.w[q] = __int_as_float(cw.y);
-                    bt.rid[q] = S_srow(a)[kk - c.e0];
-                } else {
-                    cc = __ldg(a.col + kk);
-                    bt.w[q] = __ldcg(a.wperm + kk);
-                    bt.rid[q] = __ldg(a.rowid + kk);
-                }
+            const int kc = ok ? kk : c.e0;  // n > 0 whenever a batch runs
+            int cc;
+            float wv;
+            if (SMEMG) {
+                const int2 cw = S_scw(a)[kc - c.e0];
+                cc = cw.x;
+                wv = __int_as_float(cw.y);
+            } else {
+                cc = __ldg(a.col + kc);
+                wv = __ldcg(a.wperm + kc);
             }
+            bt.w[q] = ok ? wv : 0.f;
             const float *rp = rows + (size_t)cc * Bp + lig * 4;
 #pragma unroll
-            for (int ch = 0; ch < NC; ++ch)
-                bt.v[q][ch] = ok ? __ldca(reinterpret_cast<const float4 *>(rp + ch * CW)) : zero4();
+            for (int ch = 0; ch < NC; ++ch) bt.v[q][ch] = __ldca(reinterpret_cast<const float4 *>(rp + ch * CW));
+        }
+    };
+    // The group's current row is cur and its edges end at bnd = row_ptr[cur +
+    // 1]: an edge at or past bnd starts a later row (rows without edges are
+    // skipped).  A batch that no group of the warp sees cross its bound takes
+    // the path without per-edge checks.
+    auto next_row_at = [&](int kk) {
+        flush(cur);
+        do {
+            ++cur;
+        } while (S_srp(a)[cur - c.r0 + 1] <= kk);
+        bnd = S_srp(a)[cur - c.r0 + 1];
+        if (BWD) {
+            if (HS) {
+                hcur = load_h(cur);
+            } else {
+                hcur = cur == nxt ? hnext : load_h(cur);
+                nxt = next_row(cur);
+                hnext = load_h(nxt);
+            }
         }
     };
     auto consume = [&](const Batch<NC, UNR> &bt, int kb) {
         float d[UNR];
+        const int lim = kb + UNR < k1 ? kb + UNR : k1;
+        const bool inside = __all_sync(kFull, lim <= bnd);
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
             d[q] = 0.f;
-            if (bt.rid[q] != -2 && bt.rid[q] != cur) {
-                flush(cur);
-                cur = bt.rid[q];
-                if (BWD) {
-                    if (HS) {
-                        hcur = load_h(cur);
-                    } else {
-                        hcur = cur == nxt ? hnext : load_h(cur);
-                        nxt = next_row(cur);
-                        hnext = load_h(nxt);
-                    }
-                }
+            if (!inside) {
+                const int kk = kb + q;
+                if (kk < k1 && kk >= bnd) next_row_at(kk);
             }
 #pragma unroll
             for (int ch = 0; ch < NC; ++ch) fma4(acc[ch], bt.w[q], bt.v[q][ch]);
@@ -520,7 +532,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                          S_srp(a)[cur - c.r0 + 1] == k1;
         if (fin) flush(cur);
         // an empty group sits at edge k0 < e1 (n > 0): it takes that edge's row
-        lab = len > 0 ? cur : (k0 < c.e1 ? row_at(k0) : -1);
+        lab = len > 0 ? cur : row0;
     }
     // Segmented suffix sums over the warp's groups: a group adds the carry of
     // the group d places on while both carry the same row (labels do not
@@ -948,19 +960,24 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         }
         S_sgrp(a)[i] = gr;
     }
-    // the CTA's edges: {col, w[perm[k]]} and row ids, eight edges per thread
+    // the row of each lane group's first edge (-1 past the CTA's edges)
+    for (int gi = tid; gi < a.G; gi += THREADS) {
+        const int n = c.e1 - c.e0;
+        const int k0 = c.e0 + (int)((long long)gi * n / a.G);
+        S_gst(a)[gi] = k0 < c.e1 ? __ldg(a.rowid + k0) : -1;
+    }
+    // the CTA's edges: {col, w[perm[k]]}, eight edges per thread
     // per pass so the independent loads (and then the dependent w loads) of a
     // pass are in flight together
     if (SMEMG || a.do_prologue) {
         for (int kb = c.e0 + tid; kb < c.e1; kb += 8 * THREADS) {
-            int pm[8], cl[8], rw[8];
+            int pm[8], cl[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int k = kb + j * THREADS;
                 const int kc = k < c.e1 ? k : c.e0;  // a valid edge, result unused
                 pm[j] = __ldg(a.perm + kc);
                 cl[j] = SMEMG ? __ldg(a.col + kc) : 0;
-                rw[j] = SMEMG ? __ldg(a.rowid + kc) : 0;
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -969,7 +986,6 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
                 if (k >= c.e1) continue;
                 if (SMEMG) {
                     S_scw(a)[k - c.e0] = make_int2(cl[j], __float_as_int(wv));
-                    S_srow(a)[k - c.e0] = rw[j];
                     if (BWD) S_sdw(a)[k - c.e0] = 0.f;
                 } else {
                     a.wperm[k] = wv;
@@ -1168,10 +1184,11 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     L.o_grp = (int)o; o = align16(o + 8 * (size_t)rc);
     L.o_carry = (int)o; o = align16(o + 4 * (size_t)p.groups * p.Bp);
     L.o_tile = (int)o; o = align16(o + 4 * 32 * 33);
+    L.o_gst = (int)o; o = align16(o + 4 * (size_t)p.groups);
     const size_t budget = kMaxSmem - kStaticSmem - 1024;
     const size_t rows_b = align16(4 * (size_t)rc * p.Bp);
     const size_t rows_pb = align16(4 * (size_t)rc * (p.Bp + 1));  // row stride Bp + 1
-    const size_t graph_b = (dir == 0 ? 12 : 16) * (size_t)p.cap[dir] + 48;
+    const size_t graph_b = (dir == 0 ? 8 : 12) * (size_t)p.cap[dir] + 32;
     // finish operands: forward state + drives; backward G, A, H, dOut + two sums
     const size_t stage_b = (dir == 0 ? 1 : 4) * rows_b + rows_pb + (dir == 1 ? 8 * 32 * (size_t)rc : 0) +
                            align16(4 * (size_t)rc);
@@ -1180,7 +1197,7 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     L.o_rows = (int)(o - (L.rows ? rows_b : 0));
     L.graph = want_graph && o + graph_b <= budget;
     L.o_cw = (int)o; o = align16(o + (L.graph ? 8 * (size_t)p.cap[dir] : 0));
-    L.o_row = (int)o; o = align16(o + (L.graph ? 4 * (size_t)p.cap[dir] : 0));
+
     L.o_dw = (int)o; o = align16(o + (L.graph && dir == 1 ? 4 * (size_t)p.cap[dir] : 0));
     L.stage = want_stage && o + stage_b <= budget;
     const size_t sb = L.stage ? rows_b : 0, spb = L.stage ? rows_pb : 0;
@@ -1222,7 +1239,7 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.o_rows = L.o_rows;
     k.o_tile = L.o_tile;
     k.o_cw = L.o_cw;
-    k.o_row = L.o_row;
+    k.o_gst = L.o_gst;
     k.o_dw = L.o_dw;
     k.stage = L.stage ? 1 : 0;
     k.o_st0 = L.o_st0;
