@@ -748,8 +748,116 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
     }
 }
 
+
+// ---- finish for Bp <= 32 with staged operands and row slots in shared memory
+// (every FlyGPT-shaped workload).  Warp w takes the CTA's rows at positions
+// w, w + 16, ... of the order r0 + 1, ..., r0 + nrows - 1, r0 (a first row
+// that waits for earlier CTAs' carries comes last), one row per iteration,
+// lane = batch column; every warp has rows, shared-memory offsets are 32-bit,
+// and the arithmetic is the batched finish's, term for term, so both give
+// identical results.
+
+// Row i's sum for column b (b < Bp): row_sums4's terms in its order.
+__device__ __forceinline__ float row_sum1(const KArgs &a, const Cta &c, int i, int b) {
+    const int2 g2 = S_sgrp(a)[i];
+    const int gr = g2.x;
+    const float *sc = S_scarry(a) + b;
+    const float sv = c.rows[i * a.Bp + b];
+    const int ga = gr < 0 ? 0 : gr >> 16, gb = gr < 0 ? 0 : (gr & 0xffff), h1 = g2.y;
+    const float v0 = sc[min(ga, a.G - 1) * a.Bp];
+    const float v1 = sc[min(h1, a.G - 1) * a.Bp];
+    float cs = ga < gb ? v0 : 0.f;
+    cs += h1 < gb ? v1 : 0.f;
+    for (int h = h1 + a.EPW; h < gb; h += a.EPW) cs += sc[h * a.Bp];
+    return (gr < 0 ? 0.f : sv) + cs;
+}
+
+template <int THREADS>
+__device__ __forceinline__ void finish_fwd_narrow(const KArgs &a, const Cta &c, int s,
+                                                  unsigned phase_id) {
+    constexpr int U = THREADS / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Bp = a.Bp, B = a.B, PS = Bp + 1;
+    const size_t NBp = (size_t)a.N * Bp;
+    float *hout = a.H + (size_t)(s + 1) * NBp + (size_t)c.r0 * Bp;
+    float *pout = a.Pr + (size_t)s * NBp + (size_t)c.r0 * Bp;
+    const bool lane_ok = lane < Bp, live = lane < B;
+    const int b = lane_ok ? lane : 0, bl = live ? lane : B - 1;
+    const int sh = c.glob ? 1 : 0;
+    for (int pos = warp; pos < c.nrows; pos += U) {
+        const int i = pos + sh < c.nrows ? pos + sh : 0;
+        float x = row_sum1(a, c, i, b);
+        const float2 pr = S_prm(a)[i];
+        const float hp = S_st0(a)[i * PS + b];
+        const int j = S_inp(a)[i];
+        const float dv = S_st1(a)[(j < 0 ? 0 : j) * Bp + bl];
+        const float dr = lane_ok && j >= 0 && live ? dv : 0.f;
+        if (i == 0 && c.glob && lane_ok) x += global_carry(a, c, b, phase_id);
+        const float av = x + pr.y + dr;
+        const float th = tanhf(av);
+        const float hv = live ? fmaf(pr.x, th, (1.f - pr.x) * hp) : 0.f;
+        if (lane_ok) {
+            S_st0(a)[i * PS + b] = hv;
+            hout[i * Bp + b] = hv;
+            __stcs(pout + i * Bp + b, live ? th : 0.f);
+        }
+    }
+}
+
+template <int THREADS>
+__device__ __forceinline__ void finish_bwd_narrow(const KArgs &a, const Cta &c, int s,
+                                                  unsigned phase_id) {
+    constexpr int U = THREADS / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Bp = a.Bp, B = a.B, M = a.M, PS = Bp + 1;
+    const size_t NBp = (size_t)a.N * Bp;
+    const bool pro = s == a.S;
+    const int q = s - 1;
+    const int tq = q >= 0 ? q / M : 0;
+    const bool step_end = q >= 0 && q - tq * M == M - 1;  // also the first visit of step tq
+    float *daq = a.da + (size_t)(q & 1) * NBp + (size_t)c.r0 * Bp;
+    const bool lane_ok = lane < Bp, live = lane < B;
+    const int b = lane_ok ? lane : 0, bl = live ? lane : B - 1;
+    const int sh = c.glob ? 1 : 0;
+    for (int pos = warp; pos < c.nrows; pos += U) {
+        const int i = pos + sh < c.nrows ? pos + sh : 0;
+        float x = row_sum1(a, c, i, b);
+        const float lam = S_prm(a)[i].x;
+        const int o = i * Bp + b;
+        const float g0 = S_st0(a)[o], o0 = S_st3(a)[i * PS + bl], p0 = S_st1(a)[o], h0 = S_st2(a)[o];
+        x = pro ? 0.f : x;
+        if (!pro && i == 0 && c.glob && lane_ok) x += global_carry(a, c, b, phase_id);
+        const float gv = pro ? 0.f : g0;
+        const float ov = step_end && live ? o0 : 0.f;
+        const float p = q >= 0 ? p0 : 0.f, hv = q >= 0 ? h0 : 0.f;
+        float gn = fmaf(gv, 1.f - lam, x) + ov;
+        if (!live) gn = 0.f;
+        if (lane_ok) S_st0(a)[o] = gn;
+        if (q < 0) continue;
+        float dl = 0.f, db = 0.f, d = 0.f;
+        if (lane_ok && live) {
+            d = gn * lam * (1.f - p * p);
+            dl = fmaf(gn, p - hv, dl);
+            db += d;
+            const int sl = S_sslot(a)[i];
+            if (sl >= 0) {
+                float *dd = a.ddrives + ((size_t)tq * a.n_in + sl) * B + lane;
+                *dd = step_end ? d : *dd + d;
+            }
+        }
+        if (lane_ok) daq[o] = d;
+        float2 *pa = S_acc(a) + i * 32 + lane;
+        const float2 old = q == a.S - 1 ? make_float2(0.f, 0.f) : *pa;
+        *pa = make_float2(old.x + (0.f + dl), old.y + (0.f + db));
+    }
+}
+
 template <int THREADS>
 __device__ void finish_fwd(const KArgs &a, const Cta &c, const PB &pb, int s, unsigned phase_id) {
+    if (a.Bp <= 32 && c.stage && a.rs_smem) {
+        finish_fwd_narrow<THREADS>(a, c, s, phase_id);
+        return;
+    }
     constexpr int U = THREADS / 32;
     const int warp = threadIdx.x >> 5;
     // a first row that waits for earlier CTAs' carries goes last, to the last warp
@@ -881,6 +989,10 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
 
 template <int THREADS>
 __device__ void finish_bwd(const KArgs &a, const Cta &c, const PB &pb, int s, unsigned phase_id) {
+    if (a.Bp <= 32 && c.stage && a.rs_smem) {
+        finish_bwd_narrow<THREADS>(a, c, s, phase_id);
+        return;
+    }
     constexpr int U = THREADS / 32;
     const int warp = threadIdx.x >> 5;
     const bool defer = c.glob && s != a.S;  // the prologue has no carries to wait for
