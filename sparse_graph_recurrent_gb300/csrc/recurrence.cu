@@ -87,13 +87,13 @@ struct KArgs {
 
 // ---------------------------------------------------------------- helpers
 
+__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long *p) {
     unsigned long long v;
@@ -138,9 +138,12 @@ __device__ bool grid_sync(const KArgs &a, unsigned idx, int *s_ok, F &&during) {
     if (threadIdx.x == 0) red_release_add(a.bar, 1u);
     during();
     if (threadIdx.x == 0) {
+        // the status word and the clock are checked every eighth poll, so a
+        // poll costs one round trip to the counter
         const unsigned long long t0 = globaltimer();
         int e = 0;
-        while (ld_acquire(a.bar) < target) {
+        for (unsigned n = 0; ld_acquire(a.bar) < target; ++n) {
+            if ((n & 7) != 7) continue;
             if ((e = ld_err(a.err)) != 0) break;
             if (globaltimer() - t0 > a.timeout_ns) {
                 atomicCAS(a.err, 0, kDevTimeout);
@@ -286,31 +289,32 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // all but the most recently committed group have landed
 __device__ __forceinline__ void cp_async_wait_but_last() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
+// The helpers below spread their work over nt threads, this one being number
+// t of them.
+
 // Copy this CTA's rows [r0, r0 + nrows) of a node-major array into shared memory.
-template <int THREADS>
-__device__ __forceinline__ void stage_rows(float *sdst, const float *gsrc, int nrows, int Bp) {
+__device__ __forceinline__ void stage_rows(float *sdst, const float *gsrc, int nrows, int Bp, int t,
+                                           int nt) {
     const int n16 = nrows * Bp / 4;
-    for (int j = threadIdx.x; j < n16; j += THREADS) cp_async16(sdst + 4 * j, gsrc + 4 * j);
+    for (int j = t; j < n16; j += nt) cp_async16(sdst + 4 * j, gsrc + 4 * j);
 }
 
-// Copy dOut of input step t for this CTA's rows (a [B][N] slab, rows r0 + i
+// Copy dOut of input step ts for this CTA's rows (a [B][N] slab, rows r0 + i
 // contiguous per column) into st3 as rows of stride Bp + 1: consecutive
 // threads read consecutive nodes of one column.
-template <int THREADS>
-__device__ __forceinline__ void stage_dout(const KArgs &a, const Cta &c, int t) {
-    const float *src = a.dout + (size_t)t * a.B * a.N + c.r0;
-    for (int j = threadIdx.x; j < c.nrows * a.B; j += THREADS) {
+__device__ __forceinline__ void stage_dout(const KArgs &a, const Cta &c, int ts, int t, int nt) {
+    const float *src = a.dout + (size_t)ts * a.B * a.N + c.r0;
+    for (int j = t; j < c.nrows * a.B; j += nt) {
         const int b = j / c.nrows, i = j - b * c.nrows;
         cp_async4(S_st3(a) + i * pstride(a) + b, src + (size_t)b * a.N + i);
     }
 }
 
-// Write the state held in st0 to output step t ([B][N] slab): consecutive
+// Write the state held in st0 to output step ts ([B][N] slab): consecutive
 // threads write consecutive nodes of one column.
-template <int THREADS>
-__device__ __forceinline__ void write_out(const KArgs &a, const Cta &c, int t) {
-    float *dst = a.out + (size_t)t * a.B * a.N + c.r0;
-    for (int j = threadIdx.x; j < c.nrows * a.B; j += THREADS) {
+__device__ __forceinline__ void write_out(const KArgs &a, const Cta &c, int ts, int t, int nt) {
+    float *dst = a.out + (size_t)ts * a.B * a.N + c.r0;
+    for (int j = t; j < c.nrows * a.B; j += nt) {
         const int b = j / c.nrows, i = j - b * c.nrows;
         __stcs(dst + (size_t)b * a.N + i, S_st0(a)[i * pstride(a) + b]);
     }
@@ -750,10 +754,10 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
 
 
 // ---- finish for Bp <= 32 with staged operands and row slots in shared memory
-// (every FlyGPT-shaped workload).  Warp w takes the CTA's rows at positions
-// w, w + 16, ... of the order r0 + 1, ..., r0 + nrows - 1, r0 (a first row
-// that waits for earlier CTAs' carries comes last), one row per iteration,
-// lane = batch column; every warp has rows, shared-memory offsets are 32-bit,
+// (every FlyGPT-shaped workload).  Warp w takes rows r0 + sh + w, + 16, ...,
+// one row per iteration, lane = batch column, where sh = 1 when the first row
+// waits for earlier CTAs' carries: that row goes to the last warp, after its
+// others (the last warp has the fewest).  Shared-memory offsets are 32-bit,
 // and the arithmetic is the batched finish's, term for term, so both give
 // identical results.
 
@@ -784,8 +788,7 @@ __device__ __forceinline__ void finish_fwd_narrow(const KArgs &a, const Cta &c, 
     const bool lane_ok = lane < Bp, live = lane < B;
     const int b = lane_ok ? lane : 0, bl = live ? lane : B - 1;
     const int sh = c.glob ? 1 : 0;
-    for (int pos = warp; pos < c.nrows; pos += U) {
-        const int i = pos + sh < c.nrows ? pos + sh : 0;
+    auto row = [&](int i) {
         float x = row_sum1(a, c, i, b);
         const float2 pr = S_prm(a)[i];
         const float hp = S_st0(a)[i * PS + b];
@@ -801,7 +804,9 @@ __device__ __forceinline__ void finish_fwd_narrow(const KArgs &a, const Cta &c, 
             hout[i * Bp + b] = hv;
             __stcs(pout + i * Bp + b, live ? th : 0.f);
         }
-    }
+    };
+    for (int i = sh + warp; i < c.nrows; i += U) row(i);
+    if (sh && warp == U - 1) row(0);
 }
 
 template <int THREADS>
@@ -819,8 +824,7 @@ __device__ __forceinline__ void finish_bwd_narrow(const KArgs &a, const Cta &c, 
     const bool lane_ok = lane < Bp, live = lane < B;
     const int b = lane_ok ? lane : 0, bl = live ? lane : B - 1;
     const int sh = c.glob ? 1 : 0;
-    for (int pos = warp; pos < c.nrows; pos += U) {
-        const int i = pos + sh < c.nrows ? pos + sh : 0;
+    auto row = [&](int i) {
         float x = row_sum1(a, c, i, b);
         const float lam = S_prm(a)[i].x;
         const int o = i * Bp + b;
@@ -833,7 +837,7 @@ __device__ __forceinline__ void finish_bwd_narrow(const KArgs &a, const Cta &c, 
         float gn = fmaf(gv, 1.f - lam, x) + ov;
         if (!live) gn = 0.f;
         if (lane_ok) S_st0(a)[o] = gn;
-        if (q < 0) continue;
+        if (q < 0) return;
         float dl = 0.f, db = 0.f, d = 0.f;
         if (lane_ok && live) {
             d = gn * lam * (1.f - p * p);
@@ -849,7 +853,9 @@ __device__ __forceinline__ void finish_bwd_narrow(const KArgs &a, const Cta &c, 
         float2 *pa = S_acc(a) + i * 32 + lane;
         const float2 old = q == a.S - 1 ? make_float2(0.f, 0.f) : *pa;
         *pa = make_float2(old.x + (0.f + dl), old.y + (0.f + db));
-    }
+    };
+    for (int i = sh + warp; i < c.nrows; i += U) row(i);
+    if (sh && warp == U - 1) row(0);
 }
 
 template <int THREADS>
@@ -1131,9 +1137,9 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         } else {
             if (c.stage) {
                 const size_t ro = (size_t)c.r0 * Bp;
-                stage_rows<THREADS>(S_st1(a), a.Pr + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
-                stage_rows<THREADS>(S_st2(a), a.H + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp);
-                stage_dout<THREADS>(a, c, a.T - 1);
+                stage_rows(S_st1(a), a.Pr + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp, tid, THREADS);
+                stage_rows(S_st2(a), a.H + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp, tid, THREADS);
+                stage_dout(a, c, a.T - 1, tid, THREADS);
                 cp_async_wait_all();
             }
             __syncthreads();
@@ -1143,23 +1149,23 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     }
 
     // stage mode: issue the copies of microstep s's part-B operands into
-    // shared memory; they land while part A runs
-    auto stage_for = [&](int s) {
+    // shared memory (threads t of nt); they land while part A runs
+    auto stage_for = [&](int s, int t0, int nt) {
         const size_t ro = (size_t)c.r0 * Bp;
         if (BWD) {
             // part A's source rows: r0 .. r0 + nrows (the last one only if it exists)
-            stage_rows<THREADS>(S_st4(a), a.H + (size_t)s * NBp + ro,
-                                c.r0 + c.nrows < N ? c.nrows + 1 : c.nrows, Bp);
+            stage_rows(S_st4(a), a.H + (size_t)s * NBp + ro, c.r0 + c.nrows < N ? c.nrows + 1 : c.nrows,
+                       Bp, t0, nt);
             cp_async_commit();  // its own group: part A waits for it alone
             if (s > 0) {
                 const int q = s - 1, tq = q / a.M;
-                stage_rows<THREADS>(S_st1(a), a.Pr + (size_t)q * NBp + ro, c.nrows, Bp);
-                stage_rows<THREADS>(S_st2(a), a.H + (size_t)q * NBp + ro, c.nrows, Bp);
-                if (q - tq * a.M == a.M - 1) stage_dout<THREADS>(a, c, tq);
+                stage_rows(S_st1(a), a.Pr + (size_t)q * NBp + ro, c.nrows, Bp, t0, nt);
+                stage_rows(S_st2(a), a.H + (size_t)q * NBp + ro, c.nrows, Bp, t0, nt);
+                if (q - tq * a.M == a.M - 1) stage_dout(a, c, tq, t0, nt);
             }
         } else if (c.n_inp > 0 && s % a.M == 0) {
             const int t = s / a.M;
-            for (int j = tid; j < c.nrows * a.B; j += THREADS) {
+            for (int j = t0; j < c.nrows * a.B; j += nt) {
                 const int i = j / a.B, b = j - i * a.B;
                 const int ii = S_inp(a)[i];
                 if (ii >= 0)
@@ -1169,7 +1175,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         }
         cp_async_commit();
     };
-    if (c.stage && a.s_count > 0) stage_for(a.s_first);
+    if (c.stage && a.s_count > 0) stage_for(a.s_first, tid, THREADS);
 
     for (int it = 0; it < a.s_count; ++it) {
         const int s = BWD ? a.s_first - it : a.s_first + it;
@@ -1208,8 +1214,8 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
             // part B has read the old ones)
             auto between = [&]() {
                 if (!c.stage) return;
-                if (!BWD && s % a.M == a.M - 1) write_out<THREADS>(a, c, s / a.M);
-                stage_for(BWD ? s - 1 : s + 1);
+                if (!BWD && s % a.M == a.M - 1) write_out(a, c, s / a.M, tid, THREADS);
+                stage_for(BWD ? s - 1 : s + 1, tid, THREADS);
             };
             if (!grid_sync(a, nbar++, &s_ok, between)) {
                 cp_async_wait_all();
@@ -1221,7 +1227,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     if (a.do_epilogue) {
         __syncthreads();
         if (!BWD) {
-            if (c.stage) write_out<THREADS>(a, c, a.T - 1);
+            if (c.stage) write_out(a, c, a.T - 1, tid, THREADS);
         } else {
             if (c.stage) {
                 for (int j = tid; j < c.nrows * Bp; j += THREADS) a.G_[(size_t)c.r0 * Bp + j] = S_st0(a)[j];
