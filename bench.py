@@ -61,6 +61,25 @@ def ncu_traffic(kernel):
     return None
 
 
+def max_over_ranks(x, dist, device):
+    """The largest of every rank's x: a job of replicas takes as long as its
+    slowest rank."""
+    if not dist:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(local_total_ms, steps, world, dist, device):
+    """(job time in ms, whole-job steps/s) for `world` independent replicas
+    that each timed `steps` steps: every replica's steps over the slowest
+    rank's time."""
+    total_ms = max_over_ranks(local_total_ms, dist, device)
+    return total_ms, world * steps / (total_ms / 1e3)
+
+
 def byte_model(N, E, B, T, M, n_in):
     """Algorithmic bytes per launch (every byte that must reach the SMs).
 
@@ -250,13 +269,9 @@ def run_ours(args, c, rank, world, dist):
     _ck.ck_query_status(scratch)
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
     bwd_ms = [b.elapsed_time(c2) for _, b, c2 in ev]
-    total_ms = sum(a.elapsed_time(c2) for a, _, c2 in ev)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = replica_throughput(sum(a.elapsed_time(c2) for a, _, c2 in ev), args.steps,
+                                         world, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * args.steps / (total_ms / 1e3)
 
     # end to end through the public API: host inputs in, host results out
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
@@ -281,11 +296,7 @@ def run_ours(args, c, rank, world, dist):
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
 
     if rank != 0:
         return
