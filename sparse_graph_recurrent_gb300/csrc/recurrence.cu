@@ -341,12 +341,18 @@ struct Batch {
     float4 v[UNR][NC];
 };
 
-// Sum of d over the LPE lanes of each group.  With LPE == UNR (a power of two)
-// one exchange per halving leaves lane lig holding the total of item lig;
-// otherwise each item is reduced by a tree and lane 0 holds it.
+// Sum of d over the LPE lanes of each group.  With LPE a power of two and a
+// multiple of UNR (a power of two), the first log2(UNR) exchanges (lane
+// offsets LPE/2, LPE/4, ...) each keep half of the items, and the remaining
+// ones (offsets LPE/(2 UNR) ... 1) add: lane lig then holds in d[0] the total
+// of item lig / (LPE / UNR) (item lig when LPE == UNR).  Otherwise each item
+// is reduced by a tree and lane 0 holds it.
+__device__ __forceinline__ bool butterfly_dots(int lpe, int unr) {
+    return lpe >= unr && (lpe & (lpe - 1)) == 0 && (unr & (unr - 1)) == 0;
+}
 template <int UNR>
 __device__ __forceinline__ void group_dots(float (&d)[UNR], int lig, int lpe, int lpe_p2) {
-    if (lpe == UNR && (UNR & (UNR - 1)) == 0) {
+    if (lpe == UNR && (UNR & (UNR - 1)) == 0) {  // the common case, offsets known at compile time
 #pragma unroll
         for (int o = UNR / 2; o >= 1; o >>= 1) {
 #pragma unroll
@@ -357,6 +363,19 @@ __device__ __forceinline__ void group_dots(float (&d)[UNR], int lig, int lpe, in
                 d[j] = keep + __shfl_xor_sync(kFull, send, o);
             }
         }
+    } else if (butterfly_dots(lpe, UNR)) {
+        int off = lpe >> 1;
+#pragma unroll
+        for (int o = UNR / 2; o >= 1; o >>= 1, off >>= 1) {
+#pragma unroll
+            for (int j = 0; j < o; ++j) {
+                const bool hi = (lig & off) != 0;
+                const float keep = hi ? d[j + o] : d[j];
+                const float send = hi ? d[j] : d[j + o];
+                d[j] = keep + __shfl_xor_sync(kFull, send, off);
+            }
+        }
+        for (; off >= 1; off >>= 1) d[0] += __shfl_xor_sync(kFull, d[0], off);
     } else {
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
@@ -483,6 +502,10 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             }
         }
     };
+    // backward: the edge-gradient reduction's layout (see group_dots)
+    const bool bfly = BWD && butterfly_dots(a.LPE, UNR);
+    int per_sh = 0;
+    while (bfly && (UNR << per_sh) < a.LPE) ++per_sh;  // log2(LPE / UNR)
     auto consume = [&](const Batch<NC, UNR> &bt, int kb) {
         float d[UNR];
         const int lim = kb + UNR < k1 ? kb + UNR : k1;
@@ -503,9 +526,10 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
         }
         if (BWD) {
             group_dots<UNR>(d, lig, a.LPE, a.LPE_P2);
-            if (a.LPE == UNR && (UNR & (UNR - 1)) == 0) {
-                const int kk = kb + lig;
-                if (kk < k1) {
+            if (bfly) {
+                // lanes lig = m * (LPE / UNR) hold item m
+                const int kk = kb + (lig >> per_sh);
+                if ((lig & ((1 << per_sh) - 1)) == 0 && kk < k1) {
                     if (SMEMG) S_sdw(a)[kk - c.e0] += d[0];
                     else a.dwperm[kk] += d[0];
                 }
