@@ -459,8 +459,31 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
         for (int ch = 0; ch < NC; ++ch) acc[ch] = zero4();
     };
     // Edges past the group's range (the warp runs to its longest group) load
-    // the CTA's first edge and weigh 0, so every load is unconditional.
+    // the CTA's first edge and weigh 0, so every load is unconditional.  A
+    // graph streamed from global memory is read one batch ahead (into gc,
+    // gw), so a batch's gathers never wait on its own column loads.
+    int gc[SMEMG ? 1 : UNR];
+    float gw[SMEMG ? 1 : UNR];
+    auto load_graph = [&](int kb) {
+#pragma unroll
+        for (int q = 0; q < (SMEMG ? 1 : UNR); ++q) {
+            const int kk = kb + q;
+            const int kc = kk < k1 ? kk : c.e0;
+            gc[q] = __ldg(a.col + kc);
+            gw[q] = __ldcg(a.wperm + kc);
+        }
+    };
     auto load = [&](Batch<NC, UNR> &bt, int kb) {
+        int cn[UNR];
+        float wn[UNR];
+        if (!SMEMG) {
+#pragma unroll
+            for (int q = 0; q < UNR; ++q) {
+                cn[q] = gc[SMEMG ? 0 : q];
+                wn[q] = gw[SMEMG ? 0 : q];
+            }
+            load_graph(kb + UNR);  // next batch's edges (valid addresses past the end too)
+        }
 #pragma unroll
         for (int q = 0; q < UNR; ++q) {
             const int kk = kb + q;
@@ -473,8 +496,8 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                 cc = cw.x;
                 wv = __int_as_float(cw.y);
             } else {
-                cc = __ldg(a.col + kc);
-                wv = __ldcg(a.wperm + kc);
+                cc = cn[q];
+                wv = wn[q];
             }
             bt.w[q] = ok ? wv : 0.f;
             const float *rp = rows + (size_t)cc * Bp + lig * 4;
@@ -547,6 +570,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     };
 
     Batch<NC, UNR> bt;
+    if (!SMEMG && trips > 0) load_graph(k0);
     for (int it = 0; it < trips; ++it) {
         const int kb = k0 + it * UNR;
         load(bt, kb);
