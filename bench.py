@@ -7,12 +7,15 @@ One step = ck_forward + ck_backward over the whole window, inputs resident in
 HBM; the L2 is flushed (a 512 MB write) before every timed step and the flush
 is outside the timed events.  Prints one JSON line (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference|torch-sparse]
 
 With N > 1 (under torchrun) every rank runs an independent replica of the
 same step (the method has no exchange between replicas): weak scaling.
 --impl reference times the CPU oracle (fp64, single thread) on one batch
-column per step, scaled to the whole batch.
+column per step, scaled to the whole batch.  --impl torch-sparse times, for
+context only, the step written with torch.sparse.mm in a Python loop (the
+baseline the page compares its fused kernels with); it is not part of the
+library.
 """
 from __future__ import annotations
 
@@ -157,6 +160,58 @@ def cpu_oracle_sample(c, cols):
     t0 = time.perf_counter()
     oracle.run_case(c, batch_cols=cols)
     return time.perf_counter() - t0
+
+
+def torch_sparse_step(c, dev, dtype):
+    """One training step written with torch.sparse.mm in a Python loop over
+    T x microsteps, the backward by autograd (connectome-kernels page, "Why":
+    the torch.sparse COO baseline).  Returns (out [T, B, N], gradients of
+    L = sum(out * dOut) w.r.t. w, leak, bias, drives, state0)."""
+    import torch
+    N = c["N"]
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a), device=dev, dtype=dtype)  # noqa: E731
+    w, leak, bias = (t(c[k]).requires_grad_() for k in ("w", "leak", "bias"))
+    drives, state0 = t(c["drives"]).requires_grad_(), t(c["state0"]).requires_grad_()
+    dout = t(c["dout"])
+    idx = torch.stack([torch.as_tensor(c["dst"], device=dev), torch.as_tensor(c["src"], device=dev)])
+    inp = torch.as_tensor(c["input_nodes"], device=dev)
+    T, M = drives.shape[0], c["M"]
+    W = torch.sparse_coo_tensor(idx, w, (N, N), check_invariants=False).coalesce()  # W[dst][src]; repeated pairs add
+    h = state0.t()
+    outs = []
+    for ti in range(T):
+        drive = torch.zeros(N, h.shape[1], device=dev, dtype=dtype).index_put((inp,), drives[ti])
+        for _ in range(M):
+            p = torch.tanh(torch.sparse.mm(W, h) + drive + bias[:, None])
+            h = (1 - leak[:, None]) * h + leak[:, None] * p
+        outs.append(h.t())
+    out = torch.stack(outs)
+    (out * dout).sum().backward()
+    return out.detach(), [x.grad for x in (w, leak, bias, drives, state0)]
+
+
+def run_torch_sparse(args, c, rank):
+    if rank != 0:
+        return
+    import torch
+    dev = torch.device("cuda", 0)
+    for _ in range(max(args.warmup, 1)):
+        torch_sparse_step(c, dev, torch.float32)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        torch_sparse_step(c, dev, torch.float32)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({
+        "impl": "torch-sparse", "context_only": True, "metric": METRIC, "value": 1e3 / ms,
+        "unit": "steps/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": _workload_name(c)},
+        "note": "torch.sparse.mm in a Python loop over T x microsteps, autograd backward "
+                "(the page's baseline: 207 ms on B200)"}), flush=True)
 
 
 def run_reference(args, c, rank):
@@ -347,7 +402,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--impl", choices=["ours", "reference", "torch-sparse"], default="ours")
     ap.add_argument("--cpu-cols", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -358,6 +413,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         run_reference(args, c, rank)
+        return
+    if args.impl == "torch-sparse":
+        run_torch_sparse(args, c, rank)
         return
     dist = None
     if world > 1:
