@@ -167,6 +167,56 @@ ck_status ck_backward(const ck_graph *g, const float *edge_values, const float *
                       float *d_state0, void *scratch, size_t scratch_bytes, void *stream);
 
 /*
+ * Recomputing variant: the forward keeps only the state after every input
+ * step (T + 1 checkpoints instead of 2 T M + 1 saved rows), and the backward
+ * recomputes each input step's microsteps from its checkpoint before
+ * differentiating them.  The pages save every microstep's state and
+ * pre-activation ("Design notes": 2 x T x M x N x B floats); this trades one
+ * more forward pass (and two launches per input step) for about M times less
+ * saved memory.  Results equal ck_forward / ck_backward's bit for bit.
+ *
+ * ck_workspace_size_recompute -- bytes of the checkpoints and of the scratch
+ *   buffer for the two calls below (the scratch holds one input step's window
+ *   of M + 1 states and M proposals on top of ck_workspace_size's scratch).
+ *   Errors: as ck_workspace_size.
+ */
+ck_status ck_workspace_size_recompute(const ck_graph *g, int64_t B, int64_t T,
+                                      int64_t microsteps, size_t *ckpt_bytes,
+                                      size_t *scratch_bytes);
+
+/*
+ * ck_forward_checkpointed -- ck_forward that writes, instead of `saved`, the
+ * state after every input step:
+ *   ckpt   (device) >= ckpt_bytes, 16-byte aligned: float[T+1][N][Bp], Bp = B
+ *          rounded up as in `saved`; ckpt[0] is state0 transposed
+ * Other arguments, ownership and errors as ck_forward (scratch sized by
+ * ck_workspace_size_recompute).
+ */
+ck_status ck_forward_checkpointed(const ck_graph *g, const float *edge_values,
+                                  const float *leak, const float *bias, const float *drives,
+                                  const float *state0, int64_t B, int64_t T,
+                                  int64_t microsteps, float *states_out, void *ckpt,
+                                  size_t ckpt_bytes, void *scratch, size_t scratch_bytes,
+                                  void *stream);
+
+/*
+ * ck_backward_recompute -- ck_backward from checkpoints: for t = T-1 .. 0 it
+ * recomputes microsteps tM .. tM+M-1 from ckpt[t] (one launch) and runs the
+ * backward microsteps of step t (a second launch).  Needs bias and drives
+ * besides ck_backward's inputs, since it reruns the forward.
+ *   ckpt   (device) as filled by ck_forward_checkpointed with the same g, B, T,
+ *          microsteps and inputs
+ * Other arguments, ownership and errors as ck_backward (scratch sized by
+ * ck_workspace_size_recompute).
+ */
+ck_status ck_backward_recompute(const ck_graph *g, const float *edge_values, const float *leak,
+                                const float *bias, const float *drives, int64_t B, int64_t T,
+                                int64_t microsteps, const void *ckpt, size_t ckpt_bytes,
+                                const float *d_states, float *d_edge_values, float *d_leak,
+                                float *d_bias, float *d_drives, float *d_state0, void *scratch,
+                                size_t scratch_bytes, void *stream);
+
+/*
  * ck_forward_static_scratch -- ck_forward without a scratch buffer: the
  * temporary workspace comes from a 32 MiB array of device memory compiled into
  * the library.  The pages have no counterpart for this call; it exists for

@@ -100,30 +100,79 @@ def backward(graph: SparseGraph, edge_values, leak, B: int, T: int, microsteps: 
     return dw, dl, db, dd, dh
 
 
+def forward_checkpointed(graph: SparseGraph, edge_values, leak, bias, drives, state0,
+                         microsteps: int):
+    """Forward that keeps only the state after every input step: returns
+    (out [T,B,N], checkpoints, scratch buffer) for backward_recompute."""
+    B, N = state0.shape
+    T = drives.shape[0]
+    ckpt_b, scratch_b = _ck.ck_workspace_size_recompute(graph.handle, B, T, microsteps)
+    ckpt = torch.empty(ckpt_b, dtype=torch.uint8, device=state0.device)
+    scratch = torch.empty(scratch_b, dtype=torch.uint8, device=state0.device)
+    out = torch.empty((T, B, N), dtype=torch.float32, device=state0.device)
+    _ck.ck_forward_checkpointed(graph.handle, edge_values, leak, bias, drives, state0,
+                                microsteps, out, ckpt, scratch)
+    return out, ckpt, scratch
+
+
+def backward_recompute(graph: SparseGraph, edge_values, leak, bias, drives, B: int, T: int,
+                       microsteps: int, ckpt, d_out, scratch=None):
+    """Backward from checkpoints (recomputes each input step's microsteps):
+    returns (d_edge_values, d_leak, d_bias, d_drives, d_state0)."""
+    dev = d_out.device
+    N, E, n_in = graph.num_nodes, graph.num_edges, graph.num_inputs
+    if scratch is None:
+        _, scratch_b = _ck.ck_workspace_size_recompute(graph.handle, B, T, microsteps)
+        scratch = torch.empty(scratch_b, dtype=torch.uint8, device=dev)
+    dw = torch.empty(E, dtype=torch.float32, device=dev)
+    dl = torch.empty(N, dtype=torch.float32, device=dev)
+    db = torch.empty(N, dtype=torch.float32, device=dev)
+    dd = torch.empty((T, n_in, B), dtype=torch.float32, device=dev)
+    dh = torch.empty((B, N), dtype=torch.float32, device=dev)
+    _ck.ck_backward_recompute(graph.handle, edge_values, leak, bias, drives, B, T, microsteps,
+                              ckpt, d_out.contiguous(), dw, dl, db, dd, dh, scratch)
+    return dw, dl, db, dd, dh
+
+
 class _SparseRecurrence(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, edge_values, leak, bias, drives, state0, graph, microsteps):
+    def forward(ctx, edge_values, leak, bias, drives, state0, graph, microsteps, recompute):
         ev = edge_values.detach().contiguous()
         lk = leak.detach().contiguous()
-        out, saved, _ = forward(graph, ev, lk, bias.detach().contiguous(),
-                                drives.detach().contiguous(), state0.detach().contiguous(),
-                                microsteps)
-        ctx.graph, ctx.microsteps = graph, microsteps
+        bs = bias.detach().contiguous()
+        dr = drives.detach().contiguous()
+        if recompute:
+            out, saved, _ = forward_checkpointed(graph, ev, lk, bs, dr,
+                                                 state0.detach().contiguous(), microsteps)
+            ctx.save_for_backward(ev, lk, bs, dr)
+        else:
+            out, saved, _ = forward(graph, ev, lk, bs, dr, state0.detach().contiguous(),
+                                    microsteps)
+            ctx.save_for_backward(ev, lk)
+        ctx.graph, ctx.microsteps, ctx.recompute = graph, microsteps, recompute
         ctx.shape = (state0.shape[0], drives.shape[0])
         ctx.saved_buf = saved
-        ctx.save_for_backward(ev, lk)
         return out
 
     @staticmethod
     def backward(ctx, d_out):
-        ev, lk = ctx.saved_tensors
         B, T = ctx.shape
-        grads = backward(ctx.graph, ev, lk, B, T, ctx.microsteps, ctx.saved_buf, d_out)
+        if ctx.recompute:
+            ev, lk, bs, dr = ctx.saved_tensors
+            grads = backward_recompute(ctx.graph, ev, lk, bs, dr, B, T, ctx.microsteps,
+                                       ctx.saved_buf, d_out)
+        else:
+            ev, lk = ctx.saved_tensors
+            grads = backward(ctx.graph, ev, lk, B, T, ctx.microsteps, ctx.saved_buf, d_out)
         ctx.saved_buf = None
-        return (*grads, None, None)
+        return (*grads, None, None, None)
 
 
 def sparse_recurrence(edge_values, leak, bias, drives, state0, graph: SparseGraph,
-                      microsteps: int = 1):
-    """out[T, B, N]: node states after each of the T input steps."""
-    return _SparseRecurrence.apply(edge_values, leak, bias, drives, state0, graph, microsteps)
+                      microsteps: int = 1, recompute: bool = False):
+    """out[T, B, N]: node states after each of the T input steps.  With
+    recompute=True only the state after every input step is kept for the
+    backward, which recomputes the microsteps (about M times less memory, the
+    same results)."""
+    return _SparseRecurrence.apply(edge_values, leak, bias, drives, state0, graph, microsteps,
+                                   recompute)

@@ -54,6 +54,9 @@ def load() -> ctypes.CDLL:
         "ck_workspace_size": [p, i64, i64, i64, psz, psz],
         "ck_forward": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p, sz, p],
         "ck_backward": [p, p, p, i64, i64, i64, p, sz, p, p, p, p, p, p, p, sz, p],
+        "ck_workspace_size_recompute": [p, i64, i64, i64, psz, psz],
+        "ck_forward_checkpointed": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p, sz, p],
+        "ck_backward_recompute": [p, p, p, p, p, i64, i64, i64, p, sz, p, p, p, p, p, p, p, sz, p],
         "ck_query_status": [p, p],
         "ck_set_option": [ctypes.c_int, i64],
         "ck_forward_static_scratch": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p],
@@ -164,6 +167,44 @@ def ck_backward(handle, edge_values, leak, B, T, microsteps, saved, d_states, d_
                               _ptr(d_drives) if d_drives is not None and d_drives.numel() else None,
                               _ptr(d_state0), _ptr(scratch),
                               scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def ck_workspace_size_recompute(handle, B: int, T: int, microsteps: int):
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().ck_workspace_size_recompute(handle, B, T, microsteps, ctypes.byref(a),
+                                              ctypes.byref(b)))
+    return a.value, b.value
+
+
+def ck_forward_checkpointed(handle, edge_values, leak, bias, drives, state0, microsteps,
+                            states_out, ckpt, scratch, stream=None):
+    for t, n in ((edge_values, "edge_values"), (leak, "leak"), (bias, "bias"),
+                 (drives, "drives"), (state0, "state0"), (states_out, "states_out")):
+        _need(t, torch.float32, n)
+    B = state0.shape[0]
+    T = states_out.shape[0]
+    _check(load().ck_forward_checkpointed(
+        handle, _ptr(edge_values), _ptr(leak), _ptr(bias),
+        _ptr(drives) if drives is not None and drives.numel() else None, _ptr(state0), B, T,
+        microsteps, _ptr(states_out), _ptr(ckpt), ckpt.numel() * ckpt.element_size(),
+        _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def ck_backward_recompute(handle, edge_values, leak, bias, drives, B, T, microsteps, ckpt,
+                          d_states, d_edge_values, d_leak, d_bias, d_drives, d_state0, scratch,
+                          stream=None):
+    for t, n in ((edge_values, "edge_values"), (leak, "leak"), (bias, "bias"),
+                 (drives, "drives"), (d_states, "d_states"), (d_edge_values, "d_edge_values"),
+                 (d_leak, "d_leak"), (d_bias, "d_bias"), (d_drives, "d_drives"),
+                 (d_state0, "d_state0")):
+        _need(t, torch.float32, n)
+    has_in = drives is not None and drives.numel()
+    _check(load().ck_backward_recompute(
+        handle, _ptr(edge_values), _ptr(leak), _ptr(bias), _ptr(drives) if has_in else None, B, T,
+        microsteps, _ptr(ckpt), ckpt.numel() * ckpt.element_size(), _ptr(d_states),
+        _ptr(d_edge_values), _ptr(d_leak), _ptr(d_bias),
+        _ptr(d_drives) if d_drives is not None and d_drives.numel() else None, _ptr(d_state0),
+        _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream)))
 
 
 def ck_forward_static_scratch(handle, edge_values, leak, bias, drives, state0, microsteps,

@@ -216,6 +216,67 @@ ck_status ck_forward(const ck_graph *g, const float *edge_values, const float *l
     return launch_forward(g, p, io, (cudaStream_t)stream, &g_launches);
 }
 
+ck_status ck_workspace_size_recompute(const ck_graph *g, int64_t B, int64_t T,
+                                      int64_t microsteps, size_t *ckpt_bytes,
+                                      size_t *scratch_bytes) {
+    if (!g) return fail(CK_ERR_INVALID_ARG, "graph handle is NULL");
+    Plan p;
+    ck_status st = make_plan(g, B, T, microsteps, &p);
+    if (st != CK_OK) return st;
+    if (ckpt_bytes) *ckpt_bytes = p.ckpt_bytes;
+    if (scratch_bytes) *scratch_bytes = p.scratch_bytes_rc;
+    return CK_OK;
+}
+
+ck_status ck_forward_checkpointed(const ck_graph *g, const float *edge_values,
+                                  const float *leak, const float *bias, const float *drives,
+                                  const float *state0, int64_t B, int64_t T,
+                                  int64_t microsteps, float *states_out, void *ckpt,
+                                  size_t ckpt_bytes, void *scratch, size_t scratch_bytes,
+                                  void *stream) {
+    g_launches = 0;
+    ck_status st = check_graph(g);
+    if (st != CK_OK) return st;
+    Plan p;
+    st = make_plan(g, B, T, microsteps, &p);
+    if (st != CK_OK) return st;
+    if ((g->E > 0 && !edge_values) || !leak || !bias || !state0 || !states_out || !ckpt ||
+        !scratch || (g->n_in > 0 && !drives))
+        return fail(CK_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (misaligned(ckpt) || misaligned(scratch))
+        return fail(CK_ERR_INVALID_ARG, "ckpt and scratch must be 16-byte aligned");
+    if (ckpt_bytes < p.ckpt_bytes || scratch_bytes < p.scratch_bytes_rc)
+        return fail(CK_ERR_WORKSPACE, "workspace too small: ckpt %zu < %zu or scratch %zu < %zu",
+                    ckpt_bytes, p.ckpt_bytes, scratch_bytes, p.scratch_bytes_rc);
+    FwdIO io{edge_values, leak, bias, drives, state0, states_out, (float *)ckpt, scratch};
+    return launch_forward_ckpt(g, p, io, (cudaStream_t)stream, &g_launches);
+}
+
+ck_status ck_backward_recompute(const ck_graph *g, const float *edge_values, const float *leak,
+                                const float *bias, const float *drives, int64_t B, int64_t T,
+                                int64_t microsteps, const void *ckpt, size_t ckpt_bytes,
+                                const float *d_states, float *d_edge_values, float *d_leak,
+                                float *d_bias, float *d_drives, float *d_state0, void *scratch,
+                                size_t scratch_bytes, void *stream) {
+    g_launches = 0;
+    ck_status st = check_graph(g);
+    if (st != CK_OK) return st;
+    Plan p;
+    st = make_plan(g, B, T, microsteps, &p);
+    if (st != CK_OK) return st;
+    if ((g->E > 0 && (!edge_values || !d_edge_values)) || !leak || !bias || !ckpt || !d_states ||
+        !d_leak || !d_bias || !d_state0 || !scratch || (g->n_in > 0 && (!drives || !d_drives)))
+        return fail(CK_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (misaligned(ckpt) || misaligned(scratch))
+        return fail(CK_ERR_INVALID_ARG, "ckpt and scratch must be 16-byte aligned");
+    if (ckpt_bytes < p.ckpt_bytes || scratch_bytes < p.scratch_bytes_rc)
+        return fail(CK_ERR_WORKSPACE, "workspace too small: ckpt %zu < %zu or scratch %zu < %zu",
+                    ckpt_bytes, p.ckpt_bytes, scratch_bytes, p.scratch_bytes_rc);
+    RcIO io{edge_values, leak, bias, drives, (const float *)ckpt, d_states, d_edge_values,
+            d_leak, d_bias, d_drives, d_state0, scratch};
+    return launch_backward_recompute(g, p, io, (cudaStream_t)stream, &g_launches);
+}
+
 ck_status ck_backward(const ck_graph *g, const float *edge_values, const float *leak, int64_t B,
                       int64_t T, int64_t microsteps, const void *saved, size_t saved_bytes,
                       const float *d_states, float *d_edge_values, float *d_leak,

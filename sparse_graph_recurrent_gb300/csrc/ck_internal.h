@@ -76,6 +76,7 @@ struct Plan {
     int cap[2];       // bound on edges in one CTA's piece (0: forward rows, 1: transposed)
     int rows_cap[2];  // bound on rows one CTA touches, plus 2
     SmemLayout lay_fwd, lay_bwd;
+    SmemLayout lay_bwd_flat;  // backward without staging or graph slices (recomputing windows)
     // scratch layout (byte offsets)
     size_t off_ctrl, ctrl_bytes;
     size_t off_carry;   // float [P][Bp]
@@ -87,6 +88,11 @@ struct Plan {
     size_t off_lacc;    // float2 [N][32] per-lane d_leak / d_bias partials
     size_t scratch_bytes;
     size_t saved_bytes; // float [(S+1) + S][N][Bp]
+    // checkpointing forward / recomputing backward
+    size_t off_hwin;          // float [M+1][N][Bp] window of states (first two: the forward's slots)
+    size_t off_pwin;          // float [M][N][Bp] window of proposals
+    size_t scratch_bytes_rc;  // scratch for those calls (regular scratch plus the windows)
+    size_t ckpt_bytes;        // float [T+1][N][Bp] states after every input step
 };
 
 struct Options {
@@ -106,6 +112,14 @@ struct FwdIO {
     void *scratch;
 };
 
+struct RcIO {
+    const float *w, *leak, *bias, *drives;
+    const float *ckpt;
+    const float *dout;
+    float *dw, *dleak, *dbias, *ddrives, *dstate0;
+    void *scratch;
+};
+
 struct BwdIO {
     const float *w, *leak;
     const float *saved;
@@ -118,5 +132,9 @@ ck_status launch_forward(const ck_graph *g, const Plan &p, const FwdIO &io, cuda
                          int64_t *launches);
 ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cudaStream_t s,
                           int64_t *launches);
+ck_status launch_forward_ckpt(const ck_graph *g, const Plan &p, const FwdIO &io, cudaStream_t s,
+                              int64_t *launches);
+ck_status launch_backward_recompute(const ck_graph *g, const Plan &p, const RcIO &io,
+                                    cudaStream_t s, int64_t *launches);
 
 }  // namespace ck

@@ -71,7 +71,13 @@ struct KArgs {
     const int *piece;  // per-CTA piece description, kPieceInts ints each
     const float *w, *leak, *bias, *drives, *state0;
     float *out;
-    float *H, *Pr;  // saved states and proposals
+    float *H, *Pr;  // saved states and proposals (Pr null: proposals not kept)
+    // H[s] lives in slot s - h_off of H (modulo h_mod when h_mod > 0) and
+    // Pr[s] in slot s - p_off of Pr: the saved arrays by default, a one-step
+    // window when the backward recomputes, a two-slot ping-pong when the
+    // forward keeps only checkpoints
+    int h_off, h_mod, p_off;
+    float *ckpt;  // forward: also write the state after every input step here ([T+1][N][Bp])
     const float *dout;
     float *dw, *dleak, *dbias, *ddrives, *dstate0;
     float *G_, *da, *rowsum_g;
@@ -81,11 +87,21 @@ struct KArgs {
     unsigned long long *carry;  // [P][Bp] {float bits, phase id} words
     float *wperm, *dwperm;
     int s_first, s_count, do_prologue, do_epilogue;
+    int init_w, zero_dw;  // write the permuted edge values / clear the edge-gradient sums (global)
     unsigned bar_base, bar_extra;
     unsigned long long timeout_ns;
 };
 
 // ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ float *hrow(const KArgs &a, int s) {
+    int j = s - a.h_off;
+    if (a.h_mod > 0) j %= a.h_mod;
+    return a.H + (size_t)j * a.N * a.Bp;
+}
+__device__ __forceinline__ float *prow(const KArgs &a, int s) {
+    return a.Pr + (size_t)(s - a.p_off) * a.N * a.Bp;
+}
 
 __device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -313,6 +329,7 @@ __device__ __forceinline__ void stage_dout(const KArgs &a, const Cta &c, int ts,
 // Write the state held in st0 to output step ts ([B][N] slab): consecutive
 // threads write consecutive nodes of one column.
 __device__ __forceinline__ void write_out(const KArgs &a, const Cta &c, int ts, int t, int nt) {
+    if (!a.out) return;  // a recomputation writes no outputs
     float *dst = a.out + (size_t)ts * a.B * a.N + c.r0;
     for (int j = t; j < c.nrows * a.B; j += nt) {
         const int b = j / c.nrows, i = j - b * c.nrows;
@@ -736,9 +753,9 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
     const int t = s / a.M;
     const bool step_end = s - t * a.M == a.M - 1;
     const size_t NBp = (size_t)a.N * Bp;
-    const float *hin = a.H + (size_t)s * NBp;
-    float *hout = a.H + (size_t)(s + 1) * NBp;
-    float *pout = a.Pr + (size_t)s * NBp;
+    const float *hin = hrow(a, s);
+    float *hout = hrow(a, s + 1);
+    float *pout = a.Pr ? prow(a, s) : nullptr;
     for (int cb = 0; cb < pb.CB; ++cb) {
         int ii[4], bb[4];
         bool ok[4];
@@ -791,10 +808,11 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
             if (ok[el]) {
                 const size_t o = (size_t)ii[el] * Bp + bb[el];
                 if (ST) S_st0(a)[ii[el] * pstride(a) + bb[el]] = hv;
-                else if (step_end && live)
+                else if (step_end && live && a.out)
                     __stcs(a.out + ((size_t)t * B + bb[el]) * a.N + c.r0 + ii[el], hv);
                 hout[(size_t)c.r0 * Bp + o] = hv;
-                __stcs(pout + (size_t)c.r0 * Bp + o, p0);
+                if (pout) __stcs(pout + (size_t)c.r0 * Bp + o, p0);
+                if (a.ckpt && step_end) a.ckpt[(size_t)(t + 1) * NBp + (size_t)c.r0 * Bp + o] = hv;
             }
         }
     }
@@ -831,8 +849,11 @@ __device__ __forceinline__ void finish_fwd_narrow(const KArgs &a, const Cta &c, 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Bp = a.Bp, B = a.B, PS = Bp + 1;
     const size_t NBp = (size_t)a.N * Bp;
-    float *hout = a.H + (size_t)(s + 1) * NBp + (size_t)c.r0 * Bp;
-    float *pout = a.Pr + (size_t)s * NBp + (size_t)c.r0 * Bp;
+    const int t = s / a.M;
+    const bool step_end = s - t * a.M == a.M - 1;
+    float *hout = hrow(a, s + 1) + (size_t)c.r0 * Bp;
+    float *pout = a.Pr ? prow(a, s) + (size_t)c.r0 * Bp : nullptr;
+    float *ck = a.ckpt && step_end ? a.ckpt + (size_t)(t + 1) * NBp + (size_t)c.r0 * Bp : nullptr;
     const bool lane_ok = lane < Bp, live = lane < B;
     const int b = lane_ok ? lane : 0, bl = live ? lane : B - 1;
     const int sh = c.glob ? 1 : 0;
@@ -850,7 +871,8 @@ __device__ __forceinline__ void finish_fwd_narrow(const KArgs &a, const Cta &c, 
         if (lane_ok) {
             S_st0(a)[i * PS + b] = hv;
             hout[i * Bp + b] = hv;
-            __stcs(pout + i * Bp + b, live ? th : 0.f);
+            if (pout) __stcs(pout + i * Bp + b, live ? th : 0.f);
+            if (ck) ck[i * Bp + b] = hv;
         }
     };
     for (int i = sh + warp; i < c.nrows; i += U) row(i);
@@ -942,8 +964,9 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
     const bool step_end = q >= 0 && q - tq * M == M - 1;
     const bool first = q >= 0 && q - tq * M == M - 1;  // first visit of step tq going backwards
     const size_t ro = (size_t)c.r0 * Bp;
-    const float *Pq = a.Pr + (size_t)(q >= 0 ? q : 0) * NBp + ro;
-    const float *Hq = a.H + (size_t)(q >= 0 ? q : 0) * NBp + ro;
+    const int qc = q >= a.p_off ? q : a.p_off;  // a valid slot when q < 0
+    const float *Pq = prow(a, qc) + ro;
+    const float *Hq = hrow(a, qc) + ro;
     const float *dO = a.dout + (size_t)tq * B * a.N + c.r0;  // [B][N] slab of step tq
     float *daq = a.da + (size_t)(q & 1) * NBp + ro;
     // d_leak, d_bias terms summed per element slot over the column chunks
@@ -1135,7 +1158,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     // the CTA's edges: {col, w[perm[k]]}, eight edges per thread
     // per pass so the independent loads (and then the dependent w loads) of a
     // pass are in flight together
-    if (SMEMG || a.do_prologue) {
+    if (SMEMG || a.init_w) {
         for (int kb = c.e0 + tid; kb < c.e1; kb += 8 * THREADS) {
             int pm[8], cl[8];
 #pragma unroll
@@ -1155,7 +1178,7 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
                     if (BWD) S_sdw(a)[k - c.e0] = 0.f;
                 } else {
                     a.wperm[k] = wv;
-                    if (BWD) a.dwperm[k] = 0.f;
+                    if (BWD && a.zero_dw) a.dwperm[k] = 0.f;
                 }
             }
         }
@@ -1175,18 +1198,20 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     unsigned nbar = 0;
     if (a.do_prologue) {
         if (!BWD) {
-            to_rows<THREADS>(a.H, a.state0, c.r0, c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
-            if (c.stage) {
-                for (int j = tid; j < c.nrows * Bp; j += THREADS) {
+            to_rows<THREADS>(hrow(a, 0), a.state0, c.r0, c.r0 + c.nrows, a.B, Bp, N, S_tile(a));
+            for (int j = tid; j < c.nrows * Bp; j += THREADS) {
+                const float v = __ldcg(hrow(a, 0) + (size_t)c.r0 * Bp + j);
+                if (c.stage) {
                     const int i = j / Bp, b = j - i * Bp;
-                    S_st0(a)[i * pstride(a) + b] = __ldcg(a.H + (size_t)c.r0 * Bp + j);
+                    S_st0(a)[i * pstride(a) + b] = v;
                 }
+                if (a.ckpt) a.ckpt[(size_t)c.r0 * Bp + j] = v;
             }
         } else {
             if (c.stage) {
                 const size_t ro = (size_t)c.r0 * Bp;
-                stage_rows(S_st1(a), a.Pr + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp, tid, THREADS);
-                stage_rows(S_st2(a), a.H + (size_t)(a.S - 1) * NBp + ro, c.nrows, Bp, tid, THREADS);
+                stage_rows(S_st1(a), prow(a, a.S - 1) + ro, c.nrows, Bp, tid, THREADS);
+                stage_rows(S_st2(a), hrow(a, a.S - 1) + ro, c.nrows, Bp, tid, THREADS);
                 stage_dout(a, c, a.T - 1, tid, THREADS);
                 cp_async_wait_all();
             }
@@ -1196,19 +1221,29 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
         if (!grid_sync(a, nbar++, &s_ok)) return;
     }
 
+    if (!BWD && c.stage && !a.do_prologue) {
+        // a forward window that starts from a state already in H (the backward's
+        // recomputation): it becomes the resident state
+        for (int j = tid; j < c.nrows * Bp; j += THREADS) {
+            const int i = j / Bp, b = j - i * Bp;
+            S_st0(a)[i * pstride(a) + b] = __ldcg(hrow(a, a.s_first) + (size_t)c.r0 * Bp + j);
+        }
+        __syncthreads();
+    }
+
     // stage mode: issue the copies of microstep s's part-B operands into
     // shared memory (threads t of nt); they land while part A runs
     auto stage_for = [&](int s, int t0, int nt) {
         const size_t ro = (size_t)c.r0 * Bp;
         if (BWD) {
             // part A's source rows: r0 .. r0 + nrows (the last one only if it exists)
-            stage_rows(S_st4(a), a.H + (size_t)s * NBp + ro, c.r0 + c.nrows < N ? c.nrows + 1 : c.nrows,
+            stage_rows(S_st4(a), hrow(a, s) + ro, c.r0 + c.nrows < N ? c.nrows + 1 : c.nrows,
                        Bp, t0, nt);
             cp_async_commit();  // its own group: part A waits for it alone
             if (s > 0) {
                 const int q = s - 1, tq = q / a.M;
-                stage_rows(S_st1(a), a.Pr + (size_t)q * NBp + ro, c.nrows, Bp, t0, nt);
-                stage_rows(S_st2(a), a.H + (size_t)q * NBp + ro, c.nrows, Bp, t0, nt);
+                stage_rows(S_st1(a), prow(a, q) + ro, c.nrows, Bp, t0, nt);
+                stage_rows(S_st2(a), hrow(a, q) + ro, c.nrows, Bp, t0, nt);
                 if (q - tq * a.M == a.M - 1) stage_dout(a, c, tq, t0, nt);
             }
         } else if (c.n_inp > 0 && s % a.M == 0) {
@@ -1228,18 +1263,18 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     for (int it = 0; it < a.s_count; ++it) {
         const int s = BWD ? a.s_first - it : a.s_first + it;
         const unsigned phase_id = BWD ? (unsigned)(a.S - s) : (unsigned)(s + 1);
-        const float *rows = BWD ? a.da + (size_t)(s & 1) * NBp : a.H + (size_t)s * NBp;
+        const float *rows = BWD ? a.da + (size_t)(s & 1) * NBp : hrow(a, s);
         if (!c.stage && tid == 0 && c.nrows > 0) {
             // part B's operands of this CTA's rows, fetched into L2 during part A
             const unsigned rb = (unsigned)((size_t)c.nrows * Bp * 4);
             const size_t ro = (size_t)c.r0 * Bp;
             if (BWD) {
                 if (s > 0) {
-                    prefetch_l2(a.Pr + (size_t)(s - 1) * NBp + ro, rb);
-                    prefetch_l2(a.H + (size_t)(s - 1) * NBp + ro, rb);
+                    prefetch_l2(prow(a, s - 1) + ro, rb);
+                    prefetch_l2(hrow(a, s - 1) + ro, rb);
                 }
             } else {
-                prefetch_l2(a.H + (size_t)s * NBp + ro, rb);
+                prefetch_l2(hrow(a, s) + ro, rb);
             }
         }
         if (BWD && c.stage) {
@@ -1247,9 +1282,9 @@ __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
             // finish operands committed after it may still be in flight
             cp_async_wait_but_last();
             __syncthreads();
-            stream_piece<NC, SMEMG, BWD, UNR, true>(a, c, gam, lig, active, rows, a.H + (size_t)s * NBp);
+            stream_piece<NC, SMEMG, BWD, UNR, true>(a, c, gam, lig, active, rows, hrow(a, s));
         } else {
-            stream_piece<NC, SMEMG, BWD, UNR, false>(a, c, gam, lig, active, rows, a.H + (size_t)s * NBp);
+            stream_piece<NC, SMEMG, BWD, UNR, false>(a, c, gam, lig, active, rows, hrow(a, s));
         }
         if (c.stage) cp_async_wait_all();
         __syncthreads();
@@ -1378,7 +1413,8 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     return L;
 }
 
-void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int dir) {
+void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int dir,
+                 const SmemLayout *layout = nullptr) {
     std::memset(&k, 0, sizeof(k));
     k.N = p.N;
     k.E = p.E;
@@ -1395,7 +1431,7 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.G = p.groups;
     k.cap = p.cap[dir];
     k.rows_cap = p.rows_cap[dir];
-    const SmemLayout &L = dir == 0 ? p.lay_fwd : p.lay_bwd;
+    const SmemLayout &L = layout ? *layout : dir == 0 ? p.lay_fwd : p.lay_bwd;
     k.rs_smem = L.rows ? 1 : 0;
     k.o_srp = L.o_srp;
     k.o_prm = L.o_prm;
@@ -1430,6 +1466,21 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.timeout_ns = (unsigned long long)options().timeout_ns;
 }
 
+// One cooperative launch of the kernel for layout L with k's microstep range
+// and flags as given; the control words are cleared first.
+ck_status launch_once(KArgs &k, const Plan &p, const SmemLayout &L, bool bwd, cudaStream_t s) {
+    KernelFn fn = pick_kernel(p.NC, L.graph, bwd);
+    cudaError_t e = cudaFuncSetAttribute((const void *)fn,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    e = cudaMemsetAsync((char *)k.bar, 0, p.off_carry - p.off_ctrl + 8 * (size_t)p.P * p.Bp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (control words)");
+    void *args[] = {&k};
+    e = cudaLaunchCooperativeKernel((const void *)fn, dim3(p.P), dim3(p.threads), args, L.bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
+    return CK_OK;
+}
+
 ck_status launch_all(KArgs &k, const Plan &p, bool bwd, cudaStream_t s, int64_t *launches) {
     const SmemLayout &L = bwd ? p.lay_bwd : p.lay_fwd;
     KernelFn fn = pick_kernel(p.NC, L.graph, bwd);
@@ -1451,6 +1502,7 @@ ck_status launch_all(KArgs &k, const Plan &p, bool bwd, cudaStream_t s, int64_t 
     const int steps = persistent ? 1 : S;
     for (int i = 0; i < steps; ++i) {
         KArgs ki = k;
+        ki.init_w = ki.zero_dw = persistent || i == 0;
         if (persistent) {
             ki.s_first = bwd ? S - 1 : 0;
             ki.s_count = S;
@@ -1506,6 +1558,9 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     const bool want_stage = options().persistent != 0;
     q.lay_fwd = smem_layout(q, 0, want_graph, want_stage);
     q.lay_bwd = smem_layout(q, 1, want_graph, want_stage);
+    // the recomputing backward runs in windows of one input step, every
+    // accumulator in global memory
+    q.lay_bwd_flat = smem_layout(q, 1, false, false);
     if (q.lay_fwd.bytes > (size_t)(kMaxSmem - kStaticSmem) ||
         q.lay_bwd.bytes > (size_t)(kMaxSmem - kStaticSmem))
         return fail(CK_ERR_UNSUPPORTED, "per-CTA tables exceed shared memory (rows per SM too many)");
@@ -1530,6 +1585,15 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     q.off_lacc = off;
     off = align256(off + 8 * 32 * (size_t)q.N);
     q.scratch_bytes = off;
+    // recomputation windows (after the regular scratch): M + 1 states and M
+    // proposals of one input step; the checkpointing forward's two state
+    // slots use the first two
+    q.off_hwin = off;
+    off = align256(off + 4 * NBp * (size_t)(q.M + 1));
+    q.off_pwin = off;
+    off = align256(off + 4 * NBp * (size_t)q.M);
+    q.scratch_bytes_rc = off;
+    q.ckpt_bytes = 4 * NBp * (size_t)(q.T + 1);
     q.saved_bytes = 4 * NBp * (size_t)(2 * q.S + 1);
     *p = q;
     return CK_OK;
@@ -1553,6 +1617,101 @@ ck_status launch_forward(const ck_graph *g, const Plan &p, const FwdIO &io, cuda
     k.H = io.saved;
     k.Pr = io.saved + (size_t)(p.S + 1) * p.N * p.Bp;
     return launch_all(k, p, false, s, launches);
+}
+
+ck_status launch_forward_ckpt(const ck_graph *g, const Plan &p, const FwdIO &io, cudaStream_t s,
+                              int64_t *launches) {
+    KArgs k;
+    fill_common(k, g, p, io.scratch, 0);
+    k.row_ptr = g->row_ptr;
+    k.piece = g->piece[0][pass_index(p.Bp)];
+    k.col = g->col;
+    k.perm = g->perm;
+    k.rowid = g->rowid;
+    k.w = io.w;
+    k.leak = io.leak;
+    k.bias = io.bias;
+    k.drives = io.drives;
+    k.state0 = io.state0;
+    k.out = io.out;
+    k.H = (float *)((char *)io.scratch + p.off_hwin);  // two state slots, used in turn
+    k.h_mod = 2;
+    k.Pr = nullptr;
+    k.ckpt = io.saved;
+    return launch_all(k, p, false, s, launches);
+}
+
+ck_status launch_backward_recompute(const ck_graph *g, const Plan &p, const RcIO &io,
+                                    cudaStream_t s, int64_t *launches) {
+    const size_t NBp = (size_t)p.N * p.Bp;
+    float *hwin = (float *)((char *)io.scratch + p.off_hwin);
+    float *pwin = (float *)((char *)io.scratch + p.off_pwin);
+    const int M = p.M, T = p.T, S = p.S;
+    int64_t n = 0;
+    for (int t = T - 1; t >= 0; --t) {
+        // microsteps tM .. tM + M - 1 again, from the checkpoint of step t:
+        // states into window slots 0..M, proposals into slots 0..M-1
+        cudaError_t e = cudaMemcpyAsync(hwin, io.ckpt + (size_t)t * NBp, 4 * NBp,
+                                        cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (checkpoint)");
+        KArgs kf;
+        fill_common(kf, g, p, io.scratch, 0);
+        kf.row_ptr = g->row_ptr;
+        kf.piece = g->piece[0][pass_index(p.Bp)];
+        kf.col = g->col;
+        kf.perm = g->perm;
+        kf.rowid = g->rowid;
+        kf.w = io.w;
+        kf.leak = io.leak;
+        kf.bias = io.bias;
+        kf.drives = io.drives;
+        kf.H = hwin;
+        kf.h_off = t * M;
+        kf.Pr = pwin;
+        kf.p_off = t * M;
+        kf.s_first = t * M;
+        kf.s_count = M;
+        kf.do_prologue = 0;
+        kf.do_epilogue = 0;
+        kf.init_w = 1;  // the backward windows overwrite the shared permuted values
+        ck_status st = launch_once(kf, p, p.lay_fwd, false, s);
+        if (st != CK_OK) return st;
+        ++n;
+        // the backward iterations whose elementwise terms belong to step t:
+        // s = (t + 1) M .. tM + 1 (the first is the prologue for the last
+        // step), and s = 0 after step 0
+        KArgs kb;
+        fill_common(kb, g, p, io.scratch, 1, &p.lay_bwd_flat);
+        kb.row_ptr = g->rowT_ptr;
+        kb.piece = g->piece[1][pass_index(p.Bp)];
+        kb.col = g->colT;
+        kb.perm = g->permT;
+        kb.rowid = g->rowidT;
+        kb.w = io.w;
+        kb.leak = io.leak;
+        kb.H = hwin;
+        kb.h_off = t * M;
+        kb.Pr = pwin;
+        kb.p_off = t * M;
+        kb.dout = io.dout;
+        kb.dw = io.dw;
+        kb.dleak = io.dleak;
+        kb.dbias = io.dbias;
+        kb.ddrives = io.ddrives;
+        kb.dstate0 = io.dstate0;
+        const bool last_step = t == T - 1;
+        kb.do_prologue = last_step ? 1 : 0;
+        kb.s_first = last_step ? S - 1 : (t + 1) * M;
+        kb.s_count = (last_step ? M - 1 : M) + (t == 0 ? 1 : 0);
+        kb.do_epilogue = t == 0 ? 1 : 0;
+        kb.init_w = 1;
+        kb.zero_dw = last_step ? 1 : 0;
+        st = launch_once(kb, p, p.lay_bwd_flat, true, s);
+        if (st != CK_OK) return st;
+        ++n;
+    }
+    if (launches) *launches = n;
+    return CK_OK;
 }
 
 ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cudaStream_t s,
