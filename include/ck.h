@@ -217,6 +217,17 @@ ck_status ck_backward_recompute(const ck_graph *g, const float *edge_values, con
                                 size_t scratch_bytes, void *stream);
 
 /*
+ * ck_sgd_update -- param <- param - lr * grad over n floats (device arrays,
+ * both owned by the caller), so that a whole training step -- ck_forward,
+ * ck_backward, then this update of edge_values, leak and bias -- runs on the
+ * device and can be captured as one CUDA graph (TrainKernel page, intro: a
+ * captured step holds the forward, the gradients and the SGD update).
+ * Asynchronous on `stream`.  Errors: CK_ERR_INVALID_ARG (n < 0, NULL pointer
+ * with n > 0), CK_ERR_CUDA.
+ */
+ck_status ck_sgd_update(float *param, const float *grad, int64_t n, float lr, void *stream);
+
+/*
  * ck_forward_static_scratch -- ck_forward without a scratch buffer: the
  * temporary workspace comes from a 32 MiB array of device memory compiled into
  * the library.  The pages have no counterpart for this call; it exists for

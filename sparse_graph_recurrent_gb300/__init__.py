@@ -134,6 +134,62 @@ def backward_recompute(graph: SparseGraph, edge_values, leak, bias, drives, B: i
     return dw, dl, db, dd, dh
 
 
+class TrainStep:
+    """One training step -- forward, backward of L = sum(out * d_out), and an
+    SGD update of edge_values, leak and bias -- captured once as a CUDA graph
+    and replayed (TrainKernel page: a captured step holds the forward, the
+    gradients and the SGD update, with no per-operator host launches).
+
+    The parameters are updated in place; drives, state0 and d_out are read from
+    the tensors given here, so copy new inputs into them before a replay.
+    Calling the object replays the step and returns the step's output tensor
+    (overwritten by the next replay)."""
+
+    def __init__(self, graph: SparseGraph, edge_values, leak, bias, drives, state0, d_out,
+                 microsteps: int, lr: float):
+        self.graph, self.M = graph, microsteps
+        self.w, self.leak, self.bias = edge_values, leak, bias
+        self.drives, self.state0, self.d_out = drives, state0, d_out
+        dev = state0.device
+        B, N = state0.shape
+        T = drives.shape[0]
+        self.B, self.T = B, T
+        saved_b, _ = graph.workspace_size(B, T, microsteps)
+        self.saved = torch.empty(saved_b, dtype=torch.uint8, device=dev)
+        self.scratch = graph.scratch(B, T, microsteps)
+        self.out = torch.empty((T, B, N), dtype=torch.float32, device=dev)
+        E, n_in = graph.num_edges, graph.num_inputs
+        self.grads = (torch.empty(E, device=dev), torch.empty(N, device=dev),
+                      torch.empty(N, device=dev), torch.empty((T, n_in, B), device=dev),
+                      torch.empty((B, N), device=dev))
+        # one uncaptured pass with lr = 0 sets the kernels up and leaves the
+        # parameters as they are
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            self._step(0.0)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        self.cuda_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.cuda_graph):
+            self._step(lr)
+
+    def _step(self, lr: float):
+        g, M = self.graph, self.M
+        dw, dl, db, dd, dh = self.grads
+        _ck.ck_forward(g.handle, self.w, self.leak, self.bias, self.drives, self.state0, M,
+                       self.out, self.saved, self.scratch)
+        _ck.ck_backward(g.handle, self.w, self.leak, self.B, self.T, M, self.saved, self.d_out,
+                        dw, dl, db, dd, dh, self.scratch)
+        _ck.ck_sgd_update(self.w, dw, lr)
+        _ck.ck_sgd_update(self.leak, dl, lr)
+        _ck.ck_sgd_update(self.bias, db, lr)
+
+    def __call__(self):
+        self.cuda_graph.replay()
+        return self.out
+
+
 class _SparseRecurrence(torch.autograd.Function):
     @staticmethod
     def forward(ctx, edge_values, leak, bias, drives, state0, graph, microsteps, recompute):

@@ -55,6 +55,7 @@ def load() -> ctypes.CDLL:
         "ck_forward": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p, sz, p],
         "ck_backward": [p, p, p, i64, i64, i64, p, sz, p, p, p, p, p, p, p, sz, p],
         "ck_workspace_size_recompute": [p, i64, i64, i64, psz, psz],
+        "ck_sgd_update": [p, p, i64, ctypes.c_float, p],
         "ck_forward_checkpointed": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p, sz, p],
         "ck_backward_recompute": [p, p, p, p, p, i64, i64, i64, p, sz, p, p, p, p, p, p, p, sz, p],
         "ck_query_status": [p, p],
@@ -167,6 +168,15 @@ def ck_backward(handle, edge_values, leak, B, T, microsteps, saved, d_states, d_
                               _ptr(d_drives) if d_drives is not None and d_drives.numel() else None,
                               _ptr(d_state0), _ptr(scratch),
                               scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def ck_sgd_update(param, grad, lr: float, stream=None):
+    _need(param, torch.float32, "param")
+    _need(grad, torch.float32, "grad")
+    if param.shape != grad.shape:
+        raise ValueError("param and grad differ in shape")
+    _check(load().ck_sgd_update(_ptr(param), _ptr(grad), param.numel(), float(lr),
+                                _stream(stream)))
 
 
 def ck_workspace_size_recompute(handle, B: int, T: int, microsteps: int):
