@@ -8,6 +8,10 @@ HBM; the L2 is flushed (a 512 MB write) before every timed step and the flush
 is outside the timed events.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference|torch-sparse]
+                  [--config 0-4] [--microsteps M]
+
+--config picks another of the five synthetic workloads (default 1, the FlyGPT
+shape that the headline is quoted on); --microsteps overrides its M.
 
 With N > 1 (under torchrun) every rank runs an independent replica of the
 same step (the method has no exchange between replicas): weak scaling.
@@ -98,14 +102,26 @@ def byte_model(N, E, B, T, M, n_in):
     return fwd, bwd
 
 
+L2_BYTES = 126 << 20  # about what of the 129 MB L2 a working set can keep
+
+
 def hbm_bytes(N, E, B, T, M, n_in):
-    """Compulsory DRAM bytes per step when graph and state stay in L2: saved
-    activations written and read back, out, dOut, drives and their gradient,
-    state0 and its gradient, parameters and their gradients."""
+    """Compulsory DRAM bytes per step: saved activations written and read
+    back, out, dOut, drives and their gradient, state0 and its gradient,
+    parameters and their gradients, and the graph (both compressed-row copies)
+    once per step if it fits in L2, else once per microstep of each pass."""
     S = T * M
     saved = 2 * 4 * (2 * S + 1) * N * B
     io = 4 * (2 * T * N * B + 2 * T * n_in * B + 2 * N * B + 2 * E + 4 * N)
-    return saved + io
+    graph = 2 * (8 * E + 4 * (N + 1))
+    return saved + io + (graph if graph <= L2_BYTES else S * graph)
+
+
+def flops_per_step(N, E, B, T, M):
+    """Algorithmic floating-point operations of one step: per microstep about
+    6EB (gather multiply-add forward; gather and edge-gradient dot backward)
+    and 12NB elementwise."""
+    return T * M * (6 * E * B + 12 * N * B)
 
 
 class Clocks:
@@ -238,8 +254,12 @@ def run_reference(args, c, rank):
     print(json.dumps(line), flush=True)
 
 
+CONFIG_NAMES = {0: "tiny", 1: "flygpt", 2: "ragged", 3: "wide", 4: "connectome"}
+
+
 def _workload_name(c):
-    return f"flygpt N={c['N']} E={c['E']} B={c['B']} T={c['T']} M={c['M']}"
+    name = CONFIG_NAMES.get(c.get("config_id", 1), "workload")
+    return f"{name} N={c['N']} E={c['E']} B={c['B']} T={c['T']} M={c['M']}"
 
 
 def run_ours(args, c, rank, world, dist):
@@ -361,15 +381,22 @@ def run_ours(args, c, rank, world, dist):
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     hbm_peak, hbm_src = _peaks()
     q_hbm = hbm_bytes(N, E, B, T, M, n_in)
+    headline = c.get("config_id", 1) == 1 and M == 2
+    props = torch.cuda.get_device_properties(dev)
+    sm_mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+    fp32_peak = props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12  # 128 FP32 lanes per SM
+    gflop = flops_per_step(N, E, B, T, M) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": value / PAGE_STEPS_PER_S,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / PAGE_STEPS_PER_S if headline else None,
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": _workload_name(c), "parallelism": "replicas",
                    "l2": "flushed by a 512 MB write before every timed step (outside the events)"},
         "roofline": {"bound": "l2", "kernel": dom, "achieved": achieved, "peak": l2_read,
-                     "unit": "GB/s", "frac": achieved / l2_read, "traffic": ncu_traffic(dom),
+                     "unit": "GB/s", "frac": achieved / l2_read,
+                     "traffic": ncu_traffic(dom) if headline else None,
                      "peak_source": "measured in this run: dense 16-byte L2 reads of a 64 MB buffer"},
         "roofline_hbm": {"bound": "hbm", "achieved": q_hbm / (ms_per_step / 1e3) / 1e9,
                          "peak": hbm_peak, "unit": "GB/s",
@@ -377,6 +404,8 @@ def run_ours(args, c, rank, world, dist):
                          "peak_source": f"{hbm_src} (MEASURED_PEAKS.json hbm_gbs)",
                          "bytes_per_step": q_hbm},
         "l2_probe": {"dense_read_gbs": l2_read, "row_gather_gbs": l2_gather},
+        "flops": {"gflop_per_step": gflop, "achieved_tflops": gflop / ms_per_step,
+                  "fp32_fma_peak_tflops": fp32_peak, "frac": gflop / ms_per_step / fp32_peak},
         "kernels": {"forward_ms": f_mean, "backward_ms": b_mean,
                     "forward_gbs": fb / (f_mean / 1e3) / 1e9, "backward_gbs": bb / (b_mean / 1e3) / 1e9,
                     "forward_bytes": fb, "backward_bytes": bb},
@@ -405,10 +434,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference", "torch-sparse"], default="ours")
     ap.add_argument("--cpu-cols", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--config", type=int, choices=range(5), default=1)
+    ap.add_argument("--microsteps", type=int, default=None)
     args = ap.parse_args()
 
     import workloads
-    c = workloads.make(1)
+    c = workloads.make(args.config, M=args.microsteps)
+    c["config_id"] = args.config
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -107,7 +107,8 @@ ck_status ck_graph_export(const ck_graph *g, int32_t *row_ptr, int32_t *col, int
  *                  plus the initial state (connectome-kernels page, "Design
  *                  notes": 2 x T x M x N x B floats saved; the proposal stands in
  *                  for the pre-activation, which the backward needs only through
- *                  its tanh), rows padded to a multiple of 8 floats
+ *                  its tanh), rows padded to Bp floats: B rounded up to 8, to 32
+ *                  when 16 < B <= 32, to 16 above 256
  *   scratch_bytes  temporary device memory for one ck_forward or ck_backward
  *                  call; one scratch buffer may serve both, but two calls that
  *                  run at the same time need two buffers

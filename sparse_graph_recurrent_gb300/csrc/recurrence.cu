@@ -12,7 +12,8 @@
 //                   reduction; transposed CSR for the state gradient; state and
 //                   pre-activation saved after every microstep.
 //
-// Layout in device memory (fp32, rows padded to Bp = B rounded up to 8):
+// Layout in device memory (fp32, rows padded to Bp: B rounded up to 8; to 32
+// for 16 < B <= 32, which keeps four lanes per row; to 16 above 256):
 //   H[s+1][N][Bp]  state after microstep s; H[0] = state0 transposed
 //   Pr[s][N][Bp]   proposal tanh(pre-activation) of microstep s (the backward
 //                  needs only the proposal, so it is saved instead of the
@@ -1539,7 +1540,7 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     q.n_in = (int)g->n_in;
     q.B = (int)B;
     // a lane holds NC float4 chunks of a batch row; LPE lanes hold the row
-    q.Bp = (int)(B <= 256 ? (B + 7) / 8 * 8 : (B + 15) / 16 * 16);
+    q.Bp = (int)(B > 16 && B <= 32 ? 32 : B <= 256 ? (B + 7) / 8 * 8 : (B + 15) / 16 * 16);
     q.NC = q.Bp <= 256 ? 2 : 4;
     q.LPE = q.Bp / (4 * q.NC);
     q.EPW = 32 / q.LPE;
