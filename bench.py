@@ -355,12 +355,30 @@ def run_ours(args, c, rank, world, dist):
     h2d = sum(x.numel() * 4 for x in h_in.values())
     d2h = sum(x.numel() * 4 for x in h_out)
 
+    # The two large copies overlap compute on a second stream, as a user
+    # would pipeline them: dOut (needed only by the backward) goes in during
+    # the forward, and the states come back during the backward.
+    main, side = torch.cuda.current_stream(), torch.cuda.Stream()
+
     def e2e_step():
-        d = {k: v.to(dev, non_blocking=True) for k, v in h_in.items()}
+        d = {k: h_in[k].to(dev, non_blocking=True)
+             for k in ("w", "leak", "bias", "drives", "state0")}
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            d_out = h_in["dout"].to(dev, non_blocking=True)
+        d_out.record_stream(main)
+        dout_in = side.record_event()
         o, sv, sc = pkg.forward(g, d["w"], d["leak"], d["bias"], d["drives"], d["state0"], M)
-        grads = pkg.backward(g, d["w"], d["leak"], B, T, M, sv, d["dout"], sc)
-        for hdst, src in zip(h_out, (o, *grads)):
+        fwd_done = main.record_event()
+        with torch.cuda.stream(side):
+            side.wait_event(fwd_done)
+            h_out[0].copy_(o, non_blocking=True)
+        o.record_stream(side)
+        main.wait_event(dout_in)
+        grads = pkg.backward(g, d["w"], d["leak"], B, T, M, sv, d_out, sc)
+        for hdst, src in zip(h_out[1:], grads):
             hdst.copy_(src, non_blocking=True)
+        main.wait_stream(side)
 
     for _ in range(2):
         e2e_step()
