@@ -1102,8 +1102,10 @@ __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsi
 template <int THREADS, int NC, bool SMEMG, bool BWD>
 __global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
     // edges per gather batch: more loads in flight per lane measured slower
-    // (the L2 path congests), four per batch measured fastest for NC = 2
-    constexpr int UNR = BWD ? (NC == 2 ? 4 : 2) : (NC == 2 ? 4 : 4);
+    // (the L2 path congests); for NC = 2 three per batch measured fastest in
+    // the forward and four in the backward (whose dot-product butterfly wants
+    // a power of two)
+    constexpr int UNR = BWD ? (NC == 2 ? 4 : 2) : (NC == 2 ? 3 : 4);
     __shared__ int s_ok, s_meta[8];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
