@@ -20,31 +20,37 @@
 //                  pre-activation and the backward evaluates no tanh)
 //   G[N][Bp]       running state gradient (backward)
 //   da[2][N][Bp]   d(loss)/d(pre-activation), ping-pong between microsteps
+// H[s] and Pr[s] are addressed through hrow / prow, which map s to a slot:
+// the saved arrays by default, a window of one input step when the backward
+// recomputes, a two-slot ping-pong when the forward keeps only checkpoints.
 // The caller's [T][B][N] outputs and output gradients are read and written one
 // input step at a time, transposed through shared memory when staging is on.
 //
 // Work split.  One CTA per SM and one persistent cooperative launch per call;
 // microsteps are separated by a grid-wide barrier whose wait is bounded.  CTA
-// c owns the c-th of P equal pieces of the merge path of (row ends, edges):
-// a range of edges and the rows whose ends fall in its piece.  Inside the CTA
-// the edge range is cut into G equal sub-ranges, one per lane group (LPE
-// lanes that together hold one batch row as NC chunks of 16-byte loads; a
-// warp holds 32 / LPE groups).  Each microstep has two parts:
+// c owns the c-th of P pieces of a row-weighted merge path of (row ends,
+// edges), read from a table the graph build computed: a range of edges and
+// the rows whose ends fall in its piece.  Inside the CTA the edge range is cut
+// into G equal sub-ranges, one per lane group (LPE lanes that together hold
+// one batch row as NC chunks of 16-byte loads; a warp holds 32 / LPE groups).
+// Each microstep has two parts:
 //   A  every group walks its edges in order, UNR at a time: all the gathers of
 //      a batch are issued before any is used, whatever rows they belong to.
-//      When the row id changes, the group's running sum of the row that ended
+//      When the group passes the end edge of its current row, the running sum
 //      goes to that row's slot in shared memory; the partial sum of the row it
 //      stops inside goes to the group's carry slot, after the groups of a warp
 //      that carry the same row have added theirs together (a segmented sum
 //      over shuffles), so a row split over many groups leaves one carry per
 //      warp.
-//   B  after a CTA barrier, warps finish the CTA's rows, lane = batch column,
-//      up to four rows at a time: row slot, plus the carries of the groups
-//      that hold the row's earlier edges (and, for the CTA's first row, the
-//      carries earlier CTAs published), then the elementwise terms.  Every sum
-//      is taken in a fixed order: results do not depend on timing.
+//   B  after a CTA barrier, warps finish the CTA's rows, lane = batch column
+//      (one row per warp iteration for B <= 32 with staged operands, else four
+//      rows at a time): row slot, plus the carries of the groups that hold the
+//      row's earlier edges (and, for the CTA's first row, the carries earlier
+//      CTAs published), then the elementwise terms.  Every sum is taken in a
+//      fixed order: results do not depend on timing.
 // When a CTA's slice of the graph fits in shared memory it is loaded there
-// once per call; otherwise it streams from global memory every microstep.
+// once per call; otherwise it streams from global memory every microstep, each
+// batch's {col, w} read one batch ahead of its gathers.
 #include <algorithm>
 #include <cstring>
 #include <type_traits>
