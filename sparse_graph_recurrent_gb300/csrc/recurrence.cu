@@ -486,9 +486,23 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     // the CTA's first edge and weigh 0, so every load is unconditional.  A
     // graph streamed from global memory is read one batch ahead (into gc,
     // gw), so a batch's gathers never wait on its own column loads.
+    // backward: the edge-gradient reduction's layout (see group_dots)
+    const bool bfly = BWD && butterfly_dots(a.LPE, UNR);
+    int per_sh = 0;
+    while (bfly && (UNR << per_sh) < a.LPE) ++per_sh;  // log2(LPE / UNR)
+    const bool dw_owner = bfly && (lig & ((1 << per_sh) - 1)) == 0;  // writes item lig >> per_sh
     int gc[SMEMG ? 1 : UNR];
     float gw[SMEMG ? 1 : UNR];
+    // streamed backward with the butterfly layout: the edge-gradient sum this
+    // lane updates in a batch, read one batch ahead too, so the update is a
+    // store (each edge's sum is touched by its own group only, once per
+    // microstep)
+    float gdw = 0.f, cdw = 0.f;
     auto load_graph = [&](int kb) {
+        if (BWD && !SMEMG && dw_owner) {
+            const int kk = kb + (lig >> per_sh);
+            gdw = kk < k1 ? __ldcg(a.dwperm + kk) : 0.f;
+        }
 #pragma unroll
         for (int q = 0; q < (SMEMG ? 1 : UNR); ++q) {
             const int kk = kb + q;
@@ -506,6 +520,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                 cn[q] = gc[SMEMG ? 0 : q];
                 wn[q] = gw[SMEMG ? 0 : q];
             }
+            if (BWD) cdw = gdw;
             load_graph(kb + UNR);  // next batch's edges (valid addresses past the end too)
         }
 #pragma unroll
@@ -549,10 +564,6 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             }
         }
     };
-    // backward: the edge-gradient reduction's layout (see group_dots)
-    const bool bfly = BWD && butterfly_dots(a.LPE, UNR);
-    int per_sh = 0;
-    while (bfly && (UNR << per_sh) < a.LPE) ++per_sh;  // log2(LPE / UNR)
     auto consume = [&](const Batch<NC, UNR> &bt, int kb) {
         float d[UNR];
         const int lim = kb + UNR < k1 ? kb + UNR : k1;
@@ -578,7 +589,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                 const int kk = kb + (lig >> per_sh);
                 if ((lig & ((1 << per_sh) - 1)) == 0 && kk < k1) {
                     if (SMEMG) S_sdw(a)[kk - c.e0] += d[0];
-                    else a.dwperm[kk] += d[0];
+                    else a.dwperm[kk] = cdw + d[0];
                 }
             } else if (lig == 0) {
 #pragma unroll
