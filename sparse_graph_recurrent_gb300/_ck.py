@@ -102,6 +102,22 @@ def _need(t, dtype, name):
         raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
 
 
+def _shapes(handle, B: int, T: int, **tensors):
+    """The library sees only pointers, so every tensor's shape is checked here
+    against the graph's N, E, n_in and the call's B, T."""
+    N, E, n_in = ck_graph_info(handle)
+    want = {"edge_values": (E,), "d_edge_values": (E,), "leak": (N,), "d_leak": (N,),
+            "bias": (N,), "d_bias": (N,), "drives": (T, n_in, B), "d_drives": (T, n_in, B),
+            "state0": (B, N), "d_state0": (B, N), "states_out": (T, B, N), "d_states": (T, B, N)}
+    for name, t in tensors.items():
+        if t is None:
+            if name in ("drives", "d_drives") and n_in == 0:
+                continue
+            raise ValueError(f"{name} is required")
+        if tuple(t.shape) != want[name]:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {want[name]}")
+
+
 def ck_graph_create(src, dst, num_nodes: int, input_nodes, stream=None):
     for t, n in ((src, "src"), (dst, "dst"), (input_nodes, "input_nodes")):
         _need(t, torch.int64, n)
@@ -148,6 +164,8 @@ def ck_forward(handle, edge_values, leak, bias, drives, state0, microsteps, stat
         _need(t, torch.float32, n)
     B = state0.shape[0]
     T = states_out.shape[0]
+    _shapes(handle, B, T, edge_values=edge_values, leak=leak, bias=bias, drives=drives,
+            state0=state0, states_out=states_out)
     _check(load().ck_forward(handle, _ptr(edge_values), _ptr(leak), _ptr(bias),
                              _ptr(drives) if drives is not None and drives.numel() else None,
                              _ptr(state0), B, T, microsteps, _ptr(states_out),
@@ -162,6 +180,9 @@ def ck_backward(handle, edge_values, leak, B, T, microsteps, saved, d_states, d_
                  (d_edge_values, "d_edge_values"), (d_leak, "d_leak"), (d_bias, "d_bias"),
                  (d_drives, "d_drives"), (d_state0, "d_state0")):
         _need(t, torch.float32, n)
+    _shapes(handle, B, T, edge_values=edge_values, leak=leak, d_states=d_states,
+            d_edge_values=d_edge_values, d_leak=d_leak, d_bias=d_bias, d_drives=d_drives,
+            d_state0=d_state0)
     _check(load().ck_backward(handle, _ptr(edge_values), _ptr(leak), B, T, microsteps,
                               _ptr(saved), saved.numel() * saved.element_size(),
                               _ptr(d_states), _ptr(d_edge_values), _ptr(d_leak), _ptr(d_bias),
@@ -193,6 +214,8 @@ def ck_forward_checkpointed(handle, edge_values, leak, bias, drives, state0, mic
         _need(t, torch.float32, n)
     B = state0.shape[0]
     T = states_out.shape[0]
+    _shapes(handle, B, T, edge_values=edge_values, leak=leak, bias=bias, drives=drives,
+            state0=state0, states_out=states_out)
     _check(load().ck_forward_checkpointed(
         handle, _ptr(edge_values), _ptr(leak), _ptr(bias),
         _ptr(drives) if drives is not None and drives.numel() else None, _ptr(state0), B, T,
@@ -208,6 +231,9 @@ def ck_backward_recompute(handle, edge_values, leak, bias, drives, B, T, microst
                  (d_leak, "d_leak"), (d_bias, "d_bias"), (d_drives, "d_drives"),
                  (d_state0, "d_state0")):
         _need(t, torch.float32, n)
+    _shapes(handle, B, T, edge_values=edge_values, leak=leak, bias=bias, drives=drives,
+            d_states=d_states, d_edge_values=d_edge_values, d_leak=d_leak, d_bias=d_bias,
+            d_drives=d_drives, d_state0=d_state0)
     has_in = drives is not None and drives.numel()
     _check(load().ck_backward_recompute(
         handle, _ptr(edge_values), _ptr(leak), _ptr(bias), _ptr(drives) if has_in else None, B, T,
@@ -224,6 +250,8 @@ def ck_forward_static_scratch(handle, edge_values, leak, bias, drives, state0, m
         _need(t, torch.float32, n)
     B = state0.shape[0]
     T = states_out.shape[0]
+    _shapes(handle, B, T, edge_values=edge_values, leak=leak, bias=bias, drives=drives,
+            state0=state0, states_out=states_out)
     _check(load().ck_forward_static_scratch(
         handle, _ptr(edge_values), _ptr(leak), _ptr(bias),
         _ptr(drives) if drives is not None and drives.numel() else None, _ptr(state0), B, T,

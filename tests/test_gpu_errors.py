@@ -68,3 +68,30 @@ def test_barrier_timeout_is_reported_and_context_survives():
     out, grads = run_gpu(c, graph=g)
     ref_out, ref = oracle.run_case(c)
     assert_parity(out, grads, ref_out, ref, "after timeout")
+
+
+def test_binding_rejects_wrong_shapes_before_any_launch():
+    """The library sees only pointers; the binding checks every shape against
+    the graph and the call, so a mismatched tensor never reaches a kernel."""
+    from sparse_graph_recurrent_gb300 import _ck
+    c = workloads.small(402, 40, 300, 4, 5, 2, 2)
+    g = make_graph(c)
+    t = _io(c)
+    B, T, M = 5, 2, 2
+    saved_b, scratch_b = g.workspace_size(B, T, M)
+    out = torch.empty((T, B, 40), device="cuda")
+    saved = torch.empty(saved_b, dtype=torch.uint8, device="cuda")
+    scratch = torch.empty(scratch_b, dtype=torch.uint8, device="cuda")
+    bad = {
+        "drives": t["drives"][:, :3].contiguous(),        # n_in 3 instead of 4
+        "leak": t["leak"][:39].contiguous(),               # N - 1
+        "w": t["w"][:-1].contiguous(),                      # E - 1
+    }
+    for name, tensor in bad.items():
+        args = dict(t, **{name: tensor})
+        with pytest.raises(ValueError):
+            _ck.ck_forward(g.handle, args["w"], args["leak"], args["bias"], args["drives"],
+                           args["state0"], M, out, saved, scratch)
+    with pytest.raises(ValueError):
+        _ck.ck_forward(g.handle, t["w"], t["leak"], t["bias"], t["drives"], t["state0"], M,
+                       torch.empty((T, B, 41), device="cuda"), saved, scratch)
