@@ -16,7 +16,7 @@ struct ck_graph {
     int *slot;                     // slot[i] = k if input_nodes[k] == i, else -1
     int *rowid, *rowidT;           // row of each row-ordered edge (dst[perm[k]], src[permT[k]])
     // Per direction (0: rows keyed by dst, 1: keyed by src), with the work cut
-    // into num_sms equal pieces of the merge path of (row ends, edges): the
+    // into num_pieces(g) equal pieces of the merge path of (row ends, edges): the
     // most rows any piece finishes and the most edges any piece holds.
     //
     // One cut per finish pass size v (kPassRows[v] rows finished at once by a
@@ -33,10 +33,16 @@ struct ck_graph {
 namespace ck {
 
 constexpr int kPieceInts = 8;
-// Rows one finish pass of a CTA covers (16 warps, four (row, column-chunk)
-// elements per lane), by padded batch width: index 0 for Bp <= 32, 1 for
-// Bp <= 64, 2 above.
-constexpr int kPassRows[3] = {64, 32, 16};
+// Shape of the recurrence kernels: kCtasPerSm CTAs of kThreads threads on
+// every SM, the work cut into SMs x kCtasPerSm pieces.
+constexpr int kCtasPerSm = 2;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+inline int num_pieces(const ck_graph *g) { return g->num_sms * kCtasPerSm; }
+// Rows one finish pass of a CTA covers (kWarps warps, four (row,
+// column-chunk) elements per lane), by padded batch width: index 0 for
+// Bp <= 32, 1 for Bp <= 64, 2 above.
+constexpr int kPassRows[3] = {4 * kWarps, 2 * kWarps, kWarps};
 inline int pass_index(int Bp) { return Bp <= 32 ? 0 : (Bp <= 64 ? 1 : 2); }
 
 // Per-thread error reporting used by every ABI entry point.

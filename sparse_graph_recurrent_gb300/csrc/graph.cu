@@ -412,7 +412,7 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
     // 1.5 ns per edge per 32 batch columns, a finish pass at about 0.8 us
     // (measured on the FlyGPT-shaped graph); ties go to the smaller weight.
     {
-        const int P = g->num_sms;
+        const int P = num_pieces(g);
         std::vector<int> rp(N + 1);
         const int *rps[2] = {g->row_ptr, g->rowT_ptr};
         static const int weights[] = {1, 2, 3, 4, 6, 8, 12, 16};

@@ -26,7 +26,8 @@
 // The caller's [T][B][N] outputs and output gradients are read and written one
 // input step at a time, transposed through shared memory when staging is on.
 //
-// Work split.  One CTA per SM and one persistent cooperative launch per call;
+// Work split.  kCtasPerSm CTAs per SM (ck_internal.h) and one persistent
+// cooperative launch per call;
 // microsteps are separated by a grid-wide barrier whose wait is bounded.  CTA
 // c owns the c-th of P pieces of a row-weighted merge path of (row ends,
 // edges), read from a table the graph build computed: a range of edges and
@@ -61,9 +62,9 @@ namespace ck {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kMaxSmem = 227 * 1024;
+constexpr int kMaxSmem = 227 * 1024;      // shared memory one CTA may take
+constexpr int kSmemPerSm = 228 * 1024;    // shared memory an SM holds
 constexpr int kStaticSmem = 64;
-constexpr int kThreads = 512;
 
 struct KArgs {
     int N, E, n_in, B, Bp, LPE, EPW, LPE_P2, T, M, S;
@@ -1117,7 +1118,7 @@ __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsi
 // ------------------------------------------------------------------ kernel
 
 template <int THREADS, int NC, bool SMEMG, bool BWD>
-__global__ void __launch_bounds__(THREADS, 1) rec_kernel(const KArgs a) {
+__global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a) {
     // edges per gather batch: more loads in flight per lane measured slower
     // (the L2 path congests); for NC = 2 three per batch measured fastest in
     // the forward and four in the backward (whose dot-product butterfly wants
@@ -1406,7 +1407,8 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     L.o_carry = (int)o; o = align16(o + 4 * (size_t)p.groups * p.Bp);
     L.o_tile = (int)o; o = align16(o + 4 * 32 * 33);
     L.o_gst = (int)o; o = align16(o + 4 * (size_t)p.groups);
-    const size_t budget = kMaxSmem - kStaticSmem - 1024;
+    // kCtasPerSm CTAs share the SM's shared memory, 1 KB of it reserved per CTA
+    const size_t budget = std::min<size_t>(kMaxSmem, kSmemPerSm / kCtasPerSm - 1024) - kStaticSmem;
     const size_t rows_b = align16(4 * (size_t)rc * p.Bp);
     const size_t rows_pb = align16(4 * (size_t)rc * (p.Bp + 1));  // row stride Bp + 1
     const size_t graph_b = (dir == 0 ? 8 : 12) * (size_t)p.cap[dir] + 32;
@@ -1510,9 +1512,9 @@ ck_status launch_all(KArgs &k, const Plan &p, bool bwd, cudaStream_t s, int64_t 
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)fn, p.threads, L.bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    if (per_sm < 1)
-        return fail(CK_ERR_UNSUPPORTED, "kernel does not fit on an SM (%d threads, %zu B shared)",
-                    p.threads, L.bytes);
+    if (per_sm < kCtasPerSm)
+        return fail(CK_ERR_UNSUPPORTED, "%d CTAs of %d threads and %zu B shared do not fit on an SM",
+                    kCtasPerSm, p.threads, L.bytes);
     // barrier counter, status word and published carries start at zero
     e = cudaMemsetAsync((char *)k.bar, 0, p.off_carry - p.off_ctrl + 8 * (size_t)p.P * p.Bp, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (control words)");
@@ -1566,7 +1568,7 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     q.T = (int)T;
     q.M = (int)M;
     q.S = (int)(T * M);
-    q.P = g->num_sms;
+    q.P = num_pieces(g);
     q.threads = kThreads;
     q.warps = q.threads / 32;
     q.groups = q.warps * q.EPW;
@@ -1581,8 +1583,8 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     // the recomputing backward runs in windows of one input step, every
     // accumulator in global memory
     q.lay_bwd_flat = smem_layout(q, 1, false, false);
-    if (q.lay_fwd.bytes > (size_t)(kMaxSmem - kStaticSmem) ||
-        q.lay_bwd.bytes > (size_t)(kMaxSmem - kStaticSmem))
+    const size_t cta_smem = std::min<size_t>(kMaxSmem, kSmemPerSm / kCtasPerSm - 1024) - kStaticSmem;
+    if (q.lay_fwd.bytes > cta_smem || q.lay_bwd.bytes > cta_smem || q.lay_bwd_flat.bytes > cta_smem)
         return fail(CK_ERR_UNSUPPORTED, "per-CTA tables exceed shared memory (rows per SM too many)");
     const size_t NBp = (size_t)q.N * q.Bp;
     const size_t E1 = (size_t)(q.E > 0 ? q.E : 1);
