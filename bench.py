@@ -8,10 +8,12 @@ HBM; the L2 is flushed (a 512 MB write) before every timed step and the flush
 is outside the timed events.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference|torch-sparse]
-                  [--config 0-4] [--microsteps M]
+                  [--config 0-4] [--microsteps M] [--graph-in-host-memory]
 
 --config picks another of the five synthetic workloads (default 1, the FlyGPT
 shape that the headline is quoted on); --microsteps overrides its M.
+--graph-in-host-memory builds the graph with its edge-indexed arrays in pinned
+host memory, read by the kernels over the CPU-GPU link.
 
 With N > 1 (under torchrun) every rank runs an independent replica of the
 same step (the method has no exchange between replicas): weak scaling.
@@ -273,7 +275,8 @@ def run_ours(args, c, rank, world, dist):
     dev = torch.device("cuda", local)
     tt = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     N, E, B, T, M, n_in = c["N"], c["E"], c["B"], c["T"], c["M"], c["n_in"]
-    g = pkg.SparseGraph(tt(c["src"]), tt(c["dst"]), N, tt(c["input_nodes"]))
+    g = pkg.SparseGraph(tt(c["src"]), tt(c["dst"]), N, tt(c["input_nodes"]),
+                        edges_in_host_memory=args.graph_in_host_memory)
     w, leak, bias, drives, state0, dout = (tt(c[k]) for k in ("w", "leak", "bias", "drives",
                                                               "state0", "dout"))
     saved_b, scratch_b = g.workspace_size(B, T, M)
@@ -399,7 +402,7 @@ def run_ours(args, c, rank, world, dist):
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     hbm_peak, hbm_src = _peaks()
     q_hbm = hbm_bytes(N, E, B, T, M, n_in)
-    headline = c.get("config_id", 1) == 1 and M == 2
+    headline = c.get("config_id", 1) == 1 and M == 2 and not args.graph_in_host_memory
     props = torch.cuda.get_device_properties(dev)
     sm_mhz = (clk or {}).get("sm_max_mhz") or 2070.0
     fp32_peak = props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12  # 128 FP32 lanes per SM
@@ -411,7 +414,9 @@ def run_ours(args, c, rank, world, dist):
         "vs_baseline": value / PAGE_STEPS_PER_S if headline else None,
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": _workload_name(c), "parallelism": "replicas",
-                   "l2": "flushed by a 512 MB write before every timed step (outside the events)"},
+                   "l2": "flushed by a 512 MB write before every timed step (outside the events)",
+                   **({"graph": "edge-indexed arrays in pinned host memory"}
+                      if args.graph_in_host_memory else {})},
         "roofline": {"bound": "l2", "kernel": dom, "achieved": achieved, "peak": l2_read,
                      "unit": "GB/s", "frac": achieved / l2_read,
                      "traffic": ncu_traffic(dom) if headline else None,
@@ -454,6 +459,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--config", type=int, choices=range(5), default=1)
     ap.add_argument("--microsteps", type=int, default=None)
+    ap.add_argument("--graph-in-host-memory", action="store_true")
     args = ap.parse_args()
 
     import workloads

@@ -84,7 +84,7 @@ ck_status ck_graph_create(const int64_t *src, const int64_t *dst, int64_t E, int
                           const int64_t *input_nodes, int64_t n_in, void *stream,
                           ck_graph **out);
 
-/* Frees the handle and its device arrays (synchronises the device first).  NULL is a no-op. */
+/* Frees the handle and its arrays (synchronises the device first).  NULL is a no-op. */
 ck_status ck_graph_destroy(ck_graph *g);
 
 /* Sizes recorded in the handle (any output pointer may be NULL). */
@@ -275,8 +275,15 @@ typedef enum {
     CK_OPT_BARRIER_TIMEOUT_NS = 1,  /* bound on any device-side wait (default 4e9 ns) */
     CK_OPT_TEST_BARRIER_EXTRA = 2,  /* test hook: barriers wait for this many extra arrivals
                                        that never come, so every wait runs out (default 0) */
-    CK_OPT_GRAPH_IN_SMEM = 3        /* 1 (default): keep each CTA's slice of the graph in
+    CK_OPT_GRAPH_IN_SMEM = 3,       /* 1 (default): keep each CTA's slice of the graph in
                                        shared memory when it fits; 0: always stream it */
+    CK_OPT_GRAPH_IN_HOST_MEMORY = 4 /* read by ck_graph_create.  0 (default): every graph
+                                       array in device memory.  1: the arrays indexed by
+                                       edge (col, perm and each edge's row, both directions:
+                                       24 bytes per edge) go to pinned host memory that the
+                                       kernels read in place over the CPU-GPU link; the
+                                       row pointers, slots and piece tables (O(N)) stay on
+                                       the device.  Results are bitwise those of 0. */
 } ck_option;
 
 ck_status ck_set_option(ck_option opt, int64_t value);

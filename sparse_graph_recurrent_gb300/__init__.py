@@ -24,19 +24,28 @@ class SparseGraph:
     """A fixed directed graph src[e] -> dst[e] with designated input nodes.
 
     Built once on the GPU by ck_graph_create; edge parameters stay in the
-    caller's edge order.
+    caller's edge order.  With edges_in_host_memory the arrays indexed by edge
+    (24 bytes per edge) live in pinned host memory that the kernels read in
+    place over the CPU-GPU link, leaving O(N) of the graph on the device;
+    results are bitwise the same.
     """
 
-    def __init__(self, src, dst, num_nodes: int, input_nodes):
+    def __init__(self, src, dst, num_nodes: int, input_nodes, edges_in_host_memory: bool = False):
         if src.shape != dst.shape or src.dim() != 1:
             raise ValueError("src and dst must be 1-D and of equal length")
         self.device = src.device
         self.num_nodes = int(num_nodes)
         self.num_edges = int(src.numel())
         self.num_inputs = int(input_nodes.numel())
+        self.edges_in_host_memory = bool(edges_in_host_memory)
         with torch.cuda.device(self.device):
-            self._h = _ck.ck_graph_create(src.contiguous(), dst.contiguous(), self.num_nodes,
-                                          input_nodes.contiguous())
+            keep = _ck.ck_get_option(_ck.OPT_GRAPH_IN_HOST_MEMORY)
+            _ck.ck_set_option(_ck.OPT_GRAPH_IN_HOST_MEMORY, int(self.edges_in_host_memory))
+            try:
+                self._h = _ck.ck_graph_create(src.contiguous(), dst.contiguous(), self.num_nodes,
+                                              input_nodes.contiguous())
+            finally:
+                _ck.ck_set_option(_ck.OPT_GRAPH_IN_HOST_MEMORY, keep)
         self._ws = {}
 
     def __del__(self):

@@ -84,6 +84,7 @@ ck_status ck_set_option(ck_option opt, int64_t v) {
             o.barrier_extra = (int)v;
             return CK_OK;
         case CK_OPT_GRAPH_IN_SMEM: o.graph_in_smem = v != 0; return CK_OK;
+        case CK_OPT_GRAPH_IN_HOST_MEMORY: o.graph_in_host = v != 0; return CK_OK;
     }
     return fail(CK_ERR_INVALID_ARG, "unknown option %d", (int)opt);
 }
@@ -95,6 +96,7 @@ int64_t ck_get_option(ck_option opt) {
         case CK_OPT_BARRIER_TIMEOUT_NS: return o.timeout_ns;
         case CK_OPT_TEST_BARRIER_EXTRA: return o.barrier_extra;
         case CK_OPT_GRAPH_IN_SMEM: return o.graph_in_smem;
+        case CK_OPT_GRAPH_IN_HOST_MEMORY: return o.graph_in_host;
     }
     return -1;
 }
@@ -142,10 +144,12 @@ ck_status ck_graph_create(const int64_t *src, const int64_t *dst, int64_t E, int
 ck_status ck_graph_destroy(ck_graph *g) {
     if (!g) return CK_OK;
     cudaDeviceSynchronize();
-    int *ptrs[] = {g->row_ptr, g->col, g->perm, g->rowT_ptr, g->colT, g->permT,
-                   g->slot, g->rowid, g->rowidT};
-    for (int *p : ptrs)
+    int *dev_ptrs[] = {g->row_ptr, g->rowT_ptr, g->slot};
+    for (int *p : dev_ptrs)
         if (p) cudaFree(p);
+    int *edge_ptrs[] = {g->col, g->perm, g->colT, g->permT, g->rowid, g->rowidT};
+    for (int *p : edge_ptrs)
+        if (p) g->edges_in_host ? cudaFreeHost(p) : cudaFree(p);
     for (int d = 0; d < 2; ++d)
         for (int v = 0; v < 3; ++v)
             if (g->piece[d][v]) cudaFree(g->piece[d][v]);
@@ -177,7 +181,7 @@ ck_status ck_graph_export(const ck_graph *g, int32_t *row_ptr, int32_t *col, int
     for (auto &it : items) {
         if (!it.dst || it.n == 0) continue;
         cudaError_t e = cudaMemcpyAsync(it.dst, it.src, sizeof(int32_t) * it.n,
-                                        cudaMemcpyDeviceToDevice, s);
+                                        g->edges_in_host ? cudaMemcpyDefault : cudaMemcpyDeviceToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (export)");
     }
     return CK_OK;

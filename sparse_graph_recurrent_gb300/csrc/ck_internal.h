@@ -28,6 +28,9 @@ struct ck_graph {
     // must publish).
     int max_rows[2][3], max_edges[2][3], row_weight[2][3];
     int *piece[2][3];
+    // 1 when col, perm, rowid and their transposes live in pinned, mapped host
+    // memory (the pointers above are then the device's view of it).
+    int edges_in_host;
 };
 
 namespace ck {
@@ -106,6 +109,7 @@ struct Options {
     long long timeout_ns = 4000000000LL;
     int barrier_extra = 0;
     int graph_in_smem = 1;
+    int graph_in_host = 0;
 };
 Options &options();
 

@@ -443,6 +443,43 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
             }
         }
     }
+    // Edge-indexed arrays to pinned host memory, read in place by the kernels
+    // (on a Grace-Blackwell node over the coherent CPU-GPU link): the graph
+    // then holds O(N) device memory.  Every array is complete before the copy
+    // (the piece cut above synchronised the stream after the last kernel).
+    if (options().graph_in_host) {
+        CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (graph build)");
+        int **arrays[] = {&g->col, &g->perm, &g->colT, &g->permT, &g->rowid, &g->rowidT};
+        void *h[6] = {};
+        auto drop = [&]() {
+            for (void *p : h)
+                if (p) cudaFreeHost(p);
+        };
+        // all copies first, so that a failure leaves the device arrays in place
+        for (int i = 0; i < 6; ++i) {
+            e = cudaHostAlloc(&h[i], sizeof(int) * E1, cudaHostAllocMapped | cudaHostAllocPortable);
+            if (e == cudaSuccess) e = cudaMemcpy(h[i], *arrays[i], sizeof(int) * E1, cudaMemcpyDeviceToHost);
+            void *dv = nullptr;
+            if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dv, h[i], 0);
+            if (e != cudaSuccess) {
+                drop();
+                return (e == cudaErrorMemoryAllocation)
+                           ? fail(CK_ERR_OUT_OF_MEMORY, "graph in host memory: %s", cudaGetErrorString(e))
+                           : cuda_fail(e, "graph in host memory");
+            }
+            if (dv != h[i]) {
+                // the kernels take the pointer as is and the handle frees it
+                // with cudaFreeHost: both need the unified address space
+                drop();
+                return fail(CK_ERR_UNSUPPORTED, "host memory is not mapped at the same address on the device");
+            }
+        }
+        for (int i = 0; i < 6; ++i) {
+            cudaFree(*arrays[i]);
+            *arrays[i] = (int *)h[i];
+        }
+        g->edges_in_host = 1;
+    }
 #undef CK_TRY
     return CK_OK;
 }
