@@ -170,15 +170,17 @@ ck_status ck_backward(const ck_graph *g, const float *edge_values, const float *
 /*
  * Recomputing variant: the forward keeps only the state after every input
  * step (T + 1 checkpoints instead of 2 T M + 1 saved rows), and the backward
- * recomputes each input step's microsteps from its checkpoint before
+ * recomputes the microsteps of a window of K input steps (CK_OPT_RECOMPUTE_STEPS,
+ * about sqrt(T) by default) from the window's first checkpoint before
  * differentiating them.  The pages save every microstep's state and
  * pre-activation ("Design notes": 2 x T x M x N x B floats); this trades one
- * more forward pass (and two launches per input step) for about M times less
- * saved memory.  Results equal ck_forward / ck_backward's bit for bit.
+ * more forward pass (and two launches per window) for T + 1 + 2 K M + 1 rows
+ * instead of 2 T M + 1.  Results equal ck_forward / ck_backward's bit for bit,
+ * for every K.
  *
  * ck_workspace_size_recompute -- bytes of the checkpoints and of the scratch
- *   buffer for the two calls below (the scratch holds one input step's window
- *   of M + 1 states and M proposals on top of ck_workspace_size's scratch).
+ *   buffer for the two calls below (the scratch holds a window of K M + 1
+ *   states and K M proposals on top of ck_workspace_size's scratch).
  *   Errors: as ck_workspace_size.
  */
 ck_status ck_workspace_size_recompute(const ck_graph *g, int64_t B, int64_t T,
@@ -201,9 +203,10 @@ ck_status ck_forward_checkpointed(const ck_graph *g, const float *edge_values,
                                   void *stream);
 
 /*
- * ck_backward_recompute -- ck_backward from checkpoints: for t = T-1 .. 0 it
- * recomputes microsteps tM .. tM+M-1 from ckpt[t] (one launch) and runs the
- * backward microsteps of step t (a second launch).  Needs bias and drives
+ * ck_backward_recompute -- ck_backward from checkpoints: for windows [t, t1)
+ * of K input steps from the top (the lowest may be shorter) it recomputes
+ * microsteps tM .. t1 M - 1 from ckpt[t] (one launch) and runs the backward
+ * microsteps of steps t .. t1 - 1 (a second launch).  Needs bias and drives
  * besides ck_backward's inputs, since it reruns the forward.
  *   ckpt   (device) as filled by ck_forward_checkpointed with the same g, B, T,
  *          microsteps and inputs
@@ -277,13 +280,17 @@ typedef enum {
                                        that never come, so every wait runs out (default 0) */
     CK_OPT_GRAPH_IN_SMEM = 3,       /* 1 (default): keep each CTA's slice of the graph in
                                        shared memory when it fits; 0: always stream it */
-    CK_OPT_GRAPH_IN_HOST_MEMORY = 4 /* read by ck_graph_create.  0 (default): every graph
+    CK_OPT_GRAPH_IN_HOST_MEMORY = 4,/* read by ck_graph_create.  0 (default): every graph
                                        array in device memory.  1: the arrays indexed by
                                        edge (col, perm and each edge's row, both directions:
                                        24 bytes per edge) go to pinned host memory that the
                                        kernels read in place over the CPU-GPU link; the
                                        row pointers, slots and piece tables (O(N)) stay on
                                        the device.  Results are bitwise those of 0. */
+    CK_OPT_RECOMPUTE_STEPS = 5      /* input steps K one recomputation window spans
+                                       (ck_workspace_size_recompute and the two calls
+                                       after it must see the same value); 0 (default):
+                                       round(sqrt(T)); clamped to [1, T] */
 } ck_option;
 
 ck_status ck_set_option(ck_option opt, int64_t value);

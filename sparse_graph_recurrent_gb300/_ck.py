@@ -18,7 +18,8 @@ CK_OK = 0
 STATUS = {0: "CK_OK", 1: "CK_ERR_INVALID_ARG", 2: "CK_ERR_CUDA", 3: "CK_ERR_OUT_OF_MEMORY",
           4: "CK_ERR_TIMEOUT", 5: "CK_ERR_WORKSPACE", 6: "CK_ERR_INTERNAL",
           7: "CK_ERR_UNSUPPORTED"}
-OPT_PERSISTENT, OPT_BARRIER_TIMEOUT_NS, OPT_TEST_BARRIER_EXTRA, OPT_GRAPH_IN_SMEM, OPT_GRAPH_IN_HOST_MEMORY = range(5)
+(OPT_PERSISTENT, OPT_BARRIER_TIMEOUT_NS, OPT_TEST_BARRIER_EXTRA, OPT_GRAPH_IN_SMEM,
+ OPT_GRAPH_IN_HOST_MEMORY, OPT_RECOMPUTE_STEPS) = range(6)
 
 _lib = None
 

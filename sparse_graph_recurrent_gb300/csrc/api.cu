@@ -85,6 +85,10 @@ ck_status ck_set_option(ck_option opt, int64_t v) {
             return CK_OK;
         case CK_OPT_GRAPH_IN_SMEM: o.graph_in_smem = v != 0; return CK_OK;
         case CK_OPT_GRAPH_IN_HOST_MEMORY: o.graph_in_host = v != 0; return CK_OK;
+        case CK_OPT_RECOMPUTE_STEPS:
+            if (v < 0 || v > (1 << 30)) return fail(CK_ERR_INVALID_ARG, "recompute steps must be in [0, 2^30]");
+            o.recompute_steps = (int)v;
+            return CK_OK;
     }
     return fail(CK_ERR_INVALID_ARG, "unknown option %d", (int)opt);
 }
@@ -97,6 +101,7 @@ int64_t ck_get_option(ck_option opt) {
         case CK_OPT_TEST_BARRIER_EXTRA: return o.barrier_extra;
         case CK_OPT_GRAPH_IN_SMEM: return o.graph_in_smem;
         case CK_OPT_GRAPH_IN_HOST_MEMORY: return o.graph_in_host;
+        case CK_OPT_RECOMPUTE_STEPS: return o.recompute_steps;
     }
     return -1;
 }

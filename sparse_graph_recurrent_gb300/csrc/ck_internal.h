@@ -98,8 +98,9 @@ struct Plan {
     size_t scratch_bytes;
     size_t saved_bytes; // float [(S+1) + S][N][Bp]
     // checkpointing forward / recomputing backward
-    size_t off_hwin;          // float [M+1][N][Bp] window of states (first two: the forward's slots)
-    size_t off_pwin;          // float [M][N][Bp] window of proposals
+    int rc_steps;             // input steps one recomputation window spans (K)
+    size_t off_hwin;          // float [KM+1][N][Bp] window of states (first two: the forward's slots)
+    size_t off_pwin;          // float [KM][N][Bp] window of proposals
     size_t scratch_bytes_rc;  // scratch for those calls (regular scratch plus the windows)
     size_t ckpt_bytes;        // float [T+1][N][Bp] states after every input step
 };
@@ -110,6 +111,7 @@ struct Options {
     int barrier_extra = 0;
     int graph_in_smem = 1;
     int graph_in_host = 0;
+    int recompute_steps = 0;  // 0: about sqrt(T)
 };
 Options &options();
 

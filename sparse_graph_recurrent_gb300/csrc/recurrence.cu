@@ -53,6 +53,7 @@
 // once per call; otherwise it streams from global memory every microstep, each
 // batch's {col, w} read one batch ahead of its gathers.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <type_traits>
 
@@ -1607,13 +1608,20 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     q.off_lacc = off;
     off = align256(off + 8 * 32 * (size_t)q.N);
     q.scratch_bytes = off;
-    // recomputation windows (after the regular scratch): M + 1 states and M
-    // proposals of one input step; the checkpointing forward's two state
-    // slots use the first two
+    // recomputation windows (after the regular scratch): KM + 1 states and KM
+    // proposals of K input steps; the checkpointing forward's two state slots
+    // use the first two.  K defaults to about sqrt(T), which balances the
+    // windows against the checkpoints and makes 2 ceil(T / K) launches
+    {
+        const int want = options().recompute_steps;
+        int K = want > 0 ? want : (int)std::lround(std::sqrt((double)q.T));
+        q.rc_steps = std::max(1, std::min(K, q.T));
+    }
+    const size_t KM = (size_t)q.rc_steps * q.M;
     q.off_hwin = off;
-    off = align256(off + 4 * NBp * (size_t)(q.M + 1));
+    off = align256(off + 4 * NBp * (KM + 1));
     q.off_pwin = off;
-    off = align256(off + 4 * NBp * (size_t)q.M);
+    off = align256(off + 4 * NBp * KM);
     q.scratch_bytes_rc = off;
     q.ckpt_bytes = 4 * NBp * (size_t)(q.T + 1);
     q.saved_bytes = 4 * NBp * (size_t)(2 * q.S + 1);
@@ -1668,11 +1676,13 @@ ck_status launch_backward_recompute(const ck_graph *g, const Plan &p, const RcIO
     const size_t NBp = (size_t)p.N * p.Bp;
     float *hwin = (float *)((char *)io.scratch + p.off_hwin);
     float *pwin = (float *)((char *)io.scratch + p.off_pwin);
-    const int M = p.M, T = p.T, S = p.S;
+    const int M = p.M, T = p.T, S = p.S, K = p.rc_steps;
     int64_t n = 0;
-    for (int t = T - 1; t >= 0; --t) {
-        // microsteps tM .. tM + M - 1 again, from the checkpoint of step t:
-        // states into window slots 0..M, proposals into slots 0..M-1
+    // windows [t, t1) of K input steps from the top (the lowest may be shorter)
+    for (int t1 = T; t1 > 0; t1 -= K) {
+        const int t = t1 > K ? t1 - K : 0, k = t1 - t;
+        // microsteps tM .. t1 M - 1 again, from the checkpoint of step t:
+        // states into window slots 0..kM, proposals into slots 0..kM-1
         cudaError_t e = cudaMemcpyAsync(hwin, io.ckpt + (size_t)t * NBp, 4 * NBp,
                                         cudaMemcpyDeviceToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (checkpoint)");
@@ -1692,15 +1702,15 @@ ck_status launch_backward_recompute(const ck_graph *g, const Plan &p, const RcIO
         kf.Pr = pwin;
         kf.p_off = t * M;
         kf.s_first = t * M;
-        kf.s_count = M;
+        kf.s_count = k * M;
         kf.do_prologue = 0;
         kf.do_epilogue = 0;
         kf.init_w = 1;  // the backward windows overwrite the shared permuted values
         ck_status st = launch_once(kf, p, p.lay_fwd, false, s);
         if (st != CK_OK) return st;
         ++n;
-        // the backward iterations whose elementwise terms belong to step t:
-        // s = (t + 1) M .. tM + 1 (the first is the prologue for the last
+        // the backward iterations whose elementwise terms belong to steps t ..
+        // t1 - 1: s = t1 M .. tM + 1 (the first is the prologue for the last
         // step), and s = 0 after step 0
         KArgs kb;
         fill_common(kb, g, p, io.scratch, 1, &p.lay_bwd_flat);
@@ -1721,10 +1731,10 @@ ck_status launch_backward_recompute(const ck_graph *g, const Plan &p, const RcIO
         kb.dbias = io.dbias;
         kb.ddrives = io.ddrives;
         kb.dstate0 = io.dstate0;
-        const bool last_step = t == T - 1;
+        const bool last_step = t1 == T;
         kb.do_prologue = last_step ? 1 : 0;
-        kb.s_first = last_step ? S - 1 : (t + 1) * M;
-        kb.s_count = (last_step ? M - 1 : M) + (t == 0 ? 1 : 0);
+        kb.s_first = last_step ? S - 1 : t1 * M;
+        kb.s_count = (last_step ? k * M - 1 : k * M) + (t == 0 ? 1 : 0);
         kb.do_epilogue = t == 0 ? 1 : 0;
         kb.init_w = 1;
         kb.zero_dw = last_step ? 1 : 0;

@@ -60,6 +60,37 @@ def test_recompute_flygpt_bitwise_identical():
     _check_identical(workloads.make(1))
 
 
+@pytest.fixture
+def _recompute_steps():
+    from sparse_graph_recurrent_gb300 import _ck
+    yield lambda k: _ck.ck_set_option(_ck.OPT_RECOMPUTE_STEPS, k)
+    _ck.ck_set_option(_ck.OPT_RECOMPUTE_STEPS, 0)
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 5, 7, 9])
+@pytest.mark.parametrize("M", [1, 3])
+def test_windows_of_several_steps_are_bitwise_identical(_recompute_steps, K, M):
+    """Windows of K input steps, including a shorter lowest window (T = 7)
+    and K beyond T (clamped to one window)."""
+    _recompute_steps(K)
+    _check_identical(workloads.small(409 + M, 200, 8000, 10, 20, 7, M, hub_deg=3000))
+
+
+def test_window_size_sets_the_scratch(_recompute_steps):
+    from sparse_graph_recurrent_gb300 import _ck
+    c = workloads.small(412, 300, 5000, 6, 32, 16, 2)
+    g = make_graph(c)
+    N, Bp = c["N"], 32
+    sizes = {}
+    for K in (1, 4, 16, 0):
+        _recompute_steps(K)
+        sizes[K] = _ck.ck_workspace_size_recompute(g.handle, 32, 16, 2)[1]
+    assert sizes[0] == sizes[4]  # round(sqrt(16))
+    # each extra input step in the window holds M more states and M more proposals
+    assert sizes[16] - sizes[4] == 12 * 2 * 2 * N * Bp * 4
+    assert sizes[4] - sizes[1] == 3 * 2 * 2 * N * Bp * 4
+
+
 def test_recompute_autograd_matches_oracle():
     import sparse_graph_recurrent_gb300 as pkg
     c = workloads.small(407, 150, 6000, 7, 24, 3, 2, hub_deg=2000)
