@@ -252,7 +252,7 @@ ck_status ck_sgd_update(float *param, const float *grad, int64_t n, float lr, vo
  *     Each call clears the words that must start at zero; the rest of the
  *     array keeps the previous call's contents until overwritten.
  *   - Shapes whose forward workspace exceeds the array (control words, one
- *     carry row per SM, one float per edge and per padded node-batch element)
+ *     carry row per CTA, one float per edge and per padded node-batch element)
  *     are refused with CK_ERR_UNSUPPORTED and a message giving both sizes.
  *   - Device-side wait timeouts are not reported by this call (ck_query_status
  *     needs a caller-owned scratch buffer).

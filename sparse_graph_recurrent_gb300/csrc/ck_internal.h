@@ -78,7 +78,7 @@ struct SmemLayout {
 struct Plan {
     int N, E, n_in;
     int B, Bp, LPE, EPW, NC, T, M, S;
-    int P;            // CTAs (one per SM)
+    int P;            // CTAs (kCtasPerSm per SM), one piece each
     int threads;      // threads per CTA
     int warps;        // warps per CTA
     int groups;       // lane groups per CTA (warps * EPW)

@@ -407,7 +407,7 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
         CK_TRY(cudaGetLastError(), "row_ptr launch");
         // the second side reuses kb/vb; stream order already serialises it
     }
-    // Pieces, one per SM, for each finish pass size.  The row weight is the
+    // Pieces, one per CTA (kCtasPerSm per SM), for each finish pass size.  The row weight is the
     // one (of a few) whose slowest piece is estimated fastest: part A at about
     // 1.5 ns per edge per 32 batch columns, a finish pass at about 0.8 us
     // (measured on the FlyGPT-shaped graph); ties go to the smaller weight.

@@ -53,6 +53,21 @@ def test_options_validate(lib):
         _ck.ck_set_option(17, 1)
     assert e.value.name == "CK_ERR_INVALID_ARG"
     assert _ck.ck_get_option(_ck.OPT_BARRIER_TIMEOUT_NS) == 4_000_000_000
+    # graph residency and recompute window: defaults, round trip, range
+    assert _ck.ck_get_option(_ck.OPT_GRAPH_IN_HOST_MEMORY) == 0
+    assert _ck.ck_get_option(_ck.OPT_RECOMPUTE_STEPS) == 0
+    try:
+        _ck.ck_set_option(_ck.OPT_GRAPH_IN_HOST_MEMORY, 1)
+        assert _ck.ck_get_option(_ck.OPT_GRAPH_IN_HOST_MEMORY) == 1
+        _ck.ck_set_option(_ck.OPT_RECOMPUTE_STEPS, 5)
+        assert _ck.ck_get_option(_ck.OPT_RECOMPUTE_STEPS) == 5
+        with pytest.raises(_ck.CKError) as e:
+            _ck.ck_set_option(_ck.OPT_RECOMPUTE_STEPS, -1)
+        assert e.value.name == "CK_ERR_INVALID_ARG"
+        assert _ck.ck_get_option(_ck.OPT_RECOMPUTE_STEPS) == 5
+    finally:
+        _ck.ck_set_option(_ck.OPT_GRAPH_IN_HOST_MEMORY, 0)
+        _ck.ck_set_option(_ck.OPT_RECOMPUTE_STEPS, 0)
 
 
 def test_graph_create_rejects_bad_sizes_before_cuda(lib):
