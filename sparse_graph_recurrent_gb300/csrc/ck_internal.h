@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -105,13 +107,15 @@ struct Plan {
     size_t ckpt_bytes;        // float [T+1][N][Bp] states after every input step
 };
 
+// Process-wide switches (ck_set_option).  Atomic, so that a thread setting one
+// while another plans a call reads either value, never a torn one.
 struct Options {
-    int persistent = 1;
-    long long timeout_ns = 4000000000LL;
-    int barrier_extra = 0;
-    int graph_in_smem = 1;
-    int graph_in_host = 0;
-    int recompute_steps = 0;  // 0: about sqrt(T)
+    std::atomic<int> persistent{1};
+    std::atomic<long long> timeout_ns{4000000000LL};
+    std::atomic<int> barrier_extra{0};
+    std::atomic<int> graph_in_smem{1};
+    std::atomic<int> graph_in_host{0};
+    std::atomic<int> recompute_steps{0};  // 0: about sqrt(T)
 };
 Options &options();
 
