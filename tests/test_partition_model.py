@@ -92,8 +92,12 @@ def test_flygpt_pieces_and_carries():
         rp = np.zeros(N + 1, np.int64)
         np.add.at(rp, np.asarray(c[key]) + 1, 1)
         rp = np.cumsum(rp)
-        for w in (1, 3):
-            _check(rp, N, int(rp[-1]), 152, 128, 8, w, rng)
+        # two CTAs of 8 warps per SM (304 pieces, 64 groups of 4 lanes each)
+        # and one CTA of 16 warps (152 pieces, 128 groups); the row weights
+        # the cost model picks for this graph (16 forward, 1 backward) and 3
+        for P, G in ((304, 64), (152, 128)):
+            for w in (1, 3, 16):
+                _check(rp, N, int(rp[-1]), P, G, 8, w, rng)
 
 
 def test_random_graphs_pieces_and_carries():
