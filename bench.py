@@ -127,23 +127,44 @@ def flops_per_step(N, E, B, T, M):
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons, kept for the
+    samples taken inside the timed region (begin() .. end())."""
 
-    def __init__(self, index):
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index, interval_ms=50):
         self.path = tempfile.mktemp(suffix=".csv")
         self.proc = None
         self.index = index
+        self.interval_ms = interval_ms
+        self.t_begin = self.t_end = None
 
     def start(self):
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        """Start the sampler and wait (up to 5 s) for its first line, so that
+        the timed region that follows is covered from its start."""
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        deadline = time.time() + 5.0
+        while time.time() < deadline and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
+
+    def begin(self):
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
+        if self.proc is not None:
+            time.sleep(2 * self.interval_ms / 1e3)  # the sample in flight at the end
 
     def stop(self):
         if self.proc is None:
@@ -153,22 +174,39 @@ class Clocks:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+        with open(self.path) as f:
+            lines = f.read().splitlines()
+        os.unlink(self.path)
+        return self.summarize(lines, self.t_begin, self.t_end)
+
+    @classmethod
+    def summarize(cls, lines, t_begin, t_end):
+        """Median SM clock, maximum clock and the throttle reasons seen, over
+        the samples whose timestamp lies in [t_begin, t_end] (epoch seconds);
+        if none does (a region shorter than the interval), the sample nearest
+        to the region stands in and "samples" says 0."""
+        import datetime
         rows = []
-        for line in open(self.path):
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
-        os.unlink(self.path)
         if not rows:
             return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[2]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        inside = [r for r in rows if t_begin is not None and t_end is not None and t_begin <= r[0] <= t_end]
+        use = inside
+        if not use:
+            mid = ((t_begin or 0.0) + (t_end or 0.0)) / 2
+            use = [min(rows, key=lambda r: abs(r[0] - mid))]
+        reasons = sorted({n for r in use for n, v in zip(cls.REASONS, r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(inside), "interval_ms": None if not rows else
+                round(1e3 * (rows[-1][0] - rows[0][0]) / max(len(rows) - 1, 1), 1)}
 
 
 def cpu_oracle_sample(c, cols):
@@ -331,6 +369,7 @@ def run_ours(args, c, rank, world, dist):
     launches[0] = 0
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks.begin()
     for k in range(args.steps):
         flush.fill_(k & 0xff)
         ev[k][0].record(stream)
@@ -341,6 +380,7 @@ def run_ours(args, c, rank, world, dist):
         launches[0] += _ck.ck_last_launch_count()
         ev[k][2].record(stream)
     torch.cuda.synchronize()
+    clocks.end()
     if dist:
         dist.barrier()
     clk = clocks.stop()
@@ -452,7 +492,7 @@ def run_ours(args, c, rank, world, dist):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference", "torch-sparse"], default="ours")
     ap.add_argument("--cpu-cols", type=int, default=2)

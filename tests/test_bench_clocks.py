@@ -1,0 +1,45 @@
+"""bench.py's clock record: only the nvidia-smi samples taken inside the timed
+region count (host logic, no GPU)."""
+import datetime
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import bench  # noqa: E402
+
+
+def _line(t, sm, mx=2070, reasons=("Not Active",) * 4):
+    ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return ", ".join([ts, "0", str(sm), str(mx), "900.00", "0x0000000000000000", *reasons])
+
+
+def test_samples_inside_the_region_only():
+    t0 = 1_800_000_000.0
+    lines = [_line(t0 - 0.10, 1000), _line(t0 + 0.05, 2070), _line(t0 + 0.10, 2040),
+             _line(t0 + 0.15, 2070), _line(t0 + 0.40, 900, reasons=("Active",) + ("Not Active",) * 3)]
+    r = bench.Clocks.summarize(lines, t0, t0 + 0.2)
+    assert r["samples"] == 3
+    assert r["sm_mhz"] == 2070.0 and r["sm_max_mhz"] == 2070.0
+    assert r["reasons"] == []  # the hw_slowdown sample lies after the region
+
+
+def test_reasons_inside_the_region_are_reported():
+    t0 = 1_800_000_000.0
+    lines = [_line(t0 + 0.05, 1980, reasons=("Not Active", "Not Active", "Not Active", "Active")),
+             _line(t0 + 0.10, 1900, reasons=("Not Active", "Active", "Not Active", "Not Active"))]
+    r = bench.Clocks.summarize(lines, t0, t0 + 0.2)
+    assert r["samples"] == 2
+    assert r["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+
+
+def test_short_region_falls_back_to_the_nearest_sample():
+    t0 = 1_800_000_000.0
+    lines = [_line(t0 - 1.0, 1500), _line(t0 + 0.06, 2055), _line(t0 + 1.0, 1400)]
+    r = bench.Clocks.summarize(lines, t0, t0 + 0.01)
+    assert r["samples"] == 0 and r["sm_mhz"] == 2055.0
+
+
+def test_unparsable_output_gives_no_record():
+    assert bench.Clocks.summarize(["No devices were found"], 0.0, 1.0) is None
+    assert bench.Clocks.summarize([], 0.0, 1.0) is None
