@@ -53,17 +53,28 @@ def _peaks():
         return HBM_FALLBACK, "fallback"
 
 
+def source_digest(path):
+    """First 16 hex digits of the sha256 of a C/C++ source's code: comments
+    removed and runs of whitespace collapsed, so that an edit to comments keeps
+    a profile capture valid and any edit to the code voids it."""
+    import hashlib
+    import re
+    text = open(path, encoding="utf-8").read()
+    tokens = re.compile(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|//[^\n]*|/\*.*?\*/', re.S)
+    code = tokens.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", text)
+    return hashlib.sha256(" ".join(code.split()).encode()).hexdigest()[:16]
+
+
 def ncu_traffic(kernel):
     """DRAM bytes per launch of `kernel` ("forward"/"backward") from the committed ncu
-    summary, or None when the kernel source has changed since that capture."""
-    import hashlib
+    summary, or None when the kernel source's code has changed since that capture."""
     try:
         src = os.path.join(ROOT, "sparse_graph_recurrent_gb300", "csrc", "recurrence.cu")
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        digest = source_digest(src)
         for line in open(os.path.join(ROOT, "profiles", "rec_kernel_flygpt.md")):
             if line.startswith("traffic_bytes_per_launch:"):
                 kv = dict(x.split("=") for x in line.split(":", 1)[1].split())
-                if kv.get("source_sha256_16") == sha:
+                if kv.get("source_code_sha256_16") == digest:
                     return int(kv[kernel])
     except Exception:
         pass

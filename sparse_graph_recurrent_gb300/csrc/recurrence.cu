@@ -21,7 +21,7 @@
 //   G[N][Bp]       running state gradient (backward)
 //   da[2][N][Bp]   d(loss)/d(pre-activation), ping-pong between microsteps
 // H[s] and Pr[s] are addressed through hrow / prow, which map s to a slot:
-// the saved arrays by default, a window of one input step when the backward
+// the saved arrays by default, a window of K input steps when the backward
 // recomputes, a two-slot ping-pong when the forward keeps only checkpoints.
 // The caller's [T][B][N] outputs and output gradients are read and written one
 // input step at a time, transposed through shared memory when staging is on.
@@ -1581,8 +1581,8 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     const bool want_stage = options().persistent != 0;
     q.lay_fwd = smem_layout(q, 0, want_graph, want_stage);
     q.lay_bwd = smem_layout(q, 1, want_graph, want_stage);
-    // the recomputing backward runs in windows of one input step, every
-    // accumulator in global memory
+    // the recomputing backward runs in windows of K input steps (one launch
+    // each), every accumulator in global memory
     q.lay_bwd_flat = smem_layout(q, 1, false, false);
     const size_t cta_smem = std::min<size_t>(kMaxSmem, kSmemPerSm / kCtasPerSm - 1024) - kStaticSmem;
     if (q.lay_fwd.bytes > cta_smem || q.lay_bwd.bytes > cta_smem || q.lay_bwd_flat.bytes > cta_smem)

@@ -43,3 +43,16 @@ def test_short_region_falls_back_to_the_nearest_sample():
 def test_unparsable_output_gives_no_record():
     assert bench.Clocks.summarize(["No devices were found"], 0.0, 1.0) is None
     assert bench.Clocks.summarize([], 0.0, 1.0) is None
+
+
+def test_source_digest_ignores_comments_not_code(tmp_path):
+    base = 'int f(int x) {  // the CTA\'s "row"\n    /* block\n comment */ return x + 1;\n}\nconst char *s = "a // b";\n'
+    p = tmp_path / "k.cu"
+    p.write_text(base)
+    d0 = bench.source_digest(str(p))
+    p.write_text(base.replace("the CTA's", "every CTA's").replace("block\n", "other\n\n"))
+    assert bench.source_digest(str(p)) == d0  # comments and blank lines only
+    p.write_text(base.replace("x + 1", "x + 2"))
+    assert bench.source_digest(str(p)) != d0  # code
+    p.write_text(base.replace('"a // b"', '"a // c"'))
+    assert bench.source_digest(str(p)) != d0  # "//" inside a string is code
