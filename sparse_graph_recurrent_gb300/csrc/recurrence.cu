@@ -51,7 +51,9 @@
 //      fixed order: results do not depend on timing.
 // When a CTA's slice of the graph fits in shared memory it is loaded there
 // once per call; otherwise it streams from global memory every microstep, each
-// batch's {col, w} read one batch ahead of its gathers.
+// batch's {col, w} read one batch ahead of its gathers.  The graph's arrays
+// indexed by edge may be device memory or pinned host memory (chosen when the
+// graph is built); the kernels read both the same way.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
