@@ -84,6 +84,31 @@ ck_status ck_graph_create(const int64_t *src, const int64_t *dst, int64_t E, int
                           const int64_t *input_nodes, int64_t n_in, void *stream,
                           ck_graph **out);
 
+/* Graph residency flags for ck_graph_create_flags. */
+typedef enum {
+    CK_GRAPH_EDGES_IN_HOST_MEMORY = 1  /* the arrays indexed by edge (col, perm and each edge's
+                                          row, both directions: 24 bytes per edge) go to pinned
+                                          host memory that the kernels read in place over the
+                                          CPU-GPU link (NVLink-C2C on a Grace-Blackwell node);
+                                          row pointers, slots and piece tables (O(N)) stay in
+                                          device memory.  Results are bitwise those of a
+                                          device-resident graph; speed depends on whether the
+                                          CTAs' slices fit in shared memory (read once per call)
+                                          or stream every microstep.  The connectome runtime
+                                          page ("Why this runtime") makes graph residency an
+                                          explicit choice in the same way. */
+} ck_graph_flag;
+
+/*
+ * ck_graph_create_flags -- ck_graph_create with residency flags (a bitwise OR
+ * of ck_graph_flag values; 0 is ck_graph_create).  Errors: as ck_graph_create,
+ * plus CK_ERR_INVALID_ARG for an unknown flag bit and CK_ERR_UNSUPPORTED when
+ * pinned host memory is not mapped at the same address on the device.
+ */
+ck_status ck_graph_create_flags(const int64_t *src, const int64_t *dst, int64_t E, int64_t N,
+                                const int64_t *input_nodes, int64_t n_in, uint32_t flags,
+                                void *stream, ck_graph **out);
+
 /* Frees the handle and its arrays (synchronises the device first).  NULL is a no-op. */
 ck_status ck_graph_destroy(ck_graph *g);
 
@@ -280,14 +305,7 @@ typedef enum {
                                        that never come, so every wait runs out (default 0) */
     CK_OPT_GRAPH_IN_SMEM = 3,       /* 1 (default): keep each CTA's slice of the graph in
                                        shared memory when it fits; 0: always stream it */
-    CK_OPT_GRAPH_IN_HOST_MEMORY = 4,/* read by ck_graph_create.  0 (default): every graph
-                                       array in device memory.  1: the arrays indexed by
-                                       edge (col, perm and each edge's row, both directions:
-                                       24 bytes per edge) go to pinned host memory that the
-                                       kernels read in place over the CPU-GPU link; the
-                                       row pointers, slots and piece tables (O(N)) stay on
-                                       the device.  Results are bitwise those of 0. */
-    CK_OPT_RECOMPUTE_STEPS = 5      /* input steps K one recomputation window spans
+    CK_OPT_RECOMPUTE_STEPS = 4      /* input steps K one recomputation window spans
                                        (ck_workspace_size_recompute and the two calls
                                        after it must see the same value); 0 (default):
                                        round(sqrt(T)); clamped to [1, T] */

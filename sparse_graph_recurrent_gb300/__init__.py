@@ -38,14 +38,10 @@ class SparseGraph:
         self.num_edges = int(src.numel())
         self.num_inputs = int(input_nodes.numel())
         self.edges_in_host_memory = bool(edges_in_host_memory)
+        flags = _ck.GRAPH_EDGES_IN_HOST_MEMORY if self.edges_in_host_memory else 0
         with torch.cuda.device(self.device):
-            keep = _ck.ck_get_option(_ck.OPT_GRAPH_IN_HOST_MEMORY)
-            _ck.ck_set_option(_ck.OPT_GRAPH_IN_HOST_MEMORY, int(self.edges_in_host_memory))
-            try:
-                self._h = _ck.ck_graph_create(src.contiguous(), dst.contiguous(), self.num_nodes,
-                                              input_nodes.contiguous())
-            finally:
-                _ck.ck_set_option(_ck.OPT_GRAPH_IN_HOST_MEMORY, keep)
+            self._h = _ck.ck_graph_create(src.contiguous(), dst.contiguous(), self.num_nodes,
+                                          input_nodes.contiguous(), flags=flags)
         self._ws = {}
 
     def __del__(self):

@@ -19,7 +19,8 @@ STATUS = {0: "CK_OK", 1: "CK_ERR_INVALID_ARG", 2: "CK_ERR_CUDA", 3: "CK_ERR_OUT_
           4: "CK_ERR_TIMEOUT", 5: "CK_ERR_WORKSPACE", 6: "CK_ERR_INTERNAL",
           7: "CK_ERR_UNSUPPORTED"}
 (OPT_PERSISTENT, OPT_BARRIER_TIMEOUT_NS, OPT_TEST_BARRIER_EXTRA, OPT_GRAPH_IN_SMEM,
- OPT_GRAPH_IN_HOST_MEMORY, OPT_RECOMPUTE_STEPS) = range(6)
+ OPT_RECOMPUTE_STEPS) = range(5)
+GRAPH_EDGES_IN_HOST_MEMORY = 1  # ck_graph_flag
 
 _lib = None
 
@@ -49,6 +50,7 @@ def load() -> ctypes.CDLL:
     pi64 = ctypes.POINTER(ctypes.c_int64)
     sig = {
         "ck_graph_create": [p, p, i64, i64, p, i64, p, ctypes.POINTER(p)],
+        "ck_graph_create_flags": [p, p, i64, i64, p, i64, ctypes.c_uint32, p, ctypes.POINTER(p)],
         "ck_graph_destroy": [p],
         "ck_graph_info": [p, pi64, pi64, pi64],
         "ck_graph_export": [p, p, p, p, p, p, p, p, p],
@@ -119,14 +121,17 @@ def _shapes(handle, B: int, T: int, **tensors):
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {want[name]}")
 
 
-def ck_graph_create(src, dst, num_nodes: int, input_nodes, stream=None):
+def ck_graph_create(src, dst, num_nodes: int, input_nodes, stream=None, flags: int = 0):
+    """ck_graph_create, or ck_graph_create_flags when flags is non-zero."""
     for t, n in ((src, "src"), (dst, "dst"), (input_nodes, "input_nodes")):
         _need(t, torch.int64, n)
     h = ctypes.c_void_p()
     n_in = 0 if input_nodes is None else input_nodes.numel()
-    _check(load().ck_graph_create(_ptr(src), _ptr(dst), src.numel(), num_nodes,
-                                  _ptr(input_nodes) if n_in else None, n_in, _stream(stream),
-                                  ctypes.byref(h)))
+    args = (_ptr(src), _ptr(dst), src.numel(), num_nodes, _ptr(input_nodes) if n_in else None, n_in)
+    if flags:
+        _check(load().ck_graph_create_flags(*args, int(flags), _stream(stream), ctypes.byref(h)))
+    else:
+        _check(load().ck_graph_create(*args, _stream(stream), ctypes.byref(h)))
     return h
 
 

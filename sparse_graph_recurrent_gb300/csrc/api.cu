@@ -84,7 +84,6 @@ ck_status ck_set_option(ck_option opt, int64_t v) {
             o.barrier_extra = (int)v;
             return CK_OK;
         case CK_OPT_GRAPH_IN_SMEM: o.graph_in_smem = v != 0; return CK_OK;
-        case CK_OPT_GRAPH_IN_HOST_MEMORY: o.graph_in_host = v != 0; return CK_OK;
         case CK_OPT_RECOMPUTE_STEPS:
             if (v < 0 || v > (1 << 30)) return fail(CK_ERR_INVALID_ARG, "recompute steps must be in [0, 2^30]");
             o.recompute_steps = (int)v;
@@ -100,7 +99,6 @@ int64_t ck_get_option(ck_option opt) {
         case CK_OPT_BARRIER_TIMEOUT_NS: return o.timeout_ns;
         case CK_OPT_TEST_BARRIER_EXTRA: return o.barrier_extra;
         case CK_OPT_GRAPH_IN_SMEM: return o.graph_in_smem;
-        case CK_OPT_GRAPH_IN_HOST_MEMORY: return o.graph_in_host;
         case CK_OPT_RECOMPUTE_STEPS: return o.recompute_steps;
     }
     return -1;
@@ -109,8 +107,16 @@ int64_t ck_get_option(ck_option opt) {
 ck_status ck_graph_create(const int64_t *src, const int64_t *dst, int64_t E, int64_t N,
                           const int64_t *input_nodes, int64_t n_in, void *stream,
                           ck_graph **out) {
+    return ck_graph_create_flags(src, dst, E, N, input_nodes, n_in, 0u, stream, out);
+}
+
+ck_status ck_graph_create_flags(const int64_t *src, const int64_t *dst, int64_t E, int64_t N,
+                                const int64_t *input_nodes, int64_t n_in, uint32_t flags,
+                                void *stream, ck_graph **out) {
     if (!out) return fail(CK_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
+    if (flags & ~(uint32_t)CK_GRAPH_EDGES_IN_HOST_MEMORY)
+        return fail(CK_ERR_INVALID_ARG, "unknown graph flag bits 0x%x", (unsigned)flags);
     if (N < 1 || N >= ((int64_t)1 << 31) - 1) return fail(CK_ERR_INVALID_ARG, "N must be in [1, 2^31 - 1)");
     if (E < 0 || E >= ((int64_t)1 << 31) - 1) return fail(CK_ERR_INVALID_ARG, "E must be in [0, 2^31 - 1)");
     if (n_in < 0 || n_in > N) return fail(CK_ERR_INVALID_ARG, "n_in must be in [0, N]");
@@ -134,7 +140,7 @@ ck_status ck_graph_create(const int64_t *src, const int64_t *dst, int64_t E, int
     g->N = N;
     g->E = E;
     g->n_in = n_in;
-    ck_status st = build_graph(g, src, dst, input_nodes, (cudaStream_t)stream);
+    ck_status st = build_graph(g, src, dst, input_nodes, flags, (cudaStream_t)stream);
     if (st != CK_OK) {
         char keep[sizeof(g_msg)];
         std::memcpy(keep, g_msg, sizeof(keep));

@@ -56,7 +56,7 @@ ck_status cuda_fail(cudaError_t e, const char *what);
 
 // Graph build (graph.cu).  Fills g's device arrays; synchronises `stream`.
 ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
-                      const int64_t *input_nodes, cudaStream_t stream);
+                      const int64_t *input_nodes, uint32_t graph_flags, cudaStream_t stream);
 
 // Device-side status words written by the recurrence kernels.
 enum : int { kDevOk = 0, kDevTimeout = 1, kDevInternal = 2 };
@@ -114,7 +114,6 @@ struct Options {
     std::atomic<long long> timeout_ns{4000000000LL};
     std::atomic<int> barrier_extra{0};
     std::atomic<int> graph_in_smem{1};
-    std::atomic<int> graph_in_host{0};
     std::atomic<int> recompute_steps{0};  // 0: about sqrt(T)
 };
 Options &options();

@@ -326,7 +326,7 @@ cudaError_t radix_sort(int *ka, int *va, int *kb, int *vb, int n, int key_bits, 
 }  // namespace
 
 ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
-                      const int64_t *input_nodes, cudaStream_t s) {
+                      const int64_t *input_nodes, uint32_t graph_flags, cudaStream_t s) {
     const int N = (int)g->N, E = (int)g->E, n_in = (int)g->n_in;
     cudaError_t e;
 #define CK_TRY(call, what)                                                              \
@@ -447,7 +447,7 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
     // (on a Grace-Blackwell node over the coherent CPU-GPU link): the graph
     // then holds O(N) device memory.  Every array is complete before the copy
     // (the piece cut above synchronised the stream after the last kernel).
-    if (options().graph_in_host) {
+    if (graph_flags & CK_GRAPH_EDGES_IN_HOST_MEMORY) {
         CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (graph build)");
         int **arrays[] = {&g->col, &g->perm, &g->colT, &g->permT, &g->rowid, &g->rowidT};
         void *h[6] = {};

@@ -53,12 +53,9 @@ def test_options_validate(lib):
         _ck.ck_set_option(17, 1)
     assert e.value.name == "CK_ERR_INVALID_ARG"
     assert _ck.ck_get_option(_ck.OPT_BARRIER_TIMEOUT_NS) == 4_000_000_000
-    # graph residency and recompute window: defaults, round trip, range
-    assert _ck.ck_get_option(_ck.OPT_GRAPH_IN_HOST_MEMORY) == 0
+    # recompute window: default, round trip, range
     assert _ck.ck_get_option(_ck.OPT_RECOMPUTE_STEPS) == 0
     try:
-        _ck.ck_set_option(_ck.OPT_GRAPH_IN_HOST_MEMORY, 1)
-        assert _ck.ck_get_option(_ck.OPT_GRAPH_IN_HOST_MEMORY) == 1
         _ck.ck_set_option(_ck.OPT_RECOMPUTE_STEPS, 5)
         assert _ck.ck_get_option(_ck.OPT_RECOMPUTE_STEPS) == 5
         with pytest.raises(_ck.CKError) as e:
@@ -66,7 +63,6 @@ def test_options_validate(lib):
         assert e.value.name == "CK_ERR_INVALID_ARG"
         assert _ck.ck_get_option(_ck.OPT_RECOMPUTE_STEPS) == 5
     finally:
-        _ck.ck_set_option(_ck.OPT_GRAPH_IN_HOST_MEMORY, 0)
         _ck.ck_set_option(_ck.OPT_RECOMPUTE_STEPS, 0)
 
 
@@ -80,6 +76,13 @@ def test_graph_create_rejects_bad_sizes_before_cuda(lib):
     assert lib.ck_graph_create(None, None, 3, 4, None, 0, None, ctypes.byref(h)) == 1  # NULL src
     assert b"NULL" in lib.ck_last_error_message()
     assert lib.ck_workspace_size(None, 1, 1, 1, None, None) == 1
+    # residency flags: unknown bits refused before any CUDA call
+    f = lib.ck_graph_create_flags
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
+    assert f(None, None, 0, 4, None, 0, 2, None, ctypes.byref(h)) == 1
+    assert b"flag" in lib.ck_last_error_message()
+    assert f(None, None, 0, 0, None, 0, 1, None, ctypes.byref(h)) == 1  # N < 1, valid flag
 
 
 def test_no_cpu_fallback_without_a_device(lib):

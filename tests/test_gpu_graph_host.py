@@ -1,4 +1,4 @@
-"""Graph indices in pinned host memory (CK_OPT_GRAPH_IN_HOST_MEMORY): the
+"""Graph indices in pinned host memory (CK_GRAPH_EDGES_IN_HOST_MEMORY): the
 kernels read col, perm and each edge's row in place over the CPU-GPU link and
 must give bitwise the results of the device-resident graph, in every launch
 mode and in the recomputing variant."""
@@ -19,7 +19,6 @@ def _default_options():
     yield
     _ck.ck_set_option(_ck.OPT_PERSISTENT, 1)
     _ck.ck_set_option(_ck.OPT_GRAPH_IN_SMEM, 1)
-    _ck.ck_set_option(_ck.OPT_GRAPH_IN_HOST_MEMORY, 0)
 
 
 def host_graph(c):
@@ -34,11 +33,9 @@ def _assert_same(a, b):
         np.testing.assert_array_equal(a[1][k], b[1][k], err_msg=k)
 
 
-def test_option_is_restored_and_export_matches():
-    from sparse_graph_recurrent_gb300 import _ck
+def test_export_matches_device_graph():
     c = workloads.small(501, 300, 20000, 10, 8, 1, 1, hub_deg=9000)
     gd, gh = make_graph(c), host_graph(c)
-    assert _ck.ck_get_option(_ck.OPT_GRAPH_IN_HOST_MEMORY) == 0
     ed, eh = gd.export(), gh.export()
     for k in ed:
         assert torch.equal(ed[k], eh[k]), k
