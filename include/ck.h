@@ -139,7 +139,10 @@ ck_status ck_graph_export(const ck_graph *g, int32_t *row_ptr, int32_t *col, int
  *                  run at the same time need two buffers
  * Both depend on the device's SM count: query on the device that will run the calls.
  * Errors: CK_ERR_INVALID_ARG (B, T, microsteps < 1), CK_ERR_UNSUPPORTED (B > 512,
- * or sizes whose element offsets overflow the index types).
+ * sizes whose element offsets overflow the index types, or a graph whose
+ * pieces finish more rows than a CTA's shared memory holds tables for: 24
+ * bytes per row, about 4,000 rows per piece, i.e. about 1.2 million nodes at a
+ * few edges per node on 152 SMs).
  */
 ck_status ck_workspace_size(const ck_graph *g, int64_t B, int64_t T, int64_t microsteps,
                             size_t *saved_bytes, size_t *scratch_bytes);
