@@ -31,9 +31,10 @@ def _common(c, cid):
 
 @pytest.mark.parametrize("cid", [0, 1, 2, 3])
 def test_shapes_and_structure(cid):
-    c = workloads.make(cid)
+    c = workloads.make(cid, with_dout=cid != 3)  # the wide dOut alone is 1.3 GB
     src, dst = _common(c, cid)
-    assert c["dout"].shape == (c["T"], c["B"], c["N"])
+    if cid != 3:
+        assert c["dout"].shape == (c["T"], c["B"], c["N"])
     d = _indeg(c)
     if cid == 0:
         assert np.all(src != dst)
