@@ -65,7 +65,10 @@ class SparseGraph:
         return _ck.ck_workspace_size(self._h, B, T, microsteps)
 
     def scratch(self, B: int, T: int, microsteps: int):
-        """A cached scratch buffer for (B, T, microsteps) on this graph's device."""
+        """A cached scratch buffer for (B, T, microsteps) on this graph's device
+        (the last shape asked for is kept).  Calls that may run at the same
+        time, on different streams, need buffers of their own: pass scratch=
+        to forward / backward."""
         key = (B, T, microsteps)
         buf = self._ws.get(key)
         if buf is None:
@@ -75,13 +78,15 @@ class SparseGraph:
         return buf
 
 
-def forward(graph: SparseGraph, edge_values, leak, bias, drives, state0, microsteps: int):
+def forward(graph: SparseGraph, edge_values, leak, bias, drives, state0, microsteps: int,
+            scratch=None):
     """Raw forward: returns (out [T,B,N], saved buffer, scratch buffer)."""
     B, N = state0.shape
     T = drives.shape[0]
     saved_b, _ = graph.workspace_size(B, T, microsteps)
     saved = torch.empty(saved_b, dtype=torch.uint8, device=state0.device)
-    scratch = graph.scratch(B, T, microsteps)
+    if scratch is None:
+        scratch = graph.scratch(B, T, microsteps)
     out = torch.empty((T, B, N), dtype=torch.float32, device=state0.device)
     _ck.ck_forward(graph.handle, edge_values, leak, bias, drives, state0, microsteps, out,
                    saved, scratch)
