@@ -84,9 +84,9 @@ struct KArgs {
     float *out;
     float *H, *Pr;  // saved states and proposals (Pr null: proposals not kept)
     // H[s] lives in slot s - h_off of H (modulo h_mod when h_mod > 0) and
-    // Pr[s] in slot s - p_off of Pr: the saved arrays by default, a one-step
-    // window when the backward recomputes, a two-slot ping-pong when the
-    // forward keeps only checkpoints
+    // Pr[s] in slot s - p_off of Pr: the saved arrays by default, a window of
+    // K input steps when the backward recomputes, a two-slot ping-pong when
+    // the forward keeps only checkpoints
     int h_off, h_mod, p_off;
     float *ckpt;  // forward: also write the state after every input step here ([T+1][N][Bp])
     const float *dout;
