@@ -56,3 +56,13 @@ def test_source_digest_ignores_comments_not_code(tmp_path):
     assert bench.source_digest(str(p)) != d0  # code
     p.write_text(base.replace('"a // b"', '"a // c"'))
     assert bench.source_digest(str(p)) != d0  # "//" inside a string is code
+
+
+def test_byte_model_matches_the_documented_figures():
+    """The roofline's algorithmic bytes per launch for the FlyGPT shape are the
+    ones the design notes quote (9.42 GB forward, 10.04 GB backward); the
+    gathered rows (4EB per microstep) are most of them."""
+    fwd, bwd = bench.byte_model(5000, 524324, 32, 64, 2, 64)
+    assert (fwd, bwd) == (9_417_761_280, 10_035_540_480)
+    gathered = 64 * 2 * 4 * 524324 * 32
+    assert 0.9 < gathered / fwd < 1.0 and 0.85 < gathered / bwd < 1.0
