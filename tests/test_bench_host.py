@@ -1,5 +1,6 @@
-"""bench.py's clock record: only the nvidia-smi samples taken inside the timed
-region count (host logic, no GPU)."""
+"""bench.py's host logic, no GPU: the clock record keeps only the nvidia-smi
+samples taken inside the timed region; the profile digest ignores comments but
+not code; the byte model gives the documented per-launch figures."""
 import datetime
 import os
 import sys
