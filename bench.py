@@ -130,6 +130,16 @@ def hbm_bytes(N, E, B, T, M, n_in):
     return saved + io + (graph if graph <= L2_BYTES else S * graph)
 
 
+def step_roofline(q_l2, q_hbm, bw_l2_gbs, bw_hbm_gbs, step_ms):
+    """The step-level fraction: the roofline time max(Q_L2 / BW_L2, Q_HBM /
+    BW_HBM) of a whole step over its measured time, and which bound sets it."""
+    t_l2 = q_l2 / (bw_l2_gbs * 1e9) * 1e3
+    t_hbm = q_hbm / (bw_hbm_gbs * 1e9) * 1e3
+    bound, t = ("l2", t_l2) if t_l2 >= t_hbm else ("hbm", t_hbm)
+    return {"bound": bound, "roofline_ms": t, "step_ms": step_ms, "frac": t / step_ms,
+            "l2_ms": t_l2, "hbm_ms": t_hbm}
+
+
 def flops_per_step(N, E, B, T, M):
     """Algorithmic floating-point operations of one step: per microstep about
     6EB (gather multiply-add forward; gather and edge-gradient dot backward)
@@ -477,6 +487,7 @@ def run_ours(args, c, rank, world, dist):
                          "frac": q_hbm / (ms_per_step / 1e3) / 1e9 / hbm_peak,
                          "peak_source": f"{hbm_src} (MEASURED_PEAKS.json hbm_gbs)",
                          "bytes_per_step": q_hbm},
+        "roofline_step": step_roofline(fb + bb, q_hbm, l2_read, hbm_peak, ms_per_step),
         "l2_probe": {"dense_read_gbs": l2_read, "row_gather_gbs": l2_gather},
         "flops": {"gflop_per_step": gflop, "achieved_tflops": gflop / ms_per_step,
                   "fp32_fma_peak_tflops": fp32_peak, "frac": gflop / ms_per_step / fp32_peak},

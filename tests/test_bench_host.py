@@ -67,3 +67,12 @@ def test_byte_model_matches_the_documented_figures():
     assert (fwd, bwd) == (9_417_761_280, 10_035_540_480)
     gathered = 64 * 2 * 4 * 524324 * 32
     assert 0.9 < gathered / fwd < 1.0 and 0.85 < gathered / bwd < 1.0
+
+
+def test_step_roofline_takes_the_slower_bound():
+    # FlyGPT-like: 19.45 GB at L2 over 18,000 GB/s beats 0.43 GB over 6,673 GB/s
+    r = bench.step_roofline(19.45e9, 0.43e9, 18000.0, 6673.5, 2.4)
+    assert r["bound"] == "l2" and abs(r["roofline_ms"] - 19.45 / 18.0) < 1e-9
+    assert abs(r["frac"] - (19.45 / 18.0) / 2.4) < 1e-9
+    r = bench.step_roofline(1e9, 30e9, 18000.0, 6000.0, 10.0)
+    assert r["bound"] == "hbm" and abs(r["roofline_ms"] - 5.0) < 1e-9 and abs(r["frac"] - 0.5) < 1e-9
