@@ -335,6 +335,16 @@ int64_t ck_last_launch_count(void);
 ck_status ck_probe_read(const void *buf, size_t bytes, int64_t reps, float *sink, void *stream);
 ck_status ck_probe_gather(const float *rows, int64_t nrows, int64_t row_floats,
                           const int32_t *idx, int64_t nidx, float *sink, void *stream);
+/*
+ * ck_probe_read_shape -- ck_probe_read with the load shape chosen: `depth`
+ * independent 16-byte loads in flight per thread (2, 4, 8, or 16 with at most
+ * 512 threads), CTAs of `threads` threads (128, 256, 512 or 1024),
+ * `ctas_per_sm` CTAs per SM (threads x ctas_per_sm <= 2048).  A sweep over
+ * shapes gives the highest L2 read rate of the device, the denominator of the
+ * L2 roofline.  Errors: CK_ERR_INVALID_ARG for a shape outside those sets.
+ */
+ck_status ck_probe_read_shape(const void *buf, size_t bytes, int64_t reps, int64_t depth,
+                              int64_t threads, int64_t ctas_per_sm, float *sink, void *stream);
 
 const char *ck_status_string(ck_status s);
 const char *ck_last_error_message(void);

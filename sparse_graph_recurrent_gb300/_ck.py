@@ -66,6 +66,7 @@ def load() -> ctypes.CDLL:
         "ck_forward_static_scratch": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p],
         "ck_probe_read": [p, sz, i64, p, p],
         "ck_probe_gather": [p, i64, i64, p, i64, p, p],
+        "ck_probe_read_shape": [p, sz, i64, i64, i64, i64, p, p],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -272,6 +273,11 @@ def ck_query_status(scratch, stream=None):
 def ck_probe_read(buf, reps, sink, stream=None):
     _check(load().ck_probe_read(_ptr(buf), buf.numel() * buf.element_size(), reps, _ptr(sink),
                                 _stream(stream)))
+
+
+def ck_probe_read_shape(buf, reps, depth, threads, ctas_per_sm, sink, stream=None):
+    _check(load().ck_probe_read_shape(_ptr(buf), buf.numel() * buf.element_size(), reps, depth,
+                                      threads, ctas_per_sm, _ptr(sink), _stream(stream)))
 
 
 def ck_probe_gather(rows, idx, sink, stream=None):

@@ -368,3 +368,30 @@ def test_edge_order_and_splitting(oracle_lib):
     np.testing.assert_allclose(out_p, out_b, rtol=0, atol=1e-14)
     assert abs(g_p["dw"][5] - g_b["dw"][5]) < 1e-13
     assert abs(g_p["dw"][-1] - g_b["dw"][5]) < 1e-13
+
+
+# --------------------------------------------------------------------------
+# run_case(batch_cols=...): the column-restricted run the full-size parity
+# tests compare against.  Batch columns are independent sequences (intro: the
+# recurrence runs per sample), so restricting to some columns must give those
+# columns of the full run, and the shared-parameter gradients must be the full
+# run's with dOut zero outside them.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cols", [[1, 4], [0], [5, 2, 3]])
+def test_run_case_batch_cols(oracle_lib, cols):
+    c = _case(seed=31, N=14, E=60, n_in=4, B=6, T=3, M=2)
+    out_c, g_c = oracle_lib.run_case(c, batch_cols=cols)
+    out_f, g_f = oracle_lib.run_case(c)
+    np.testing.assert_allclose(out_c, out_f[:, cols], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(g_c["ddrives"], g_f["ddrives"][:, :, cols], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(g_c["dstate0"], g_f["dstate0"][cols], rtol=0, atol=1e-15)
+    masked = dict(c)
+    keep = np.zeros(c["B"], bool)
+    keep[cols] = True
+    masked["dout"] = np.where(keep[None, :, None], c["dout"], 0.0)
+    _, g_m = oracle_lib.run_case(masked)
+    for k in ("dw", "dleak", "dbias"):
+        np.testing.assert_allclose(g_c[k], g_m[k], rtol=1e-13, atol=1e-15, err_msg=k)
+        # and the mask matters: the unmasked full run differs
+        assert np.abs(g_f[k] - g_c[k]).max() > 1e-6, k
