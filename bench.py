@@ -17,8 +17,8 @@ host memory, read by the kernels over the CPU-GPU link.
 
 With N > 1 (under torchrun) every rank runs an independent replica of the
 same step (the method has no exchange between replicas): weak scaling.
---impl reference times the CPU oracle (fp64, single thread) on one batch
-column per step, scaled to the whole batch.  --impl torch-sparse times, for
+--impl reference times the CPU oracle (fp64) on whole steps, every batch
+column, spread over all host cores with OpenMP.  --impl torch-sparse times, for
 context only, the step written with torch.sparse.mm in a Python loop (the
 baseline the page compares its fused kernels with); it is not part of the
 library.
@@ -140,6 +140,21 @@ def step_roofline(q_l2, q_hbm, bw_l2_gbs, bw_hbm_gbs, step_ms):
             "l2_ms": t_l2, "hbm_ms": t_hbm}
 
 
+def memory_figures(N, E, B, T, n_in, graph_bytes, saved_b, scratch_b, ckpt_b, scratch_rc_b):
+    """Device bytes one training step holds: the graph, the caller's inputs,
+    outputs and gradients, and the saved activations and scratch of the
+    regular pair or of the recomputing pair."""
+    io = 4 * (E + 2 * N + T * n_in * B + B * N  # w, leak, bias, drives, state0
+              + 2 * T * B * N                     # out, dOut
+              + E + 2 * N + T * n_in * B + B * N)  # their gradients
+    return {"graph_bytes": graph_bytes, "io_bytes": io, "saved_bytes": saved_b,
+            "scratch_bytes": scratch_b, "step_bytes": graph_bytes + io + saved_b + scratch_b,
+            "recompute": {"ckpt_bytes": ckpt_b, "scratch_bytes": scratch_rc_b,
+                          "step_bytes": graph_bytes + io + ckpt_b + scratch_rc_b},
+            "page_context": "connectome-kernels page, Why table (B200): fused kernels 0.55 GB, "
+                            "torch.sparse 2.43 GB per training step"}
+
+
 def flops_per_step(N, E, B, T, M):
     """Algorithmic floating-point operations of one step: per microstep about
     6EB (gather multiply-add forward; gather and edge-gradient dot backward)
@@ -230,13 +245,53 @@ class Clocks:
                 round(1e3 * (rows[-1][0] - rows[0][0]) / max(len(rows) - 1, 1), 1)}
 
 
-def cpu_oracle_sample(c, cols):
-    """Time the oracle (single thread) on some batch columns of the workload."""
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def oracle_step_seconds(c, threads):
+    """Seconds of one whole oracle step (forward and backward over every batch
+    column): the single-thread oracle for threads == 1, else its column-parallel
+    statement on `threads` OpenMP threads."""
     import oracle
     oracle.build()
     t0 = time.perf_counter()
-    oracle.run_case(c, batch_cols=cols)
+    if threads == 1:
+        oracle.run_case(c)
+    else:
+        oracle.step_columns(c, threads)
     return time.perf_counter() - t0
+
+
+def cpu_baseline(c, omp_steps=3):
+    """The oracle timed on this host: one whole single-thread step, and
+    `omp_steps` whole steps over all cores (OpenMP across batch columns)."""
+    import oracle
+    oracle.build()
+    cores = oracle.threads_available()
+    single = oracle_step_seconds(c, 1)
+    multi = [oracle_step_seconds(c, cores) for _ in range(omp_steps)]
+    per = statistics.mean(multi)
+    return {"value": 1.0 / per, "unit": "steps/s", "cores": cores, "threads": cores,
+            "cpu_model": cpu_model(), "kind": "oracle",
+            "sample": f"{omp_steps} whole steps (all {c['B']} batch columns, full graph and "
+                      f"window), fp64, OpenMP over batch columns on {cores} threads",
+            "single_thread": {"value": 1.0 / single, "unit": "steps/s", "threads": 1,
+                              "sample": "one whole step on one thread (the oracle as it stands)"}}
 
 
 def torch_sparse_step(c, dev, dtype):
@@ -292,23 +347,31 @@ def run_torch_sparse(args, c, rank):
 
 
 def run_reference(args, c, rank):
+    """The reference arm: the CPU oracle, whole steps over all batch columns,
+    OpenMP across columns on every host core (rank 0 only)."""
     if rank != 0:
         return
-    B = c["B"]
+    import oracle
+    oracle.build()
+    cores = oracle.threads_available()
     for _ in range(args.warmup):
-        cpu_oracle_sample(c, [0])
-    times = [cpu_oracle_sample(c, [k % B]) for k in range(args.steps)]
-    per_step = statistics.mean(times) * B
+        oracle_step_seconds(c, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step_seconds(c, cores)
+    per_step = (time.perf_counter() - t0) / args.steps
     value = 1.0 / per_step
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": value / PAGE_STEPS_PER_S, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": _workload_name(c), "parallelism": "replicas"},
-        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                         "sample": f"1 of {B} batch columns per step (full graph, T, M), "
-                                   f"time x{B}"},
+        "config": {"workload": _workload_name(c), "parallelism": "replicas",
+                   "l2": "not applicable (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "threads": cores,
+                         "cpu_model": cpu_model(), "kind": "oracle",
+                         "sample": f"{args.steps} whole steps (all {c['B']} batch columns), fp64, "
+                                   f"OpenMP over batch columns on {cores} threads"},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -321,6 +384,29 @@ CONFIG_NAMES = {0: "tiny", 1: "flygpt", 2: "ragged", 3: "wide", 4: "connectome"}
 def _workload_name(c):
     name = CONFIG_NAMES.get(c.get("config_id", 1), "workload")
     return f"{name} N={c['N']} E={c['E']} B={c['B']} T={c['T']} M={c['M']}"
+
+
+# Shapes of the dense L2 read probe swept for the roofline's denominator:
+# (load bytes, loads in flight per thread, threads per CTA, CTAs per SM).
+# Each keeps one pass of the whole grid (loads x threads x bytes) within half
+# of the 64 MB buffer, so every thread runs its loads-in-flight loop.
+L2_SWEEP = [(16, 4, 512, 2), (16, 8, 512, 2), (16, 16, 256, 2), (16, 8, 1024, 1),
+            (32, 2, 512, 2), (32, 4, 256, 4), (32, 4, 512, 2), (32, 2, 512, 4),
+            (32, 8, 256, 2), (32, 4, 1024, 1), (32, 2, 256, 8)]
+L2_SWEEP_BYTES = 64 << 20
+
+
+def l2_read_sweep(timed, buf, sink):
+    """GB/s of the dense L2 read probe for each swept shape (and the fixed
+    ck_probe_read); `timed(fn)` returns the rate of 10 reads of `buf`."""
+    from sparse_graph_recurrent_gb300 import _ck
+    out = [{"shape": "ck_probe_read (16-byte loads, 4 in flight, 2 x 512 threads per SM)",
+            "gbs": timed(lambda: _ck.ck_probe_read(buf, 10, sink))}]
+    for lb, depth, thr, cps in L2_SWEEP:
+        out.append({"shape": f"{lb}-byte loads, {depth} in flight, {cps} x {thr} threads per SM",
+                    "gbs": timed(lambda: _ck.ck_probe_read_shape(buf, 10, lb, depth, thr, cps,
+                                                                 sink))})
+    return out
 
 
 def run_ours(args, c, rank, world, dist):
@@ -339,6 +425,9 @@ def run_ours(args, c, rank, world, dist):
     w, leak, bias, drives, state0, dout = (tt(c[k]) for k in ("w", "leak", "bias", "drives",
                                                               "state0", "dout"))
     saved_b, scratch_b = g.workspace_size(B, T, M)
+    ckpt_b, scratch_rc_b = _ck.ck_workspace_size_recompute(g.handle, B, T, M)
+    mem = memory_figures(N, E, B, T, n_in, _ck.ck_graph_memory(g.handle)[0], saved_b, scratch_b,
+                         ckpt_b, scratch_rc_b)
     saved = torch.empty(saved_b, dtype=torch.uint8, device=dev)
     scratch = torch.empty(scratch_b, dtype=torch.uint8, device=dev)
     out = torch.empty((T, B, N), device=dev)
@@ -364,7 +453,7 @@ def run_ours(args, c, rank, world, dist):
     # L2 peaks in this run: dense read of a 64 MB buffer, and a gather of
     # random 128-byte rows from a state-sized table (the forward's pattern)
     sink = torch.zeros(1, device=dev)
-    buf = torch.ones(16 << 20, device=dev)
+    buf = torch.ones(L2_SWEEP_BYTES // 4, device=dev)
     rows = torch.ones((N, 32), device=dev)
     idx = torch.randint(0, N, (E,), dtype=torch.int32, device=dev)
 
@@ -379,7 +468,9 @@ def run_ours(args, c, rank, world, dist):
         torch.cuda.synchronize()
         return nbytes / (e0.elapsed_time(e1) / 1e3 / reps) / 1e9
 
-    l2_read = probe(lambda: _ck.ck_probe_read(buf, 10, sink), buf.numel() * 4 * 10)
+    l2_sweep = l2_read_sweep(lambda f: probe(f, buf.numel() * 4 * 10), buf, sink)
+    l2_best = max(l2_sweep, key=lambda r: r["gbs"])
+    l2_read = l2_best["gbs"]
     l2_gather = probe(lambda: _ck.ck_probe_gather(rows, idx, sink), E * 128)
 
     clocks = Clocks(local)
@@ -481,14 +572,16 @@ def run_ours(args, c, rank, world, dist):
         "roofline": {"bound": "l2", "kernel": dom, "achieved": achieved, "peak": l2_read,
                      "unit": "GB/s", "frac": achieved / l2_read,
                      "traffic": ncu_traffic(dom) if headline else None,
-                     "peak_source": "measured in this run: dense 16-byte L2 reads of a 64 MB buffer"},
+                     "peak_source": "measured in this run: the fastest of a sweep of dense L2 "
+                                    "reads of a 64 MB buffer (" + l2_best["shape"] + ")"},
         "roofline_hbm": {"bound": "hbm", "achieved": q_hbm / (ms_per_step / 1e3) / 1e9,
                          "peak": hbm_peak, "unit": "GB/s",
                          "frac": q_hbm / (ms_per_step / 1e3) / 1e9 / hbm_peak,
                          "peak_source": f"{hbm_src} (MEASURED_PEAKS.json hbm_gbs)",
                          "bytes_per_step": q_hbm},
         "roofline_step": step_roofline(fb + bb, q_hbm, l2_read, hbm_peak, ms_per_step),
-        "l2_probe": {"dense_read_gbs": l2_read, "row_gather_gbs": l2_gather},
+        "l2_probe": {"dense_read_gbs": l2_read, "row_gather_gbs": l2_gather,
+                     "sweep": [{"shape": r["shape"], "gbs": round(r["gbs"], 1)} for r in l2_sweep]},
         "flops": {"gflop_per_step": gflop, "achieved_tflops": gflop / ms_per_step,
                   "fp32_fma_peak_tflops": fp32_peak, "frac": gflop / ms_per_step / fp32_peak},
         "kernels": {"forward_ms": f_mean, "backward_ms": b_mean,
@@ -497,17 +590,12 @@ def run_ours(args, c, rank, world, dist):
         "e2e": {"value": world / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches[0],
+        "memory": mem,
         "clocks": clk,
         "samples_ms": [round(a + b, 4) for a, b in zip(fwd_ms, bwd_ms)],
     }
     if not args.no_cpu_baseline and world == 1:
-        cols = list(range(args.cpu_cols))
-        secs = cpu_oracle_sample(c, cols)
-        per_step = secs * B / len(cols)
-        line["cpu_baseline"] = {"value": 1.0 / per_step, "unit": "steps/s", "cores": 1,
-                                "kind": "oracle",
-                                "sample": f"{len(cols)} of {B} batch columns, full graph and window "
-                                          f"({secs:.1f} s), scaled x{B / len(cols):g}"}
+        line["cpu_baseline"] = cpu_baseline(c)
     print(json.dumps(line), flush=True)
 
 
@@ -517,7 +605,6 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference", "torch-sparse"], default="ours")
-    ap.add_argument("--cpu-cols", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--config", type=int, choices=range(5), default=1)
     ap.add_argument("--microsteps", type=int, default=None)

@@ -115,6 +115,10 @@ ck_status ck_graph_destroy(ck_graph *g);
 /* Sizes recorded in the handle (any output pointer may be NULL). */
 ck_status ck_graph_info(const ck_graph *g, int64_t *N, int64_t *E, int64_t *n_in);
 
+/* Memory the handle holds until ck_graph_destroy: device bytes and pinned host
+ * bytes (nonzero with CK_GRAPH_EDGES_IN_HOST_MEMORY).  Either pointer may be NULL. */
+ck_status ck_graph_memory(const ck_graph *g, size_t *device_bytes, size_t *host_bytes);
+
 /*
  * ck_graph_export -- copy the graph arrays out, for tests: (device) int32
  * row_ptr[N+1], col[E], perm[E], rowT_ptr[N+1], colT[E], permT[E], slot[N].
@@ -123,6 +127,33 @@ ck_status ck_graph_info(const ck_graph *g, int64_t *N, int64_t *E, int64_t *n_in
 ck_status ck_graph_export(const ck_graph *g, int32_t *row_ptr, int32_t *col, int32_t *perm,
                           int32_t *rowT_ptr, int32_t *colT, int32_t *permT, int32_t *slot,
                           void *stream);
+
+/*
+ * ck_graph_tiling -- the shared-memory tiling of one direction (dir 0: rows
+ * keyed by dst, the forward; 1: keyed by src, the backward), which the
+ * kernels use when the padded batch is at most 32 columns (connectome-kernels
+ * page, "Design notes": the state stored [N, B] is gathered row by row; here a
+ * CTA gathers from a chunk of the state rows held in its shared memory).  The
+ * column nodes are cut into C chunks and the rows into G blocks; CTA
+ * t = g * C + j owns cell (g, j): the edges of block g whose column lies in
+ * chunk j, in row order.  info receives {C, G, P = G * C, most rows in a block,
+ * most rows a CTA finishes, most nodes in a chunk, most edges in a cell, length
+ * of the row-pointer array}; all zero when the direction has no tiling (graphs
+ * whose state rows do not fit eight CTAs' shared memory).
+ */
+ck_status ck_graph_tiling(const ck_graph *g, int dir, int64_t info[8]);
+
+/*
+ * ck_graph_export_tiling -- copy one direction's tiling out, for tests:
+ * (device) int32 meta[P][12] (per CTA: first row, rows, first and end edge,
+ * chunk's first node, chunk nodes, offset of its row pointers, first and end
+ * row it finishes relative to the block, chunk, block, 0), ptr[ptr length]
+ * (per CTA, rows + 1 positions into the edge arrays), col[E] (column node minus
+ * its chunk's first node), perm[E] (caller's edge id), rowid[E] (row node).
+ * Any pointer may be NULL.  Errors: CK_ERR_INVALID_ARG (dir, no tiling).
+ */
+ck_status ck_graph_export_tiling(const ck_graph *g, int dir, int32_t *meta, int32_t *ptr,
+                                 int32_t *col, int32_t *perm, int32_t *rowid, void *stream);
 
 /*
  * ck_workspace_size -- bytes of the two caller-owned buffers for batch B,
@@ -272,9 +303,12 @@ ck_status ck_sgd_update(float *param, const float *grad, int64_t n, float lr, vo
  *
  *   - Allocates nothing and calls no allocating routine.
  *   - Every GPU that loads the library holds the 32 MiB array until the process
- *     exits.  The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     exits.  Each call made outside a stream capture looks up the array's
+ *     device address (cudaGetSymbolAddress) with the call's device current, so
+ *     a reset of the device's primary context, which moves the array, is
+ *     followed; a call inside a capture reuses the last address looked up on
+ *     that device, so make a first call on each device before any capture, and
+ *     none across a context reset inside a capture.
  *   - All calls share the one array: two calls whose work overlaps on the GPU
  *     (different streams, different threads) race and corrupt each other.
  *     Each call clears the words that must start at zero; the rest of the
@@ -282,8 +316,9 @@ ck_status ck_sgd_update(float *param, const float *grad, int64_t n, float lr, vo
  *   - Shapes whose forward workspace exceeds the array (control words, one
  *     carry row per CTA, one float per edge and per padded node-batch element)
  *     are refused with CK_ERR_UNSUPPORTED and a message giving both sizes.
- *   - Device-side wait timeouts are not reported by this call (ck_query_status
- *     needs a caller-owned scratch buffer).
+ *   - A device-side wait that times out makes the kernel stop early; this call
+ *     still returns CK_OK (it does not wait for the kernel), so check
+ *     ck_query_status_static before using the outputs or `saved`.
  * Errors: CK_ERR_INVALID_ARG, CK_ERR_WORKSPACE, CK_ERR_UNSUPPORTED, CK_ERR_CUDA.
  */
 ck_status ck_forward_static_scratch(const ck_graph *g, const float *edge_values,
@@ -291,6 +326,16 @@ ck_status ck_forward_static_scratch(const ck_graph *g, const float *edge_values,
                                     const float *state0, int64_t B, int64_t T,
                                     int64_t microsteps, float *states_out, void *saved,
                                     size_t saved_bytes, void *stream);
+
+/*
+ * ck_query_status_static -- ck_query_status for ck_forward_static_scratch:
+ * synchronise `stream` and report whether the last static-scratch forward on
+ * the current device finished every device-side wait (CK_OK), or a bounded
+ * wait gave up (CK_ERR_TIMEOUT: that forward stopped early; its outputs and
+ * `saved` are not valid).  Reads the status word out of the static array with
+ * cudaMemcpyFromSymbol; allocates nothing.  Also reports pending CUDA errors.
+ */
+ck_status ck_query_status_static(void *stream);
 
 /*
  * ck_query_status -- synchronise `stream` and report whether the last
@@ -308,10 +353,28 @@ typedef enum {
                                        that never come, so every wait runs out (default 0) */
     CK_OPT_GRAPH_IN_SMEM = 3,       /* 1 (default): keep each CTA's slice of the graph in
                                        shared memory when it fits; 0: always stream it */
-    CK_OPT_RECOMPUTE_STEPS = 4      /* input steps K one recomputation window spans
+    CK_OPT_RECOMPUTE_STEPS = 4,     /* input steps K one recomputation window spans
                                        (ck_workspace_size_recompute and the two calls
                                        after it must see the same value); 0 (default):
                                        round(sqrt(T)); clamped to [1, T] */
+    CK_OPT_ROWS_IN_SMEM = 5,        /* 1 (default): keep each CTA's per-row partial sums in
+                                       shared memory when they fit; 0: always in the
+                                       scratch buffer (a test switch: results are bitwise
+                                       the same either way) */
+    CK_OPT_TEST_BOUNDS_PROBE = 6,   /* test hook for the bounds-checked build of the library
+                                       (compiled with -DCK_DEBUG_BOUNDS, which checks every
+                                       gathered row, table and carry index on the device and
+                                       reports a bad one through ck_query_status as
+                                       CK_ERR_INTERNAL instead of making the access): 1 makes
+                                       each recurrence kernel check one deliberately
+                                       out-of-range index, never used for an access, so a test
+                                       sees the report; no effect in the ordinary build
+                                       (default 0) */
+    CK_OPT_TILED = 7                /* 1: when the graph has a shared-memory tiling
+                                       (ck_graph_tiling) and the padded batch is at most 32
+                                       columns, run the tiled kernels; 0 (default): always
+                                       the L2-gather kernels.  ck_workspace_size and the
+                                       calls after it must see the same value */
 } ck_option;
 
 ck_status ck_set_option(ck_option opt, int64_t value);
@@ -336,15 +399,17 @@ ck_status ck_probe_read(const void *buf, size_t bytes, int64_t reps, float *sink
 ck_status ck_probe_gather(const float *rows, int64_t nrows, int64_t row_floats,
                           const int32_t *idx, int64_t nidx, float *sink, void *stream);
 /*
- * ck_probe_read_shape -- ck_probe_read with the load shape chosen: `depth`
- * independent 16-byte loads in flight per thread (2, 4, 8, or 16 with at most
- * 512 threads), CTAs of `threads` threads (128, 256, 512 or 1024),
- * `ctas_per_sm` CTAs per SM (threads x ctas_per_sm <= 2048).  A sweep over
- * shapes gives the highest L2 read rate of the device, the denominator of the
- * L2 roofline.  Errors: CK_ERR_INVALID_ARG for a shape outside those sets.
+ * ck_probe_read_shape -- ck_probe_read with the load shape chosen: loads of
+ * `load_bytes` bytes (16, or 32: the 256-bit vector load of sm_100 and later),
+ * `depth` of them in flight per thread (2, 4, 8, or 16 with at most 512
+ * threads), CTAs of `threads` threads (128, 256, 512 or 1024), `ctas_per_sm`
+ * CTAs per SM (threads x ctas_per_sm <= 2048); `buf` 32-byte aligned.  A sweep
+ * over shapes gives the highest L2 read rate of the device, the denominator of
+ * the L2 roofline.  Errors: CK_ERR_INVALID_ARG for a shape outside those sets.
  */
-ck_status ck_probe_read_shape(const void *buf, size_t bytes, int64_t reps, int64_t depth,
-                              int64_t threads, int64_t ctas_per_sm, float *sink, void *stream);
+ck_status ck_probe_read_shape(const void *buf, size_t bytes, int64_t reps, int64_t load_bytes,
+                              int64_t depth, int64_t threads, int64_t ctas_per_sm, float *sink,
+                              void *stream);
 
 const char *ck_status_string(ck_status s);
 const char *ck_last_error_message(void);

@@ -34,8 +34,12 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB_PATH) or \
             os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared",
-                               "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
+        base = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math"]
+        # OpenMP serves only oracle_step_columns (batch columns on several
+        # cores); without it that function runs on one thread
+        if subprocess.call(base + ["-fopenmp", "-o", tmp, _SRC, "-lm"],
+                           stderr=subprocess.DEVNULL) != 0:
+            subprocess.check_call(base + ["-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -51,6 +55,11 @@ def _load():
         lib.oracle_backward.argtypes = [i64, i64, p, p, p, p, i64, p, i64, i64,
                                         i64, p, p, p, p, p, p, p, p]
         lib.oracle_backward.restype = ctypes.c_int
+        lib.oracle_step_columns.argtypes = [i64, i64, p, p, p, p, p, i64, p, p, p, p,
+                                            i64, i64, i64, ctypes.c_int, p, p, p, p, p, p]
+        lib.oracle_step_columns.restype = ctypes.c_int
+        lib.oracle_threads_available.argtypes = []
+        lib.oracle_threads_available.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -131,6 +140,36 @@ def run_case(case: dict, M: int | None = None, batch_cols=None):
     grads = backward(case["N"], case["src"], case["dst"], case["w"], case["leak"],
                      case["input_nodes"], hprev, pre, dout, M)
     return out, grads
+
+
+def threads_available() -> int:
+    """Cores the OpenMP step may use (1 when built without OpenMP)."""
+    return int(_load().oracle_threads_available())
+
+
+def step_columns(case: dict, threads: int, M: int | None = None):
+    """One whole step (forward and backward) of a workload dict, its batch
+    columns spread over `threads` threads.  Same results as run_case up to
+    the grouping of the sums over columns of dw, dleak and dbias (per thread,
+    then over threads in order).  Returns (out, grads) like run_case."""
+    M = case["M"] if M is None else M
+    N = case["N"]
+    src, dst, inp = _i64(case["src"]), _i64(case["dst"]), _i64(case["input_nodes"])
+    w, leak, bias = _f64(case["w"]), _f64(case["leak"]), _f64(case["bias"])
+    drives, state0, dout = _f64(case["drives"]), _f64(case["state0"]), _f64(case["dout"])
+    T, n_in, B = drives.shape
+    E = src.size
+    out = np.empty((T, B, N))
+    g = dict(dw=np.empty(E), dleak=np.empty(N), dbias=np.empty(N),
+             ddrives=np.empty((T, n_in, B)), dstate0=np.empty((B, N)))
+    rc = _load().oracle_step_columns(N, E, _ptr(src), _ptr(dst), _ptr(w), _ptr(leak),
+                                     _ptr(bias), n_in, _ptr(inp), _ptr(drives), _ptr(state0),
+                                     _ptr(dout), B, T, M, int(threads), _ptr(out),
+                                     _ptr(g["dw"]), _ptr(g["dleak"]), _ptr(g["dbias"]),
+                                     _ptr(g["ddrives"]), _ptr(g["dstate0"]))
+    if rc != 0:
+        raise MemoryError("oracle_step_columns could not allocate")
+    return out, g
 
 
 def csr(N: int, key, other):

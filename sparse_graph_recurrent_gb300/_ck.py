@@ -19,7 +19,7 @@ STATUS = {0: "CK_OK", 1: "CK_ERR_INVALID_ARG", 2: "CK_ERR_CUDA", 3: "CK_ERR_OUT_
           4: "CK_ERR_TIMEOUT", 5: "CK_ERR_WORKSPACE", 6: "CK_ERR_INTERNAL",
           7: "CK_ERR_UNSUPPORTED"}
 (OPT_PERSISTENT, OPT_BARRIER_TIMEOUT_NS, OPT_TEST_BARRIER_EXTRA, OPT_GRAPH_IN_SMEM,
- OPT_RECOMPUTE_STEPS) = range(5)
+ OPT_RECOMPUTE_STEPS, OPT_ROWS_IN_SMEM, OPT_TEST_BOUNDS_PROBE, OPT_TILED) = range(8)
 GRAPH_EDGES_IN_HOST_MEMORY = 1  # ck_graph_flag
 
 _lib = None
@@ -32,16 +32,22 @@ class CKError(RuntimeError):
         self.name = STATUS.get(status, str(status))
 
 
+def library_variant():
+    """The library variant this process loads: None (libck.so) or "bounds"
+    (libck_bounds.so, the bounds-checked build), from CK_LIBRARY_VARIANT."""
+    return os.environ.get("CK_LIBRARY_VARIANT") or None
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.lib_path(library_variant())
 
 
 def load() -> ctypes.CDLL:
-    """Load libck.so, building it with nvcc first if it is missing or stale."""
+    """Load the library, building it with nvcc first if it is missing or stale."""
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.build()
+    path = _build.build(variant=library_variant())
     if not os.path.exists(path):
         raise ImportError(f"libck.so not found at {path}")
     lib = ctypes.CDLL(path)
@@ -53,6 +59,9 @@ def load() -> ctypes.CDLL:
         "ck_graph_create_flags": [p, p, i64, i64, p, i64, ctypes.c_uint32, p, ctypes.POINTER(p)],
         "ck_graph_destroy": [p],
         "ck_graph_info": [p, pi64, pi64, pi64],
+        "ck_graph_memory": [p, psz, psz],
+        "ck_graph_tiling": [p, ctypes.c_int, pi64],
+        "ck_graph_export_tiling": [p, ctypes.c_int, p, p, p, p, p, p],
         "ck_graph_export": [p, p, p, p, p, p, p, p, p],
         "ck_workspace_size": [p, i64, i64, i64, psz, psz],
         "ck_forward": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p, sz, p],
@@ -62,11 +71,12 @@ def load() -> ctypes.CDLL:
         "ck_forward_checkpointed": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p, sz, p],
         "ck_backward_recompute": [p, p, p, p, p, i64, i64, i64, p, sz, p, p, p, p, p, p, p, sz, p],
         "ck_query_status": [p, p],
+        "ck_query_status_static": [p],
         "ck_set_option": [ctypes.c_int, i64],
         "ck_forward_static_scratch": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p],
         "ck_probe_read": [p, sz, i64, p, p],
         "ck_probe_gather": [p, i64, i64, p, i64, p, p],
-        "ck_probe_read_shape": [p, sz, i64, i64, i64, i64, p, p],
+        "ck_probe_read_shape": [p, sz, i64, i64, i64, i64, i64, p, p],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -270,14 +280,41 @@ def ck_query_status(scratch, stream=None):
     _check(load().ck_query_status(_ptr(scratch), _stream(stream)))
 
 
+def ck_graph_memory(handle):
+    """(device bytes, pinned host bytes) the graph handle holds."""
+    d, h = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(load().ck_graph_memory(handle, ctypes.byref(d), ctypes.byref(h)))
+    return d.value, h.value
+
+
+TILING_KEYS = ("C", "G", "P", "max_rows", "max_fin", "max_chunk", "max_edges", "ptr_len")
+
+
+def ck_graph_tiling(handle, direction: int) -> dict:
+    """The shared-memory tiling of one direction (all zero when it has none)."""
+    info = (ctypes.c_int64 * 8)()
+    _check(load().ck_graph_tiling(handle, direction, info))
+    return dict(zip(TILING_KEYS, list(info)))
+
+
+def ck_graph_export_tiling(handle, direction: int, meta, ptr, col, perm, rowid, stream=None):
+    _check(load().ck_graph_export_tiling(handle, direction, _ptr(meta), _ptr(ptr), _ptr(col),
+                                         _ptr(perm), _ptr(rowid), _stream(stream)))
+
+
+def ck_query_status_static(stream=None):
+    _check(load().ck_query_status_static(_stream(stream)))
+
+
 def ck_probe_read(buf, reps, sink, stream=None):
     _check(load().ck_probe_read(_ptr(buf), buf.numel() * buf.element_size(), reps, _ptr(sink),
                                 _stream(stream)))
 
 
-def ck_probe_read_shape(buf, reps, depth, threads, ctas_per_sm, sink, stream=None):
-    _check(load().ck_probe_read_shape(_ptr(buf), buf.numel() * buf.element_size(), reps, depth,
-                                      threads, ctas_per_sm, _ptr(sink), _stream(stream)))
+def ck_probe_read_shape(buf, reps, load_bytes, depth, threads, ctas_per_sm, sink, stream=None):
+    _check(load().ck_probe_read_shape(_ptr(buf), buf.numel() * buf.element_size(), reps,
+                                      load_bytes, depth, threads, ctas_per_sm, _ptr(sink),
+                                      _stream(stream)))
 
 
 def ck_probe_gather(rows, idx, sink, stream=None):

@@ -84,6 +84,9 @@ ck_status ck_set_option(ck_option opt, int64_t v) {
             o.barrier_extra = (int)v;
             return CK_OK;
         case CK_OPT_GRAPH_IN_SMEM: o.graph_in_smem = v != 0; return CK_OK;
+        case CK_OPT_ROWS_IN_SMEM: o.rows_in_smem = v != 0; return CK_OK;
+        case CK_OPT_TEST_BOUNDS_PROBE: o.bounds_probe = v != 0; return CK_OK;
+        case CK_OPT_TILED: o.tiled = v != 0; return CK_OK;
         case CK_OPT_RECOMPUTE_STEPS:
             if (v < 0 || v > (1 << 30)) return fail(CK_ERR_INVALID_ARG, "recompute steps must be in [0, 2^30]");
             o.recompute_steps = (int)v;
@@ -100,6 +103,9 @@ int64_t ck_get_option(ck_option opt) {
         case CK_OPT_TEST_BARRIER_EXTRA: return o.barrier_extra;
         case CK_OPT_GRAPH_IN_SMEM: return o.graph_in_smem;
         case CK_OPT_RECOMPUTE_STEPS: return o.recompute_steps;
+        case CK_OPT_ROWS_IN_SMEM: return o.rows_in_smem;
+        case CK_OPT_TEST_BOUNDS_PROBE: return o.bounds_probe;
+        case CK_OPT_TILED: return o.tiled;
     }
     return -1;
 }
@@ -164,6 +170,13 @@ ck_status ck_graph_destroy(ck_graph *g) {
     for (int d = 0; d < 2; ++d)
         for (int v = 0; v < 3; ++v)
             if (g->piece[d][v]) cudaFree(g->piece[d][v]);
+    for (int d = 0; d < 2; ++d) {
+        Tiled &t = g->tiled[d];
+        for (int *p : {t.meta, t.ptr})
+            if (p) cudaFree(p);
+        for (int *p : {t.col, t.perm, t.rowid})
+            if (p) g->edges_in_host ? cudaFreeHost(p) : cudaFree(p);
+    }
     delete g;
     return CK_OK;
 }
@@ -173,6 +186,46 @@ ck_status ck_graph_info(const ck_graph *g, int64_t *N, int64_t *E, int64_t *n_in
     if (N) *N = g->N;
     if (E) *E = g->E;
     if (n_in) *n_in = g->n_in;
+    return CK_OK;
+}
+
+ck_status ck_graph_memory(const ck_graph *g, size_t *device_bytes, size_t *host_bytes) {
+    if (!g) return fail(CK_ERR_INVALID_ARG, "graph handle is NULL");
+    if (device_bytes) *device_bytes = g->device_bytes;
+    if (host_bytes) *host_bytes = g->host_bytes;
+    return CK_OK;
+}
+
+ck_status ck_graph_tiling(const ck_graph *g, int dir, int64_t info[8]) {
+    if (!g || !info || dir < 0 || dir > 1) return fail(CK_ERR_INVALID_ARG, "bad graph, info or dir");
+    const Tiled &t = g->tiled[dir];
+    const int64_t ptr_len = t.C ? (int64_t)t.C * (g->N + t.G) : 0;
+    const int64_t v[8] = {t.C, t.G, t.P, t.max_rows, t.max_fin, t.max_chunk, t.max_edges, ptr_len};
+    for (int i = 0; i < 8; ++i) info[i] = v[i];
+    return CK_OK;
+}
+
+ck_status ck_graph_export_tiling(const ck_graph *g, int dir, int32_t *meta, int32_t *ptr,
+                                 int32_t *col, int32_t *perm, int32_t *rowid, void *stream) {
+    if (!g || dir < 0 || dir > 1) return fail(CK_ERR_INVALID_ARG, "bad graph or dir");
+    const Tiled &t = g->tiled[dir];
+    if (t.C == 0) return fail(CK_ERR_INVALID_ARG, "direction %d has no tiling", dir);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t E = (size_t)g->E;
+    struct {
+        int32_t *dst;
+        const int *src;
+        size_t n;
+    } cp[] = {{meta, t.meta, (size_t)t.P * kTileInts},
+              {ptr, t.ptr, (size_t)t.C * (size_t)(g->N + t.G)},
+              {col, t.col, E},
+              {perm, t.perm, E},
+              {rowid, t.rowid, E}};
+    for (auto &c : cp) {
+        if (!c.dst || c.n == 0) continue;
+        cudaError_t e = cudaMemcpyAsync(c.dst, c.src, sizeof(int) * c.n, cudaMemcpyDefault, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (tiling export)");
+    }
     return CK_OK;
 }
 
@@ -327,6 +380,9 @@ ck_status ck_query_status(const void *scratch, void *stream) {
     e = cudaMemcpy(&word, (const char *)scratch + kStatusOffset, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy (status word)");
     if (word == kDevTimeout) return fail(CK_ERR_TIMEOUT, "a device-side wait timed out");
+    if (word == kDevBounds)
+        return fail(CK_ERR_INTERNAL, "an index out of bounds was caught and its access skipped "
+                                     "(bounds-checked build)");
     if (word != kDevOk) return fail(CK_ERR_INTERNAL, "device status word %d", word);
     return CK_OK;
 }

@@ -13,6 +13,7 @@
 // masks taken in element order.  Every pass keeps equal keys in their previous
 // order, so the result lists each row's edges in ascending caller edge id.
 #include <algorithm>
+#include <cstring>
 #include <vector>
 
 #include "ck_internal.h"
@@ -297,6 +298,121 @@ std::vector<int> piece_meta(const Cut &k, const std::vector<int> &rp, int N, int
     return m;
 }
 
+// Cut [0, n) into k contiguous ranges of about equal total weight (prefix
+// weights pre[0..n], pre[0] = 0): range r ends at the first index whose prefix
+// reaches (r + 1) / k of the total.  Returns k + 1 bounds.
+std::vector<int> balanced_cuts(const std::vector<long long> &pre, int n, int k) {
+    std::vector<int> b(k + 1, n);
+    b[0] = 0;
+    const long long total = pre[n];
+    int i = 0;
+    for (int r = 1; r < k; ++r) {
+        const long long target = (total * r + k - 1) / k;
+        while (i < n && pre[i] < target) ++i;
+        b[r] = std::max(b[r - 1], i);
+    }
+    return b;
+}
+
+// Host-side tiling of one direction (ck::Tiled), from its compressed rows.
+// Returns the layout in host vectors; C == 0 when no tiling fits.
+struct TiledHost {
+    Tiled t;
+    std::vector<int> meta, ptr, col, perm, rowid;
+};
+
+TiledHost tile_direction(int dir, int N, int E, int sms, const std::vector<int> &rp,
+                         const std::vector<int> &col, const std::vector<int> &perm) {
+    TiledHost h;
+    std::memset(&h.t, 0, sizeof(h.t));
+    // column degrees (edges whose column is each node)
+    std::vector<long long> colpre(N + 1, 0);
+    for (int k = 0; k < E; ++k) colpre[col[k] + 1] += 1;
+    for (int i = 0; i < N; ++i) colpre[i + 1] += colpre[i] + 1;  // + 1: a node's row of the chunk
+    std::vector<long long> rowpre(N + 1, 0);
+    for (int i = 0; i < N; ++i) rowpre[i + 1] = rowpre[i] + (rp[i + 1] - rp[i]) + 4;
+    static const int kChunks[] = {1, 2, 3, 4, 5, 6, 8};
+    for (int C : kChunks) {
+        if (C > N) break;
+        const int G = std::min(sms / C, N);
+        if (G < 1) break;
+        std::vector<int> cb = balanced_cuts(colpre, N, C);
+        int max_chunk = 0;
+        for (int j = 0; j < C; ++j) max_chunk = std::max(max_chunk, cb[j + 1] - cb[j]);
+        if (!tiled_fits(dir, kTiledMaxBp, 0, 0, max_chunk)) {
+            // edge-balanced chunks too uneven: equal node ranges
+            for (int j = 0; j <= C; ++j) cb[j] = (int)((long long)N * j / C);
+            max_chunk = 0;
+            for (int j = 0; j < C; ++j) max_chunk = std::max(max_chunk, cb[j + 1] - cb[j]);
+        }
+        const std::vector<int> rb = balanced_cuts(rowpre, N, G);
+        int max_rows = 0;
+        for (int g = 0; g < G; ++g) max_rows = std::max(max_rows, rb[g + 1] - rb[g]);
+        const int max_fin = (max_rows + C - 1) / C;
+        if (!tiled_fits(dir, kTiledMaxBp, max_rows, max_fin, max_chunk)) continue;
+        // chunk of every column node
+        std::vector<int> chunk_of(N);
+        for (int j = 0; j < C; ++j)
+            for (int i = cb[j]; i < cb[j + 1]; ++i) chunk_of[i] = j;
+        const int P = G * C;
+        std::vector<long long> cnt(P + 1, 0);
+        for (int g = 0; g < G; ++g)
+            for (int k = rp[rb[g]]; k < rp[rb[g + 1]]; ++k) cnt[g * C + chunk_of[col[k]] + 1] += 1;
+        for (int t = 0; t < P; ++t) cnt[t + 1] += cnt[t];
+        std::vector<long long> pos(cnt.begin(), cnt.end() - 1);
+        std::vector<int> off(P + 1, 0);
+        for (int t = 0; t < P; ++t) off[t + 1] = off[t] + (rb[t / C + 1] - rb[t / C]) + 1;
+        h.ptr.assign(off[P], 0);
+        const size_t E1 = E > 0 ? (size_t)E : 1;
+        h.col.assign(E1, 0);
+        h.perm.assign(E1, 0);
+        h.rowid.assign(E1, 0);
+        int max_edges = 0;
+        for (int g = 0; g < G; ++g) {
+            for (int i = rb[g]; i < rb[g + 1]; ++i) {
+                for (int j = 0; j < C; ++j) h.ptr[off[g * C + j] + (i - rb[g])] = (int)pos[g * C + j];
+                for (int k = rp[i]; k < rp[i + 1]; ++k) {
+                    const int j = chunk_of[col[k]];
+                    const long long q = pos[g * C + j]++;
+                    h.col[q] = col[k] - cb[j];
+                    h.perm[q] = perm[k];
+                    h.rowid[q] = i;
+                }
+            }
+            for (int j = 0; j < C; ++j) {
+                const int t = g * C + j;
+                h.ptr[off[t] + (rb[g + 1] - rb[g])] = (int)pos[t];
+                max_edges = std::max(max_edges, (int)(cnt[t + 1] - cnt[t]));
+            }
+        }
+        h.meta.assign((size_t)P * kTileInts, 0);
+        for (int t = 0; t < P; ++t) {
+            const int g = t / C, j = t % C, R = rb[g + 1] - rb[g];
+            int *m = &h.meta[(size_t)t * kTileInts];
+            m[0] = rb[g];
+            m[1] = R;
+            m[2] = (int)cnt[t];
+            m[3] = (int)cnt[t + 1];
+            m[4] = cb[j];
+            m[5] = cb[j + 1] - cb[j];
+            m[6] = off[t];
+            m[7] = (int)((long long)R * j / C);
+            m[8] = (int)((long long)R * (j + 1) / C);
+            m[9] = j;
+            m[10] = g;
+        }
+        h.t.C = C;
+        h.t.G = G;
+        h.t.P = P;
+        h.t.max_rows = max_rows;
+        h.t.max_fin = max_fin;
+        h.t.max_chunk = max_chunk;
+        h.t.max_edges = max_edges;
+        return h;
+    }
+    return h;  // no tiling fits
+}
+
 struct DevBuf {
     void *p = nullptr;
     ~DevBuf() {
@@ -348,6 +464,7 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
     CK_TRY(cudaMalloc((void **)&g->permT, sizeof(int) * E1), "cudaMalloc permT");
     CK_TRY(cudaMalloc((void **)&g->rowid, sizeof(int) * E1), "cudaMalloc rowid");
     CK_TRY(cudaMalloc((void **)&g->rowidT, sizeof(int) * E1), "cudaMalloc rowidT");
+    g->device_bytes += sizeof(int) * (3 * (size_t)N + 2 + 6 * E1);
 
     const int ntiles = (E + kTile - 1) / kTile;
     const size_t n_hist = 256 * (size_t)(ntiles > 0 ? ntiles : 1);
@@ -435,11 +552,49 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
                 }
                 const std::vector<int> m = piece_meta(cuts[best], rp, (int)N, P);
                 CK_TRY(cudaMalloc((void **)&g->piece[d][v], sizeof(int) * m.size()), "cudaMalloc piece");
+                g->device_bytes += sizeof(int) * m.size();
                 CK_TRY(cudaMemcpy(g->piece[d][v], m.data(), sizeof(int) * m.size(), cudaMemcpyHostToDevice),
                        "copy piece descriptions");
                 g->max_rows[d][v] = cuts[best].max_rows;
                 g->max_edges[d][v] = cuts[best].max_edges;
                 g->row_weight[d][v] = weights[best];
+            }
+        }
+    }
+    // Shared-memory tilings (ck::Tiled), one per direction, for graphs whose
+    // state rows fit a few CTAs' shared memory: built on the host from the
+    // compressed rows.
+    {
+        CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (graph build)");
+        std::vector<int> rp(N + 1), cl((size_t)E), pm((size_t)E);
+        const int *rps[2] = {g->row_ptr, g->rowT_ptr};
+        const int *cls[2] = {g->col, g->colT};
+        const int *pms[2] = {g->perm, g->permT};
+        for (int d = 0; d < 2; ++d) {
+            // a chunk of at least one node per C, at 32 columns, must fit: skip large graphs early
+            if (!tiled_fits(d, kTiledMaxBp, 0, 0, (N + 7) / 8)) continue;
+            CK_TRY(cudaMemcpy(rp.data(), rps[d], sizeof(int) * (N + 1), cudaMemcpyDeviceToHost),
+                   "copy row pointers (tiling)");
+            if (E > 0) {
+                CK_TRY(cudaMemcpy(cl.data(), cls[d], sizeof(int) * E, cudaMemcpyDeviceToHost),
+                       "copy columns (tiling)");
+                CK_TRY(cudaMemcpy(pm.data(), pms[d], sizeof(int) * E, cudaMemcpyDeviceToHost),
+                       "copy permutation (tiling)");
+            }
+            TiledHost th = tile_direction(d, N, E, g->num_sms, rp, cl, pm);
+            if (th.t.C == 0) continue;
+            Tiled &t = g->tiled[d];
+            t = th.t;
+            struct Arr {
+                int **dst;
+                const std::vector<int> *src;
+            } arrs[] = {{&t.meta, &th.meta}, {&t.ptr, &th.ptr}, {&t.col, &th.col},
+                        {&t.perm, &th.perm}, {&t.rowid, &th.rowid}};
+            for (auto &a : arrs) {
+                const size_t bytes = sizeof(int) * a.src->size();
+                CK_TRY(cudaMalloc((void **)a.dst, bytes), "cudaMalloc tiling");
+                g->device_bytes += bytes;
+                CK_TRY(cudaMemcpy(*a.dst, a.src->data(), bytes, cudaMemcpyHostToDevice), "copy tiling");
             }
         }
     }
@@ -449,16 +604,26 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
     // (the piece cut above synchronised the stream after the last kernel).
     if (graph_flags & CK_GRAPH_EDGES_IN_HOST_MEMORY) {
         CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (graph build)");
-        int **arrays[] = {&g->col, &g->perm, &g->colT, &g->permT, &g->rowid, &g->rowidT};
-        void *h[6] = {};
+        const size_t Et = E > 0 ? (size_t)E : 1;  // tiled arrays' length
+        int **arrays[12] = {&g->col, &g->perm, &g->colT, &g->permT, &g->rowid, &g->rowidT};
+        size_t lens[12] = {E1, E1, E1, E1, E1, E1};
+        int na = 6;
+        for (int d = 0; d < 2; ++d) {
+            if (g->tiled[d].C == 0) continue;
+            for (int **p : {&g->tiled[d].col, &g->tiled[d].perm, &g->tiled[d].rowid}) {
+                arrays[na] = p;
+                lens[na++] = Et;
+            }
+        }
+        void *h[12] = {};
         auto drop = [&]() {
             for (void *p : h)
                 if (p) cudaFreeHost(p);
         };
         // all copies first, so that a failure leaves the device arrays in place
-        for (int i = 0; i < 6; ++i) {
-            e = cudaHostAlloc(&h[i], sizeof(int) * E1, cudaHostAllocMapped | cudaHostAllocPortable);
-            if (e == cudaSuccess) e = cudaMemcpy(h[i], *arrays[i], sizeof(int) * E1, cudaMemcpyDeviceToHost);
+        for (int i = 0; i < na; ++i) {
+            e = cudaHostAlloc(&h[i], sizeof(int) * lens[i], cudaHostAllocMapped | cudaHostAllocPortable);
+            if (e == cudaSuccess) e = cudaMemcpy(h[i], *arrays[i], sizeof(int) * lens[i], cudaMemcpyDeviceToHost);
             void *dv = nullptr;
             if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dv, h[i], 0);
             if (e != cudaSuccess) {
@@ -474,9 +639,11 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
                 return fail(CK_ERR_UNSUPPORTED, "host memory is not mapped at the same address on the device");
             }
         }
-        for (int i = 0; i < 6; ++i) {
+        for (int i = 0; i < na; ++i) {
             cudaFree(*arrays[i]);
             *arrays[i] = (int *)h[i];
+            g->device_bytes -= sizeof(int) * lens[i];
+            g->host_bytes += sizeof(int) * lens[i];
         }
         g->edges_in_host = 1;
     }

@@ -22,26 +22,30 @@ namespace {
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
 static __device__ __align__(256) unsigned char g_forward_scratch[kStaticScratchBytes];
 
-// Device address of g_forward_scratch, looked up once per device.  In host
-// code the array's name only stands in for the symbol; kernels need this.
+// Device address of g_forward_scratch on each device.  In host code the
+// array's name only stands in for the symbol; kernels need this address.  It
+// is looked up again on every call made outside a stream capture (a reset of
+// the device's primary context reloads the module and moves the array), and
+// the last address is reused inside a capture, where the lookup may not run.
 constexpr int kMaxDevices = 64;
 void *g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mu;
 
-ck_status static_scratch(int dev, void **out) {
+ck_status static_scratch(int dev, cudaStream_t stream, void **out) {
     if (dev < 0 || dev >= kMaxDevices) return fail(CK_ERR_UNSUPPORTED, "device id %d out of range", dev);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone || !g_scratch_addr[dev]) {
         void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_forward_scratch);
+        e = cudaGetSymbolAddress(&p, g_forward_scratch);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress (static forward scratch)");
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];
     return CK_OK;
 }
-
-size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 }  // namespace ck
@@ -71,29 +75,36 @@ extern "C" ck_status ck_forward_static_scratch(const ck_graph *g, const float *e
     if (saved_bytes < p.saved_bytes)
         return fail(CK_ERR_WORKSPACE, "saved too small: %zu < %zu", saved_bytes, p.saved_bytes);
 
-    // The forward touches only these scratch regions: control words, carries,
-    // permuted edge values and row sums.  Lay them out back to back.
+    // the regions the forward touches, laid out back to back in the array
     Plan q = p;
-    size_t off = 0;
-    q.off_ctrl = off;
-    off += q.ctrl_bytes;
-    q.off_carry = off;
-    off = up256(off + 8 * (size_t)q.P * q.Bp);
-    q.off_wperm = off;
-    off = up256(off + 4 * (size_t)(q.E > 0 ? q.E : 1));
-    q.off_rowsum = off;
-    off = up256(off + 4 * (size_t)q.N * q.Bp);
-    q.off_dwperm = q.off_G = q.off_da = q.off_lacc = 0;  // backward-only regions, unused here
-    q.scratch_bytes = off;
-    if (off > kStaticScratchBytes)
+    forward_only_scratch(&q);
+    if (q.scratch_bytes > kStaticScratchBytes)
         return fail(CK_ERR_UNSUPPORTED,
                     "this shape needs %zu bytes of forward scratch; the static array holds %zu "
                     "(use ck_forward with a caller-allocated scratch buffer)",
-                    off, kStaticScratchBytes);
+                    q.scratch_bytes, kStaticScratchBytes);
     void *scratch = nullptr;
-    st = static_scratch(dev, &scratch);
+    st = static_scratch(dev, (cudaStream_t)stream, &scratch);
     if (st != CK_OK) return st;
     FwdIO io{edge_values, leak, bias, drives, state0, states_out, (float *)saved, scratch};
     int64_t launches = 0;
     return launch_forward(g, q, io, (cudaStream_t)stream, &launches);
+}
+
+extern "C" ck_status ck_query_status_static(void *stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "pending CUDA error");
+    int word = 0;
+    // the control block sits at offset 0 of the array (forward_only_scratch)
+    e = cudaMemcpyFromSymbol(&word, g_forward_scratch, sizeof(int), kStatusOffset,
+                             cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol (status word)");
+    if (word == kDevTimeout) return fail(CK_ERR_TIMEOUT, "a device-side wait timed out");
+    if (word == kDevBounds)
+        return fail(CK_ERR_INTERNAL, "an index out of bounds was caught and its access skipped "
+                                     "(bounds-checked build)");
+    if (word != kDevOk) return fail(CK_ERR_INTERNAL, "device status word %d", word);
+    return CK_OK;
 }

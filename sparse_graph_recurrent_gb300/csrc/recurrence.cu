@@ -101,6 +101,16 @@ struct KArgs {
     int init_w, zero_dw;  // write the permuted edge values / clear the edge-gradient sums (global)
     unsigned bar_base, bar_extra;
     unsigned long long timeout_ns;
+    int bounds_probe;  // bounds-checked build: check one out-of-range index (test hook)
+    // tiled kernels: per-CTA cell descriptions and row pointers, the chunk of
+    // gathered rows in shared memory, the exchange of partial row totals
+    const int *tmeta, *tptr;
+    int o_chunk;       // shared-memory offset of the chunk of gathered rows
+    int chunk_cap;     // most nodes in a chunk
+    int fin_cap;       // most rows a CTA finishes
+    int tC;            // chunks (CTAs per block)
+    int xrows;         // row stride of the exchange buffer per CTA (most rows in a block)
+    unsigned long long *xbuf;  // [P][xrows][Bp] {float bits, phase id} partial totals
 };
 
 // ---------------------------------------------------------------- helpers
@@ -297,6 +307,7 @@ __device__ __forceinline__ float *S_st3(const KArgs &a) { return reinterpret_cas
 __device__ __forceinline__ float *S_st4(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_st4); }
 __device__ __forceinline__ int *S_inp(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_inp); }
 __device__ __forceinline__ float2 *S_acc(const KArgs &a) { return reinterpret_cast<float2 *>(ck_smem + a.o_acc); }
+__device__ __forceinline__ float *S_chunk(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_chunk); }
 // Row stride of the staged arrays that are also read or written across rows
 // (forward st0, backward st3): Bp + 1 words, so a warp walking down a column
 // touches 32 distinct banks as well as one walking along a row.
@@ -415,7 +426,9 @@ __device__ __forceinline__ void group_dots(float (&d)[UNR], int lig, int lpe, in
     }
 }
 
-template <int NC, bool SMEMG, bool BWD, int UNR, bool HS>
+// TT: the gathered rows are the chunk in shared memory (tiled kernels; column
+// indices then count from the chunk's first node), else `rows` in global memory.
+template <int NC, bool SMEMG, bool BWD, int UNR, bool HS, bool TT = false>
 __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int gam, int lig,
                                              bool active, const float *__restrict__ rows,
                                              const float *__restrict__ hprev) {
@@ -446,13 +459,15 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     auto load_h = [&](int row) -> HRow {
         HRow h;
         if (HS) {
-            const int i = row - c.r0;
+            int i = row - c.r0;
             const bool in = row >= 0 && i <= c.nrows;  // always, for a valid graph
+            if (in && !CK_IN(a.err, i, a.rows_cap)) i = 0;
             const float *hp = S_st4(a) + (size_t)(in ? i : 0) * Bp + lig * 4;
 #pragma unroll
             for (int ch = 0; ch < HN; ++ch)
                 h.v[ch] = in ? *reinterpret_cast<const float4 *>(hp + ch * CW) : zero4();
         } else {
+            if (row >= 0 && !CK_IN(a.err, row, a.N)) row = 0;
             const float *hp = hprev + (size_t)(row < 0 ? 0 : row) * Bp + lig * 4;
 #pragma unroll
             for (int ch = 0; ch < HN; ++ch)
@@ -463,7 +478,9 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     HRow hcur, hnext;
     int nxt = -1;
     auto next_row = [&](int row) -> int {  // the row after `row` that has edges in [k0, k1)
-        const int pos = S_srp(a)[row - c.r0 + 1];
+        int ir = row - c.r0 + 1;
+        if (!CK_IN(a.err, ir, a.rows_cap)) ir = 0;
+        const int pos = S_srp(a)[ir];
         return pos < k1 ? row_at(pos) : -1;
     };
     if (BWD) {
@@ -504,13 +521,15 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     float gdw = 0.f, cdw = 0.f;
     auto load_graph = [&](int kb) {
         if (BWD && !SMEMG && dw_owner) {
-            const int kk = kb + (lig >> per_sh);
+            int kk = kb + (lig >> per_sh);
+            if (kk < k1 && !CK_IN(a.err, kk, a.E)) kk = k1;
             gdw = kk < k1 ? __ldcg(a.dwperm + kk) : 0.f;
         }
 #pragma unroll
         for (int q = 0; q < (SMEMG ? 1 : UNR); ++q) {
             const int kk = kb + q;
-            const int kc = kk < k1 ? kk : c.e0;
+            int kc = kk < k1 ? kk : c.e0;
+            if (!CK_IN(a.err, kc, a.E)) kc = 0;
             gc[q] = __ldg(a.col + kc);
             gw[q] = __ldcg(a.wperm + kc);
         }
@@ -535,7 +554,9 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             int cc;
             float wv;
             if (SMEMG) {
-                const int2 cw = S_scw(a)[kc - c.e0];
+                int ks = kc - c.e0;
+                if (!CK_IN(a.err, ks, a.cap)) ks = 0;
+                const int2 cw = S_scw(a)[ks];
                 cc = cw.x;
                 wv = __int_as_float(cw.y);
             } else {
@@ -543,9 +564,18 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                 wv = wn[q];
             }
             bt.w[q] = ok ? wv : 0.f;
-            const float *rp = rows + (size_t)cc * Bp + lig * 4;
+            if constexpr (TT) {
+                if (!CK_IN(a.err, cc, a.chunk_cap)) cc = 0;
+                const float *rp = S_chunk(a) + cc * Bp + lig * 4;
 #pragma unroll
-            for (int ch = 0; ch < NC; ++ch) bt.v[q][ch] = __ldca(reinterpret_cast<const float4 *>(rp + ch * CW));
+                for (int ch = 0; ch < NC; ++ch) bt.v[q][ch] = *reinterpret_cast<const float4 *>(rp + ch * CW);
+            } else {
+                if (!CK_IN(a.err, cc, a.N)) cc = 0;
+                const float *rp = rows + (size_t)cc * Bp + lig * 4;
+#pragma unroll
+                for (int ch = 0; ch < NC; ++ch)
+                    bt.v[q][ch] = __ldca(reinterpret_cast<const float4 *>(rp + ch * CW));
+            }
         }
     };
     // The group's current row is cur and its edges end at bnd = row_ptr[cur +
@@ -556,6 +586,10 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
         flush(cur);
         do {
             ++cur;
+            if (!CK_IN(a.err, cur - c.r0 + 1, a.rows_cap)) {
+                cur = c.r0 + a.rows_cap - 2;
+                break;
+            }
         } while (S_srp(a)[cur - c.r0 + 1] <= kk);
         bnd = S_srp(a)[cur - c.r0 + 1];
         if (BWD) {
@@ -591,7 +625,8 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             if (bfly) {
                 // lanes lig = m * (LPE / UNR) hold item m
                 const int kk = kb + (lig >> per_sh);
-                if ((lig & ((1 << per_sh) - 1)) == 0 && kk < k1) {
+                if ((lig & ((1 << per_sh) - 1)) == 0 && kk < k1 &&
+                    CK_IN(a.err, SMEMG ? kk - c.e0 : kk, SMEMG ? a.cap : a.E)) {
                     if (SMEMG) S_sdw(a)[kk - c.e0] += d[0];
                     else a.dwperm[kk] = cdw + d[0];
                 }
@@ -599,7 +634,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
 #pragma unroll
                 for (int q = 0; q < UNR; ++q) {
                     const int kk = kb + q;
-                    if (kk < k1) {
+                    if (kk < k1 && CK_IN(a.err, SMEMG ? kk - c.e0 : kk, SMEMG ? a.cap : a.E)) {
                         if (SMEMG) S_sdw(a)[kk - c.e0] += d[q];
                         else a.dwperm[kk] += d[q];
                     }
@@ -650,7 +685,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             }
         }
     }
-    if (active) {
+    if (active && CK_IN(a.err, gam, a.G)) {
         float *dst = S_scarry(a) + (size_t)gam * Bp + lig * 4;
 #pragma unroll
         for (int ch = 0; ch < NC; ++ch) *reinterpret_cast<float4 *>(dst + ch * CW) = acc[ch];
@@ -692,7 +727,7 @@ __device__ __forceinline__ float carry_sum(const KArgs &a, const float *sc, int 
     const float v1 = sc[(size_t)min(h1, a.G - 1) * a.Bp];
     float x = ga < gb ? v0 : 0.f;
     x += h1 < gb ? v1 : 0.f;
-    for (int h = h1 + a.EPW; h < gb; h += a.EPW) x += sc[(size_t)h * a.Bp];
+    for (int h = h1 + a.EPW; h < gb && CK_IN(a.err, h, a.G); h += a.EPW) x += sc[(size_t)h * a.Bp];
     return x;
 }
 
@@ -726,7 +761,8 @@ __device__ __forceinline__ void row_sums4(const KArgs &a, const Cta &c, const in
     }
 #pragma unroll
     for (int el = 0; el < 4; ++el)
-        for (int h = h2[el]; h < gb[el]; h += a.EPW) cs[el] += sc[(size_t)h * a.Bp + bb[el]];
+        for (int h = h2[el]; h < gb[el] && CK_IN(a.err, h, a.G); h += a.EPW)
+            cs[el] += sc[(size_t)h * a.Bp + bb[el]];
 #pragma unroll
     for (int el = 0; el < 4; ++el) x[el] = slot[el] + cs[el];
 }
@@ -736,7 +772,8 @@ __device__ __forceinline__ float global_carry(const KArgs &a, const Cta &c, int 
                                               unsigned phase_id) {
     float x = 0.f;
     for (int cc = c.c_lo; cc < (int)blockIdx.x; ++cc)
-        x += wait_carry(a, a.carry + (size_t)cc * a.Bp + b, phase_id);
+        if (CK_IN(a.err, cc, a.P) && CK_IN(a.err, b, a.Bp))
+            x += wait_carry(a, a.carry + (size_t)cc * a.Bp + b, phase_id);
     return x;
 }
 
@@ -851,6 +888,7 @@ __device__ __forceinline__ void finish_fwd_batch(const KArgs &a, const Cta &c, c
 
 // Row i's sum for column b (b < Bp): row_sums4's terms in its order.
 __device__ __forceinline__ float row_sum1(const KArgs &a, const Cta &c, int i, int b) {
+    if (!CK_IN(a.err, i, a.rows_cap)) i = 0;
     const int2 g2 = S_sgrp(a)[i];
     const int gr = g2.x;
     const float *sc = S_scarry(a) + b;
@@ -860,13 +898,16 @@ __device__ __forceinline__ float row_sum1(const KArgs &a, const Cta &c, int i, i
     const float v1 = sc[min(h1, a.G - 1) * a.Bp];
     float cs = ga < gb ? v0 : 0.f;
     cs += h1 < gb ? v1 : 0.f;
-    for (int h = h1 + a.EPW; h < gb; h += a.EPW) cs += sc[h * a.Bp];
+    for (int h = h1 + a.EPW; h < gb && CK_IN(a.err, h, a.G); h += a.EPW) cs += sc[h * a.Bp];
     return (gr < 0 ? 0.f : sv) + cs;
 }
 
-template <int THREADS>
+// The row total of a finished row i (relative to c.r0) in column b: rowx(i,
+// b, lane_ok) -- the row slot plus carries (and earlier CTAs' carries) here,
+// the sum of the chunks' partial totals in the tiled kernels.
+template <int THREADS, class RowX>
 __device__ __forceinline__ void finish_fwd_narrow(const KArgs &a, const Cta &c, int s,
-                                                  unsigned phase_id) {
+                                                  RowX &&rowx) {
     constexpr int U = THREADS / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Bp = a.Bp, B = a.B, PS = Bp + 1;
@@ -880,13 +921,13 @@ __device__ __forceinline__ void finish_fwd_narrow(const KArgs &a, const Cta &c, 
     const int b = lane_ok ? lane : 0, bl = live ? lane : B - 1;
     const int sh = c.glob ? 1 : 0;
     auto row = [&](int i) {
-        float x = row_sum1(a, c, i, b);
+        const float x = rowx(i, b, lane_ok);
         const float2 pr = S_prm(a)[i];
         const float hp = S_st0(a)[i * PS + b];
-        const int j = S_inp(a)[i];
+        int j = S_inp(a)[i];
+        if (j >= 0 && !CK_IN(a.err, j, a.rows_cap)) j = -1;
         const float dv = S_st1(a)[(j < 0 ? 0 : j) * Bp + bl];
         const float dr = lane_ok && j >= 0 && live ? dv : 0.f;
-        if (i == 0 && c.glob && lane_ok) x += global_carry(a, c, b, phase_id);
         const float av = x + pr.y + dr;
         const float th = tanhf(av);
         const float hv = live ? fmaf(pr.x, th, (1.f - pr.x) * hp) : 0.f;
@@ -901,9 +942,9 @@ __device__ __forceinline__ void finish_fwd_narrow(const KArgs &a, const Cta &c, 
     if (sh && warp == U - 1) row(0);
 }
 
-template <int THREADS>
+template <int THREADS, class RowX>
 __device__ __forceinline__ void finish_bwd_narrow(const KArgs &a, const Cta &c, int s,
-                                                  unsigned phase_id) {
+                                                  RowX &&rowx) {
     constexpr int U = THREADS / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Bp = a.Bp, B = a.B, M = a.M, PS = Bp + 1;
@@ -917,12 +958,10 @@ __device__ __forceinline__ void finish_bwd_narrow(const KArgs &a, const Cta &c, 
     const int b = lane_ok ? lane : 0, bl = live ? lane : B - 1;
     const int sh = c.glob ? 1 : 0;
     auto row = [&](int i) {
-        float x = row_sum1(a, c, i, b);
+        const float x = pro ? 0.f : rowx(i, b, lane_ok);
         const float lam = S_prm(a)[i].x;
         const int o = i * Bp + b;
         const float g0 = S_st0(a)[o], o0 = S_st3(a)[i * PS + bl], p0 = S_st1(a)[o], h0 = S_st2(a)[o];
-        x = pro ? 0.f : x;
-        if (!pro && i == 0 && c.glob && lane_ok) x += global_carry(a, c, b, phase_id);
         const float gv = pro ? 0.f : g0;
         const float ov = step_end && live ? o0 : 0.f;
         const float p = q >= 0 ? p0 : 0.f, hv = q >= 0 ? h0 : 0.f;
@@ -936,7 +975,7 @@ __device__ __forceinline__ void finish_bwd_narrow(const KArgs &a, const Cta &c, 
             dl = fmaf(gn, p - hv, dl);
             db += d;
             const int sl = S_sslot(a)[i];
-            if (sl >= 0) {
+            if (sl >= 0 && CK_IN(a.err, sl, a.n_in)) {
                 float *dd = a.ddrives + ((size_t)tq * a.n_in + sl) * B + lane;
                 *dd = step_end ? d : *dd + d;
             }
@@ -953,7 +992,11 @@ __device__ __forceinline__ void finish_bwd_narrow(const KArgs &a, const Cta &c, 
 template <int THREADS>
 __device__ void finish_fwd(const KArgs &a, const Cta &c, const PB &pb, int s, unsigned phase_id) {
     if (a.Bp <= 32 && c.stage && a.rs_smem) {
-        finish_fwd_narrow<THREADS>(a, c, s, phase_id);
+        finish_fwd_narrow<THREADS>(a, c, s, [&](int i, int b, bool lane_ok) {
+            float x = row_sum1(a, c, i, b);
+            if (i == 0 && c.glob && lane_ok) x += global_carry(a, c, b, phase_id);
+            return x;
+        });
         return;
     }
     constexpr int U = THREADS / 32;
@@ -1054,7 +1097,7 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
                 dl[el] = fmaf(gn[el], p[el] - hv[el], dl[el]);
                 db[el] += d;
                 const int sl = S_sslot(a)[ii[el]];
-                if (sl >= 0) {
+                if (sl >= 0 && CK_IN(a.err, sl, a.n_in)) {
                     float *dd = a.ddrives + ((size_t)tq * a.n_in + sl) * B + bb[el];
                     *dd = first ? d : *dd + d;
                 }
@@ -1089,7 +1132,11 @@ __device__ __forceinline__ void finish_bwd_batch(const KArgs &a, const Cta &c, c
 template <int THREADS>
 __device__ void finish_bwd(const KArgs &a, const Cta &c, const PB &pb, int s, unsigned phase_id) {
     if (a.Bp <= 32 && c.stage && a.rs_smem) {
-        finish_bwd_narrow<THREADS>(a, c, s, phase_id);
+        finish_bwd_narrow<THREADS>(a, c, s, [&](int i, int b, bool lane_ok) {
+            float x = row_sum1(a, c, i, b);
+            if (i == 0 && c.glob && lane_ok) x += global_carry(a, c, b, phase_id);
+            return x;
+        });
         return;
     }
     constexpr int U = THREADS / 32;
@@ -1141,6 +1188,8 @@ __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a)
     Cta c;
     c.stage = a.stage != 0;
 
+    // bounds-checked build, test hook: one index out of range, never used
+    if (a.bounds_probe && cta == 0 && tid == 0) (void)CK_IN(a.err, a.N, a.N);
     // ---- this CTA's piece of the merge path of (row ends, edges), computed
     // when the graph was built
     if (tid < 6) s_meta[tid] = __ldg(a.piece + (size_t)cta * kPieceInts + tid);
@@ -1153,7 +1202,9 @@ __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a)
     c.publish = s_meta[5] != 0;
     c.glob = c.c_lo < cta && c.nrows > 0;
     c.rows = a.rs_smem ? reinterpret_cast<float *>(ck_smem + a.o_rows) : a.rowsum_g + (size_t)c.r0 * Bp;
-    if (c.nrows + 2 > a.rows_cap || (SMEMG && c.e1 - c.e0 > a.cap)) {
+    if (c.nrows + 2 > a.rows_cap || (SMEMG && c.e1 - c.e0 > a.cap) ||
+        !CK_IN(a.err, c.r0 + c.nrows, a.N + 1) || !CK_IN(a.err, c.e1, a.E + 1) ||
+        !CK_IN(a.err, c.e0, c.e1 + 1)) {
         if (tid == 0) atomicCAS(a.err, 0, kDevInternal);
         return;  // every other CTA sees the error word at its next wait
     }
@@ -1188,9 +1239,11 @@ __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int k = kb + j * THREADS;
-                const int kc = k < c.e1 ? k : c.e0;  // a valid edge, result unused
+                int kc = k < c.e1 ? k : c.e0;  // a valid edge, result unused
+                if (!CK_IN(a.err, kc, a.E)) kc = 0;
                 pm[j] = __ldg(a.perm + kc);
                 cl[j] = SMEMG ? __ldg(a.col + kc) : 0;
+                if (!CK_IN(a.err, pm[j], a.E)) pm[j] = 0;
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -1363,13 +1416,393 @@ __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a)
                 for (int j = 0; j < 8; ++j) {
                     const int k = kb + j * THREADS;
                     pm[j] = __ldg(a.perm + (k < c.e1 ? k : c.e0));
+                    if (k < c.e1 && !CK_IN(a.err, pm[j], a.E)) pm[j] = -1;
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int k = kb + j * THREADS;
-                    if (k < c.e1) a.dw[pm[j]] = SMEMG ? S_sdw(a)[k - c.e0] : a.dwperm[k];
+                    if (k < c.e1 && pm[j] >= 0) a.dw[pm[j]] = SMEMG ? S_sdw(a)[k - c.e0] : a.dwperm[k];
                 }
             }
+        }
+    }
+}
+
+// ------------------------------------------------------------ tiled kernels
+//
+// For graphs whose state rows fit a few CTAs' shared memory (chosen when the
+// graph is built, ck::Tiled): the column nodes are cut into C chunks and the
+// rows into G blocks, and CTA t = g * C + j (one per SM) owns cell (g, j) --
+// the edges of block g whose column lies in chunk j.  Each microstep a CTA
+// copies chunk j of the gathered rows (the state forward, d(pre-activation)
+// backward) from global memory into shared memory with bulk asynchronous
+// copies, then walks its cell exactly like part A above but gathers from
+// shared memory: every gathered row is read from L2 once per CTA of its
+// chunk's group, not once per edge.  The C CTAs of a block then exchange their
+// partial row totals: each publishes, as {value, microstep id} words, the
+// totals of the block rows the others finish, and finishes its own share of
+// the block's rows with the C partials summed in chunk order (a fixed order:
+// results do not depend on timing).
+
+__device__ __forceinline__ unsigned smem_u32(const void *p) {
+    return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(unsigned long long *m, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(m)), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long *m, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(m)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long *m, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(m)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global to this CTA's shared memory, completing on mbarrier m.
+__device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, unsigned bytes,
+                                         unsigned long long *m) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(m))
+        : "memory");
+}
+// Order this thread's view of memory written by other CTAs (made visible by
+// an acquire) before its asynchronous-proxy copies, and the CTA's generic reads
+// of shared memory before the copies overwrite it.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Wait, bounded by a.timeout_ns, for phase `parity` of mbarrier m.  Every
+// thread may call it.  The copies it waits for always complete; the bound
+// only guards against a fault elsewhere.
+__device__ __forceinline__ bool mbar_wait(const KArgs &a, unsigned long long *m, unsigned parity) {
+    if (mbar_try_wait(m, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(m, parity)) {
+        if (globaltimer() - t0 > a.timeout_ns) {
+            atomicCAS(a.err, 0, kDevTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Issue (thread 0) the copy of `rows` rows of Bp floats from gsrc into sdst,
+// in pieces of at most 32 KB; returns the bytes.
+__device__ __forceinline__ unsigned bulk_rows(float *sdst, const float *gsrc, int rows, int Bp,
+                                              unsigned long long *m) {
+    const unsigned total = (unsigned)rows * (unsigned)Bp * 4u;
+    constexpr unsigned kPiece = 32u << 10;
+    for (unsigned o = 0; o < total; o += kPiece) {
+        const unsigned n = total - o < kPiece ? total - o : kPiece;
+        bulk_g2s(reinterpret_cast<char *>(sdst) + o, reinterpret_cast<const char *>(gsrc) + o, n, m);
+    }
+    return total;
+}
+
+// Partial total of block row li (block-relative) in column b published by
+// CTA t of this block, waited for (bounded) until its microstep id matches.
+__device__ __forceinline__ const unsigned long long *xword(const KArgs &a, int t, int li, int b) {
+    return a.xbuf + ((size_t)t * a.xrows + li) * a.Bp + b;
+}
+
+template <int THREADS, bool SMEMG, bool BWD>
+__global__ void __launch_bounds__(THREADS, 1) tiled_kernel(const KArgs a) {
+    constexpr int NC = 1;
+    constexpr int UNR = BWD ? 8 : 4;
+    __shared__ int s_ok, s_meta[16];
+    __shared__ __align__(8) unsigned long long s_mbar;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cta = blockIdx.x;
+    const int N = a.N, Bp = a.Bp;
+    const int g = lane / a.LPE, lig = lane - (lane / a.LPE) * a.LPE;
+    const bool active = g < a.EPW;
+    const int gam = warp * a.EPW + g;
+
+    if (a.bounds_probe && cta == 0 && tid == 0) (void)CK_IN(a.err, a.N, a.N);
+    if (tid < kTileInts) s_meta[tid] = __ldg(a.tmeta + (size_t)cta * kTileInts + tid);
+    if (tid == 0) mbar_init(&s_mbar, 1);
+    __syncthreads();
+    // cb: the block (part A); cf: the rows this CTA finishes
+    Cta cb, cf;
+    cb.r0 = s_meta[0];
+    cb.nrows = s_meta[1];
+    cb.e0 = s_meta[2];
+    cb.e1 = s_meta[3];
+    cb.c_lo = cta;
+    cb.publish = false;
+    cb.glob = false;
+    cb.stage = true;
+    cb.n_inp = 0;
+    const int cn0 = s_meta[4], cnr = s_meta[5], poff = s_meta[6], f0 = s_meta[7], f1 = s_meta[8];
+    const int cj = s_meta[9], cgb = s_meta[10];
+    cb.rows = a.rs_smem ? reinterpret_cast<float *>(ck_smem + a.o_rows)
+                        : a.rowsum_g + (size_t)cta * a.rows_cap * Bp;
+    cf = cb;
+    cf.r0 = cb.r0 + f0;
+    cf.nrows = f1 - f0;
+    if (cb.nrows + 2 > a.rows_cap || cf.nrows > a.fin_cap || f0 < 0 || f1 > cb.nrows ||
+        cnr > a.chunk_cap || cnr < 0 || (SMEMG && cb.e1 - cb.e0 > a.cap) ||
+        !CK_IN(a.err, cb.r0 + cb.nrows, a.N + 1) || !CK_IN(a.err, cn0 + cnr, a.N + 1) ||
+        !CK_IN(a.err, cb.e1, a.E + 1) || !CK_IN(a.err, cb.e0, cb.e1 + 1) ||
+        !CK_IN(a.err, cj, a.tC) || !CK_IN(a.err, cgb * a.tC + cj, a.P)) {
+        if (tid == 0) atomicCAS(a.err, 0, kDevInternal);
+        return;  // every other CTA sees the error word at its next wait
+    }
+    // ---- part A tables (block rows), from the cell's row pointers
+    for (int i = tid; i < cb.nrows + 2; i += THREADS)
+        S_srp(a)[i] = __ldg(a.tptr + poff + min(i, cb.nrows));
+    for (int i = tid; i < cb.nrows; i += THREADS) {
+        const int rs = __ldg(a.tptr + poff + i), re = __ldg(a.tptr + poff + i + 1);
+        int2 gr = make_int2(-1, 0);
+        if (re > rs) {
+            const int ga = group_of(cb, a.G, rs);
+            const int gb = group_of(cb, a.G, re - 1);
+            gr = make_int2((ga << 16) | gb, next_warp_group(a, ga));
+        }
+        S_sgrp(a)[i] = gr;
+    }
+    for (int gi = tid; gi < a.G; gi += THREADS) {
+        const int n = cb.e1 - cb.e0;
+        const int k0 = cb.e0 + (int)((long long)gi * n / a.G);
+        S_gst(a)[gi] = k0 < cb.e1 ? __ldg(a.rowid + k0) : -1;
+    }
+    // ---- finish tables (this CTA's rows)
+    for (int i = tid; i < cf.nrows; i += THREADS) {
+        const int r = cf.r0 + i;
+        S_prm(a)[i] = make_float2(__ldg(a.leak + r), BWD ? 0.f : __ldg(a.bias + r));
+        S_sslot(a)[i] = __ldg(a.slot + r);
+    }
+    // ---- the cell's edges: {column in chunk, w[perm[k]]} in shared memory, or
+    // the permuted values in scratch (streamed)
+    if (SMEMG || a.init_w) {
+        for (int kb = cb.e0 + tid; kb < cb.e1; kb += 8 * THREADS) {
+            int pm[8], cl[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int k = kb + j * THREADS;
+                int kc = k < cb.e1 ? k : cb.e0;
+                if (!CK_IN(a.err, kc, a.E)) kc = 0;
+                pm[j] = __ldg(a.perm + kc);
+                cl[j] = SMEMG ? __ldg(a.col + kc) : 0;
+                if (!CK_IN(a.err, pm[j], a.E)) pm[j] = 0;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int k = kb + j * THREADS;
+                const float wv = __ldg(a.w + pm[j]);
+                if (k >= cb.e1) continue;
+                if (SMEMG) {
+                    S_scw(a)[k - cb.e0] = make_int2(cl[j], __float_as_int(wv));
+                    if (BWD) S_sdw(a)[k - cb.e0] = 0.f;
+                } else {
+                    a.wperm[k] = wv;
+                    if (BWD && a.zero_dw) a.dwperm[k] = 0.f;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (!BWD) {
+        if (tid == 0) {
+            int n = 0;
+            for (int i = 0; i < cf.nrows; ++i) S_inp(a)[i] = S_sslot(a)[i] >= 0 ? n++ : -1;
+            s_meta[12] = n;
+        }
+        __syncthreads();
+        cf.n_inp = s_meta[12];
+    }
+
+    // ---- the row total x of finished row i (relative to cf.r0), column b:
+    // the C chunks' partials in chunk order, this CTA's own from its row slots
+    auto tiled_x = [&](unsigned phase_id) {
+        return [&a, &cb, f0, cj, cgb, phase_id](int i, int b, bool lane_ok) -> float {
+            if (!lane_ok) return 0.f;
+            const int li = f0 + i;
+            unsigned long long w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < a.tC && j != cj) w[j] = ld_relaxed64(xword(a, cgb * a.tC + j, li, b));
+            float x = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= a.tC) break;
+                if (j == cj) {
+                    x += row_sum1(a, cb, li, b);
+                } else if ((unsigned)(w[j] >> 32) == phase_id) {
+                    x += __uint_as_float((unsigned)w[j]);
+                } else {
+                    x += wait_carry(a, xword(a, cgb * a.tC + j, li, b), phase_id);
+                }
+            }
+            return x;
+        };
+    };
+    // finish operands of microstep s for this CTA's rows, copied into shared
+    // memory (cp.async) while other CTAs finish
+    auto stage_for = [&](int s, int t0, int nt) {
+        const size_t ro = (size_t)cf.r0 * Bp;
+        if (BWD) {
+            if (s > 0) {
+                const int q = s - 1, tq = q / a.M;
+                stage_rows(S_st1(a), prow(a, q) + ro, cf.nrows, Bp, t0, nt);
+                stage_rows(S_st2(a), hrow(a, q) + ro, cf.nrows, Bp, t0, nt);
+                if (q - tq * a.M == a.M - 1) stage_dout(a, cf, tq, t0, nt);
+            }
+        } else if (cf.n_inp > 0 && s % a.M == 0) {
+            const int t = s / a.M;
+            for (int j = t0; j < cf.nrows * a.B; j += nt) {
+                const int i = j / a.B, b = j - i * a.B;
+                const int ii = S_inp(a)[i];
+                if (ii >= 0)
+                    cp_async4(S_st1(a) + (size_t)ii * Bp + b,
+                              a.drives + ((size_t)t * a.n_in + S_sslot(a)[i]) * a.B + b);
+            }
+        }
+        cp_async_commit();
+    };
+
+    unsigned nbar = 0;
+    if (!BWD) {
+        if (a.do_prologue) {
+            to_rows<THREADS>(hrow(a, 0), a.state0, cf.r0, cf.r0 + cf.nrows, a.B, Bp, N, S_tile(a));
+            for (int j = tid; j < cf.nrows * Bp; j += THREADS) {
+                const float v = __ldcg(hrow(a, 0) + (size_t)cf.r0 * Bp + j);
+                const int i = j / Bp, b = j - i * Bp;
+                S_st0(a)[i * pstride(a) + b] = v;
+                if (a.ckpt) a.ckpt[(size_t)cf.r0 * Bp + j] = v;
+            }
+            if (!grid_sync(a, nbar++, &s_ok)) return;
+        } else {
+            // a window that starts from a state already in H: it becomes the resident state
+            for (int j = tid; j < cf.nrows * Bp; j += THREADS) {
+                const int i = j / Bp, b = j - i * Bp;
+                S_st0(a)[i * pstride(a) + b] = __ldcg(hrow(a, a.s_first) + (size_t)cf.r0 * Bp + j);
+            }
+            __syncthreads();
+        }
+    } else {
+        if (a.do_prologue) {
+            const size_t ro = (size_t)cf.r0 * Bp;
+            stage_rows(S_st1(a), prow(a, a.S - 1) + ro, cf.nrows, Bp, tid, THREADS);
+            stage_rows(S_st2(a), hrow(a, a.S - 1) + ro, cf.nrows, Bp, tid, THREADS);
+            stage_dout(a, cf, a.T - 1, tid, THREADS);
+            cp_async_wait_all();
+            __syncthreads();
+            finish_bwd_narrow<THREADS>(a, cf, a.S, [](int, int, bool) { return 0.f; });
+            if (!grid_sync(a, nbar++, &s_ok)) return;
+        } else {
+            // a window that continues a backward: G and the per-lane sums from scratch
+            for (int j = tid; j < cf.nrows * Bp; j += THREADS)
+                S_st0(a)[j] = __ldcg(a.G_ + (size_t)cf.r0 * Bp + j);
+            for (int j = tid; j < cf.nrows * 32; j += THREADS)
+                S_acc(a)[j] = a.lacc[(size_t)cf.r0 * 32 + j];
+            __syncthreads();
+        }
+    }
+    if (a.s_count > 0) stage_for(a.s_first, tid, THREADS);
+
+    for (int it = 0; it < a.s_count; ++it) {
+        const int s = BWD ? a.s_first - it : a.s_first + it;
+        const unsigned phase_id = BWD ? (unsigned)(a.S - s) : (unsigned)(s + 1);
+        // ---- the chunk of gathered rows (and, backward, the block's rows of
+        // the state entering microstep s) into shared memory
+        if (tid == 0) {
+            fence_proxy_async();
+            const float *table = BWD ? a.da + (size_t)(s & 1) * N * Bp : hrow(a, s);
+            const int hr = BWD ? min(cb.nrows + 1, N - cb.r0) : 0;
+            const unsigned bytes = (unsigned)(cnr + hr) * (unsigned)Bp * 4u;
+            mbar_expect_tx(&s_mbar, bytes);
+            if (cnr > 0) bulk_rows(S_chunk(a), table + (size_t)cn0 * Bp, cnr, Bp, &s_mbar);
+            if (hr > 0) bulk_rows(S_st4(a), hrow(a, s) + (size_t)cb.r0 * Bp, hr, Bp, &s_mbar);
+        }
+        if (!mbar_wait(a, &s_mbar, (unsigned)(it & 1))) {
+            cp_async_wait_all();
+            mbar_wait(a, &s_mbar, (unsigned)(it & 1));  // its copies, once more, before leaving
+            return;
+        }
+        // ---- part A over the cell
+        stream_piece<NC, SMEMG, BWD, UNR, BWD, true>(a, cb, gam, lig, active, nullptr, hrow(a, s));
+        cp_async_wait_all();
+        __syncthreads();
+        // ---- publish the totals of the block rows the other CTAs finish
+        for (int e = tid; e < cb.nrows * Bp; e += THREADS) {
+            const int li = e / Bp, b = e - li * Bp;
+            if (li >= f0 && li < f1) continue;
+            const float x = row_sum1(a, cb, li, b);
+            st_relaxed64(const_cast<unsigned long long *>(xword(a, cta, li, b)),
+                         ((unsigned long long)phase_id << 32) | __float_as_uint(x));
+        }
+        // ---- finish this CTA's rows
+        if (BWD) finish_bwd_narrow<THREADS>(a, cf, s, tiled_x(phase_id));
+        else finish_fwd_narrow<THREADS>(a, cf, s, tiled_x(phase_id));
+        if (it + 1 < a.s_count) {
+            auto between = [&]() {
+                if (!BWD && s % a.M == a.M - 1) write_out(a, cf, s / a.M, tid, THREADS);
+                stage_for(BWD ? s - 1 : s + 1, tid, THREADS);
+            };
+            if (!grid_sync(a, nbar++, &s_ok, between)) {
+                cp_async_wait_all();
+                return;
+            }
+        }
+    }
+
+    __syncthreads();
+    if (!BWD) {
+        // the state that ends an input step, if the launch's last microstep ends one
+        const int s_last = a.s_first + a.s_count - 1;
+        if (a.s_count > 0 && s_last % a.M == a.M - 1) write_out(a, cf, s_last / a.M, tid, THREADS);
+        return;
+    }
+    if (!a.do_epilogue) {
+        // a window that a later one continues: G and the per-lane sums to scratch
+        for (int j = tid; j < cf.nrows * Bp; j += THREADS) a.G_[(size_t)cf.r0 * Bp + j] = S_st0(a)[j];
+        for (int j = tid; j < cf.nrows * 32; j += THREADS) a.lacc[(size_t)cf.r0 * 32 + j] = S_acc(a)[j];
+        if (SMEMG)
+            for (int k = cb.e0 + tid; k < cb.e1; k += THREADS) a.dwperm[k] = S_sdw(a)[k - cb.e0];
+        return;
+    }
+    for (int j = tid; j < cf.nrows * Bp; j += THREADS) a.G_[(size_t)cf.r0 * Bp + j] = S_st0(a)[j];
+    __syncthreads();
+    for (int i = warp; i < cf.nrows; i += THREADS / 32) {
+        float2 v = S_acc(a)[i * 32 + lane];
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            v.x += __shfl_xor_sync(kFull, v.x, m);
+            v.y += __shfl_xor_sync(kFull, v.y, m);
+        }
+        if (lane == 0) {
+            a.dleak[cf.r0 + i] = v.x;
+            a.dbias[cf.r0 + i] = v.y;
+        }
+    }
+    from_rows<THREADS>(a.dstate0, a.G_, cf.r0, cf.r0 + cf.nrows, a.B, Bp, N, S_tile(a));
+    // dw back to the caller's edge order
+    for (int kb = cb.e0 + tid; kb < cb.e1; kb += 8 * THREADS) {
+        int pm[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int k = kb + j * THREADS;
+            pm[j] = __ldg(a.perm + (k < cb.e1 ? k : cb.e0));
+            if (k < cb.e1 && !CK_IN(a.err, pm[j], a.E)) pm[j] = -1;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int k = kb + j * THREADS;
+            if (k < cb.e1 && pm[j] >= 0) a.dw[pm[j]] = SMEMG ? S_sdw(a)[k - cb.e0] : a.dwperm[k];
         }
     }
 }
@@ -1388,6 +1821,21 @@ KernelFn pick_kernel(int nc, bool smem, bool bwd) {
     return bwd ? pick_nc<kThreads, true>(nc, smem) : pick_nc<kThreads, false>(nc, smem);
 }
 
+KernelFn pick_tiled(bool smem, bool bwd) {
+    if (bwd) return smem ? tiled_kernel<kTiledThreads, true, true> : tiled_kernel<kTiledThreads, false, true>;
+    return smem ? tiled_kernel<kTiledThreads, true, false> : tiled_kernel<kTiledThreads, false, false>;
+}
+
+// The kernel, grid and block of one direction's launch under plan p.
+struct LaunchShape {
+    KernelFn fn;
+    int grid, block, per_sm;
+};
+LaunchShape launch_shape(const Plan &p, const SmemLayout &L, bool bwd) {
+    if (p.tiled) return {pick_tiled(L.graph, bwd), p.tP[bwd ? 1 : 0], kTiledThreads, 1};
+    return {pick_kernel(p.NC, L.graph, bwd), p.P, p.threads, kCtasPerSm};
+}
+
 int pow2ceil(int x) {
     int p = 1;
     while (p < x) p <<= 1;
@@ -1398,7 +1846,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
 // Shared-memory layout of one direction.
-SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage) {
+SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage,
+                       bool want_rows = true) {
     SmemLayout L;
     std::memset(&L, 0, sizeof(L));
     size_t o = 0;
@@ -1418,7 +1867,7 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     // finish operands: forward state + drives; backward G, A, H, dOut + two sums
     const size_t stage_b = (dir == 0 ? 1 : 4) * rows_b + rows_pb + (dir == 1 ? 8 * 32 * (size_t)rc : 0) +
                            align16(4 * (size_t)rc);
-    L.rows = o + rows_b <= budget;
+    L.rows = want_rows && o + rows_b <= budget;
     if (L.rows) o += rows_b;
     L.o_rows = (int)(o - (L.rows ? rows_b : 0));
     L.graph = want_graph && o + graph_b <= budget;
@@ -1434,6 +1883,51 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage)
     L.o_st4 = (int)o; o += dir == 1 ? sb : 0;
     L.o_acc = (int)o; o = align16(o + (L.stage && dir == 1 ? 8 * 32 * (size_t)rc : 0));
     L.o_inp = (int)o; o = align16(o + (L.stage ? 4 * (size_t)rc : 0));
+    L.bytes = o;
+    return L;
+}
+
+// Shared-memory layout of a tiled kernel (one CTA per SM).  Required: the
+// chunk of gathered rows and, backward, the block's rows of the state (both
+// bulk-copy destinations, 128-byte aligned), the part A tables, the finish
+// tables and staged operands of the rows the CTA finishes.  Then, if they fit:
+// the row slots (else in scratch) and the cell's graph slice (else streamed).
+// `fits` is false when the required part exceeds the budget.
+constexpr size_t kTiledBudget = (size_t)kMaxSmem - 512;  // static shared memory below 512 bytes
+
+SmemLayout tiled_layout(int dir, int Bp, int groups, int rows_cap, int fin_cap, int chunk_cap,
+                        int ecap, bool want_graph, bool want_rows, bool *fits) {
+    SmemLayout L;
+    std::memset(&L, 0, sizeof(L));
+    auto a128 = [](size_t x) { return (x + 127) & ~(size_t)127; };
+    size_t o = 0;
+    L.o_chunk = (int)o; o = a128(o + 4 * (size_t)chunk_cap * Bp);
+    L.o_st4 = (int)o; o = a128(o + (dir == 1 ? 4 * (size_t)rows_cap * Bp : 0));
+    L.o_srp = (int)o; o = align16(o + 4 * (size_t)rows_cap);
+    L.o_grp = (int)o; o = align16(o + 8 * (size_t)rows_cap);
+    L.o_gst = (int)o; o = align16(o + 4 * (size_t)groups);
+    L.o_carry = (int)o; o = align16(o + 4 * (size_t)groups * Bp);
+    L.o_tile = (int)o; o = align16(o + 4 * 32 * 33);
+    const size_t F = (size_t)fin_cap + 1;
+    L.o_prm = (int)o; o = align16(o + 8 * F);
+    L.o_slot = (int)o; o = align16(o + 4 * F);
+    L.o_inp = (int)o; o = align16(o + (dir == 0 ? 4 * F : 0));
+    const size_t fr = align16(4 * F * Bp), frp = align16(4 * F * (Bp + 1));
+    L.o_st0 = (int)o; o += dir == 0 ? frp : fr;
+    L.o_st1 = (int)o; o += fr;
+    L.o_st2 = (int)o; o += dir == 1 ? fr : 0;
+    L.o_st3 = (int)o; o += dir == 1 ? frp : 0;
+    L.o_acc = (int)o; o = align16(o + (dir == 1 ? 8 * 32 * F : 0));
+    L.stage = true;
+    *fits = o <= kTiledBudget;
+    const size_t rows_b = align16(4 * (size_t)rows_cap * Bp);
+    L.rows = want_rows && o + rows_b <= kTiledBudget;
+    L.o_rows = (int)o;
+    if (L.rows) o += rows_b;
+    const size_t graph_b = align16(8 * (size_t)ecap) + (dir == 1 ? align16(4 * (size_t)ecap) : 0);
+    L.graph = want_graph && o + graph_b <= kTiledBudget;
+    L.o_cw = (int)o; o = align16(o + (L.graph ? 8 * (size_t)ecap : 0));
+    L.o_dw = (int)o; o = align16(o + (L.graph && dir == 1 ? 4 * (size_t)ecap : 0));
     L.bytes = o;
     return L;
 }
@@ -1478,48 +1972,80 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.o_acc = L.o_acc;
     k.slot = g->slot;
     char *sc = (char *)scratch;
+    auto region = [&](size_t off) -> char * { return off == kNoRegion ? nullptr : sc + off; };
     k.bar = (unsigned *)(sc + p.off_ctrl);
     k.err = (int *)(sc + p.off_ctrl + kStatusOffset);
-    k.carry = (unsigned long long *)(sc + p.off_carry);
-    k.wperm = (float *)(sc + p.off_wperm);
-    k.dwperm = (float *)(sc + p.off_dwperm);
-    k.G_ = (float *)(sc + p.off_G);
-    k.da = (float *)(sc + p.off_da);
-    k.rowsum_g = (float *)(sc + p.off_rowsum);
-    k.lacc = (float2 *)(sc + p.off_lacc);
+    k.carry = (unsigned long long *)region(p.off_carry);
+    k.wperm = (float *)region(p.off_wperm);
+    k.dwperm = (float *)region(p.off_dwperm);
+    k.G_ = (float *)region(p.off_G);
+    k.da = (float *)region(p.off_da);
+    k.rowsum_g = (float *)region(p.off_rowsum);
+    k.lacc = (float2 *)region(p.off_lacc);
     k.bar_extra = (unsigned)options().barrier_extra;
     k.timeout_ns = (unsigned long long)options().timeout_ns;
+    k.bounds_probe = options().bounds_probe;
+    k.o_chunk = L.o_chunk;
+    if (p.tiled) {
+        const Tiled &t = g->tiled[dir];
+        k.P = p.tP[dir];
+        k.tmeta = t.meta;
+        k.tptr = t.ptr;
+        k.chunk_cap = p.chunk_cap[dir];
+        k.fin_cap = p.fin_cap[dir];
+        k.tC = t.C;
+        k.xrows = p.xrows;
+        k.xbuf = (unsigned long long *)region(p.off_xbuf);
+    }
+}
+
+// The graph arrays of direction dir: the compressed rows (and their pieces),
+// or the tiling's cells.
+void set_graph(KArgs &k, const ck_graph *g, const Plan &p, int dir) {
+    if (p.tiled) {
+        const Tiled &t = g->tiled[dir];
+        k.col = t.col;
+        k.perm = t.perm;
+        k.rowid = t.rowid;
+        return;
+    }
+    k.row_ptr = dir == 0 ? g->row_ptr : g->rowT_ptr;
+    k.piece = g->piece[dir][pass_index(p.Bp)];
+    k.col = dir == 0 ? g->col : g->colT;
+    k.perm = dir == 0 ? g->perm : g->permT;
+    k.rowid = dir == 0 ? g->rowid : g->rowidT;
 }
 
 // One cooperative launch of the kernel for layout L with k's microstep range
 // and flags as given; the control words are cleared first.
 ck_status launch_once(KArgs &k, const Plan &p, const SmemLayout &L, bool bwd, cudaStream_t s) {
-    KernelFn fn = pick_kernel(p.NC, L.graph, bwd);
-    cudaError_t e = cudaFuncSetAttribute((const void *)fn,
+    const LaunchShape sh = launch_shape(p, L, bwd);
+    cudaError_t e = cudaFuncSetAttribute((const void *)sh.fn,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-    e = cudaMemsetAsync((char *)k.bar, 0, p.off_carry - p.off_ctrl + 8 * (size_t)p.P * p.Bp, s);
+    e = cudaMemsetAsync((char *)k.bar, 0, p.clear_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (control words)");
     void *args[] = {&k};
-    e = cudaLaunchCooperativeKernel((const void *)fn, dim3(p.P), dim3(p.threads), args, L.bytes, s);
+    e = cudaLaunchCooperativeKernel((const void *)sh.fn, dim3(sh.grid), dim3(sh.block), args, L.bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
     return CK_OK;
 }
 
 ck_status launch_all(KArgs &k, const Plan &p, bool bwd, cudaStream_t s, int64_t *launches) {
     const SmemLayout &L = bwd ? p.lay_bwd : p.lay_fwd;
-    KernelFn fn = pick_kernel(p.NC, L.graph, bwd);
+    const LaunchShape sh = launch_shape(p, L, bwd);
+    KernelFn fn = sh.fn;
     cudaError_t e = cudaFuncSetAttribute((const void *)fn,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)fn, p.threads, L.bytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)fn, sh.block, L.bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    if (per_sm < kCtasPerSm)
+    if (per_sm < sh.per_sm)
         return fail(CK_ERR_UNSUPPORTED, "%d CTAs of %d threads and %zu B shared do not fit on an SM",
-                    kCtasPerSm, p.threads, L.bytes);
-    // barrier counter, status word and published carries start at zero
-    e = cudaMemsetAsync((char *)k.bar, 0, p.off_carry - p.off_ctrl + 8 * (size_t)p.P * p.Bp, s);
+                    sh.per_sm, sh.block, L.bytes);
+    // barrier counter, status word, published carries and partial totals start at zero
+    e = cudaMemsetAsync((char *)k.bar, 0, p.clear_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (control words)");
     int64_t n = 0;
     const bool persistent = options().persistent != 0;
@@ -1542,7 +2068,7 @@ ck_status launch_all(KArgs &k, const Plan &p, bool bwd, cudaStream_t s, int64_t 
             ki.bar_base = i == 0 ? 0u : 1u;
         }
         void *args[] = {&ki};
-        e = cudaLaunchCooperativeKernel((const void *)fn, dim3(p.P), dim3(p.threads), args, L.bytes,
+        e = cudaLaunchCooperativeKernel((const void *)fn, dim3(sh.grid), dim3(sh.block), args, L.bytes,
                                         s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
         ++n;
@@ -1552,6 +2078,14 @@ ck_status launch_all(KArgs &k, const Plan &p, bool bwd, cudaStream_t s, int64_t 
 }
 
 }  // namespace
+
+bool tiled_fits(int dir, int Bp, int max_rows, int max_fin, int max_chunk) {
+    const int lpe = Bp / 4, epw = 32 / lpe;
+    bool fits = false;
+    tiled_layout(dir, Bp, (kTiledThreads / 32) * epw, max_rows + 3, max_fin, max_chunk, 0, false,
+                 false, &fits);
+    return fits;
+}
 
 ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p) {
     if (B < 1 || T < 1 || M < 1) return fail(CK_ERR_INVALID_ARG, "B, T and microsteps must be >= 1");
@@ -1581,14 +2115,50 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     }
     const bool want_graph = options().graph_in_smem && options().persistent;
     const bool want_stage = options().persistent != 0;
-    q.lay_fwd = smem_layout(q, 0, want_graph, want_stage);
-    q.lay_bwd = smem_layout(q, 1, want_graph, want_stage);
-    // the recomputing backward runs in windows of K input steps (one launch
-    // each), every accumulator in global memory
-    q.lay_bwd_flat = smem_layout(q, 1, false, false);
-    const size_t cta_smem = std::min<size_t>(kMaxSmem, kSmemPerSm / kCtasPerSm - 1024) - kStaticSmem;
-    if (q.lay_fwd.bytes > cta_smem || q.lay_bwd.bytes > cta_smem || q.lay_bwd_flat.bytes > cta_smem)
-        return fail(CK_ERR_UNSUPPORTED, "per-CTA tables exceed shared memory (rows per SM too many)");
+    const bool want_rows = options().rows_in_smem != 0;
+    // tiled kernels: a tiling in both directions and at most 32 padded columns
+    q.tiled = options().tiled && g->tiled[0].C > 0 && g->tiled[1].C > 0 && B <= kTiledMaxBp;
+    if (q.tiled) {
+        q.Bp = (int)((B + 3) / 4 * 4);
+        q.NC = 1;
+        q.LPE = q.Bp / 4;
+        q.EPW = 32 / q.LPE;
+        q.threads = kTiledThreads;
+        q.warps = q.threads / 32;
+        q.groups = q.warps * q.EPW;
+        q.xrows = 0;
+        q.P = 0;
+        bool ok = true;
+        for (int d = 0; d < 2; ++d) {
+            const Tiled &t = g->tiled[d];
+            q.tP[d] = t.P;
+            q.P = std::max(q.P, t.P);
+            q.cap[d] = t.max_edges + 1;
+            q.rows_cap[d] = t.max_rows + 3;
+            q.fin_cap[d] = t.max_fin;
+            q.chunk_cap[d] = t.max_chunk;
+            q.xrows = std::max(q.xrows, t.max_rows);
+        }
+        bool f0 = false, f1 = false, f2 = false;
+        // the graph slice stays in global memory with one launch per microstep, as above
+        q.lay_fwd = tiled_layout(0, q.Bp, q.groups, q.rows_cap[0], q.fin_cap[0], q.chunk_cap[0],
+                                 q.cap[0], want_graph, want_rows, &f0);
+        q.lay_bwd = tiled_layout(1, q.Bp, q.groups, q.rows_cap[1], q.fin_cap[1], q.chunk_cap[1],
+                                 q.cap[1], want_graph, want_rows, &f1);
+        q.lay_bwd_flat = tiled_layout(1, q.Bp, q.groups, q.rows_cap[1], q.fin_cap[1],
+                                      q.chunk_cap[1], q.cap[1], false, want_rows, &f2);
+        ok = f0 && f1 && f2;
+        if (!ok) return fail(CK_ERR_INTERNAL, "tiled layout does not fit although the build checked it");
+    } else {
+        q.lay_fwd = smem_layout(q, 0, want_graph, want_stage, want_rows);
+        q.lay_bwd = smem_layout(q, 1, want_graph, want_stage, want_rows);
+        // the recomputing backward runs in windows of K input steps (one launch
+        // each), every accumulator in global memory
+        q.lay_bwd_flat = smem_layout(q, 1, false, false, want_rows);
+        const size_t cta_smem = std::min<size_t>(kMaxSmem, kSmemPerSm / kCtasPerSm - 1024) - kStaticSmem;
+        if (q.lay_fwd.bytes > cta_smem || q.lay_bwd.bytes > cta_smem || q.lay_bwd_flat.bytes > cta_smem)
+            return fail(CK_ERR_UNSUPPORTED, "per-CTA tables exceed shared memory (rows per SM too many)");
+    }
     const size_t NBp = (size_t)q.N * q.Bp;
     const size_t E1 = (size_t)(q.E > 0 ? q.E : 1);
     size_t off = 0;
@@ -1597,6 +2167,9 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     off += q.ctrl_bytes;
     q.off_carry = off;
     off = align256(off + 8 * (size_t)q.P * q.Bp);
+    q.off_xbuf = off;
+    off = align256(off + (q.tiled ? 8 * (size_t)q.P * q.xrows * q.Bp : 0));
+    q.clear_bytes = off - q.off_ctrl;
     q.off_wperm = off;
     off = align256(off + 4 * E1);
     q.off_dwperm = off;
@@ -1606,7 +2179,9 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     q.off_da = off;
     off = align256(off + 8 * NBp);
     q.off_rowsum = off;
-    off = align256(off + 4 * NBp);
+    // row slots out of shared memory: per row, or (tiled) per CTA and block row
+    off = align256(off + 4 * std::max(NBp, q.tiled ? (size_t)q.P * q.rows_cap[0] * q.Bp +
+                                                         (size_t)q.P * q.rows_cap[1] * q.Bp : 0));
     q.off_lacc = off;
     off = align256(off + 8 * 32 * (size_t)q.N);
     q.scratch_bytes = off;
@@ -1631,15 +2206,30 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
     return CK_OK;
 }
 
+void forward_only_scratch(Plan *q) {
+    size_t off = 0;
+    q->off_ctrl = off;
+    off += q->ctrl_bytes;
+    q->off_carry = off;
+    off = align256(off + 8 * (size_t)q->P * q->Bp);
+    q->off_xbuf = off;
+    off = align256(off + (q->tiled ? 8 * (size_t)q->P * q->xrows * q->Bp : 0));
+    q->clear_bytes = off - q->off_ctrl;
+    q->off_wperm = off;
+    off = align256(off + 4 * (size_t)(q->E > 0 ? q->E : 1));
+    q->off_rowsum = off;
+    off = align256(off + 4 * std::max((size_t)q->N * q->Bp,
+                                      q->tiled ? (size_t)q->P * q->rows_cap[0] * q->Bp : 0));
+    q->off_dwperm = q->off_G = q->off_da = q->off_lacc = kNoRegion;
+    q->off_hwin = q->off_pwin = kNoRegion;
+    q->scratch_bytes = off;
+}
+
 ck_status launch_forward(const ck_graph *g, const Plan &p, const FwdIO &io, cudaStream_t s,
                          int64_t *launches) {
     KArgs k;
     fill_common(k, g, p, io.scratch, 0);
-    k.row_ptr = g->row_ptr;
-    k.piece = g->piece[0][pass_index(p.Bp)];
-    k.col = g->col;
-    k.perm = g->perm;
-    k.rowid = g->rowid;
+    set_graph(k, g, p, 0);
     k.w = io.w;
     k.leak = io.leak;
     k.bias = io.bias;
@@ -1655,11 +2245,7 @@ ck_status launch_forward_ckpt(const ck_graph *g, const Plan &p, const FwdIO &io,
                               int64_t *launches) {
     KArgs k;
     fill_common(k, g, p, io.scratch, 0);
-    k.row_ptr = g->row_ptr;
-    k.piece = g->piece[0][pass_index(p.Bp)];
-    k.col = g->col;
-    k.perm = g->perm;
-    k.rowid = g->rowid;
+    set_graph(k, g, p, 0);
     k.w = io.w;
     k.leak = io.leak;
     k.bias = io.bias;
@@ -1690,11 +2276,7 @@ ck_status launch_backward_recompute(const ck_graph *g, const Plan &p, const RcIO
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (checkpoint)");
         KArgs kf;
         fill_common(kf, g, p, io.scratch, 0);
-        kf.row_ptr = g->row_ptr;
-        kf.piece = g->piece[0][pass_index(p.Bp)];
-        kf.col = g->col;
-        kf.perm = g->perm;
-        kf.rowid = g->rowid;
+        set_graph(kf, g, p, 0);
         kf.w = io.w;
         kf.leak = io.leak;
         kf.bias = io.bias;
@@ -1716,11 +2298,7 @@ ck_status launch_backward_recompute(const ck_graph *g, const Plan &p, const RcIO
         // step), and s = 0 after step 0
         KArgs kb;
         fill_common(kb, g, p, io.scratch, 1, &p.lay_bwd_flat);
-        kb.row_ptr = g->rowT_ptr;
-        kb.piece = g->piece[1][pass_index(p.Bp)];
-        kb.col = g->colT;
-        kb.perm = g->permT;
-        kb.rowid = g->rowidT;
+        set_graph(kb, g, p, 1);
         kb.w = io.w;
         kb.leak = io.leak;
         kb.H = hwin;
@@ -1752,11 +2330,7 @@ ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cud
                           int64_t *launches) {
     KArgs k;
     fill_common(k, g, p, io.scratch, 1);
-    k.row_ptr = g->rowT_ptr;
-    k.piece = g->piece[1][pass_index(p.Bp)];
-    k.col = g->colT;
-    k.perm = g->permT;
-    k.rowid = g->rowidT;
+    set_graph(k, g, p, 1);
     k.w = io.w;
     k.leak = io.leak;
     k.H = const_cast<float *>(io.saved);

@@ -33,6 +33,14 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_bounds_checked_build_exports_the_same_symbols():
+    """The bounds-checked variant (libck_bounds.so) is the same ABI."""
+    from sparse_graph_recurrent_gb300 import build
+    lib_b = ctypes.CDLL(build.build(variant="bounds"))
+    for n in sorted(_declared()):
+        assert hasattr(lib_b, n), n
+
+
 def test_status_strings(lib):
     for code, name in [(0, b"CK_OK"), (1, b"CK_ERR_INVALID_ARG"), (4, b"CK_ERR_TIMEOUT"),
                        (5, b"CK_ERR_WORKSPACE"), (7, b"CK_ERR_UNSUPPORTED")]:

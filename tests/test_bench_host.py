@@ -76,3 +76,27 @@ def test_step_roofline_takes_the_slower_bound():
     assert abs(r["frac"] - (19.45 / 18.0) / 2.4) < 1e-9
     r = bench.step_roofline(1e9, 30e9, 18000.0, 6000.0, 10.0)
     assert r["bound"] == "hbm" and abs(r["roofline_ms"] - 5.0) < 1e-9 and abs(r["frac"] - 0.5) < 1e-9
+
+
+def test_memory_figures_add_up():
+    import bench
+    m = bench.memory_figures(N=10, E=30, B=4, T=3, n_in=2, graph_bytes=1000, saved_b=500,
+                             scratch_b=200, ckpt_b=100, scratch_rc_b=300)
+    io = 4 * ((30 + 20 + 24 + 40) + 2 * 120 + (30 + 20 + 24 + 40))
+    assert m["io_bytes"] == io
+    assert m["step_bytes"] == 1000 + io + 500 + 200
+    assert m["recompute"]["step_bytes"] == 1000 + io + 100 + 300
+
+
+def test_l2_sweep_shapes_are_accepted_by_the_probe():
+    """Every swept shape satisfies ck_probe_read_shape's documented limits, so
+    the bench's sweep cannot be cut short by a refused shape."""
+    import bench
+    for lb, depth, thr, cps in bench.L2_SWEEP:
+        assert lb in (16, 32) and depth in (2, 4, 8, 16) and thr in (128, 256, 512, 1024)
+        assert 1 <= cps and thr * cps <= 2048
+        assert not (depth == 16 and thr > 512)
+    assert any(lb == 32 for lb, *_ in bench.L2_SWEEP)
+    # one pass of a 160-SM grid stays within half the buffer
+    for lb, depth, thr, cps in bench.L2_SWEEP:
+        assert lb * depth * thr * cps * 160 <= bench.L2_SWEEP_BYTES // 2

@@ -20,6 +20,19 @@ def _default_options():
     yield
     _ck.ck_set_option(_ck.OPT_PERSISTENT, 1)
     _ck.ck_set_option(_ck.OPT_GRAPH_IN_SMEM, 1)
+    _ck.ck_set_option(_ck.OPT_ROWS_IN_SMEM, 1)
+    _ck.ck_set_option(_ck.OPT_TILED, 0)
+
+
+# The two kernel families: the tiled kernels (state chunks gathered from shared
+# memory; used when the graph has a tiling and B <= 32) and the L2-gather
+# kernels (every other shape, and all shapes with the tiled kernels off).
+KERNELS = {"tiled": 1, "l2": 0}
+
+
+def _kernels(name):
+    from sparse_graph_recurrent_gb300 import _ck
+    _ck.ck_set_option(_ck.OPT_TILED, KERNELS[name])
 
 
 SMALL = [
@@ -42,35 +55,53 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("kernels", list(KERNELS))
 @pytest.mark.parametrize("seed,N,E,n_in,B,T,M,extra", SMALL, ids=[f"s{c[0]}_N{c[1]}_E{c[2]}_B{c[4]}_M{c[6]}" for c in SMALL])
-def test_small_cases(seed, N, E, n_in, B, T, M, extra):
+def test_small_cases(seed, N, E, n_in, B, T, M, extra, kernels):
+    _kernels(kernels)
     c = workloads.small(seed, N, E, n_in, B, T, M, **extra)
     out, g = run_gpu(c)
     ref_out, ref = oracle.run_case(c)
     assert_parity(out, g, ref_out, ref, f"seed {seed}")
 
 
-def test_config0_tiny():
+@pytest.mark.parametrize("kernels", list(KERNELS))
+def test_config0_tiny(kernels):
+    _kernels(kernels)
     c = workloads.make(0)
     out, g = run_gpu(c)
     ref_out, ref = oracle.run_case(c)
     assert_parity(out, g, ref_out, ref, "tiny")
 
 
+_ORACLE = {}
+
+
+def _oracle_full(cid, M=None):
+    """The oracle's full run of a workload, computed once per test session."""
+    key = (cid, M)
+    if key not in _ORACLE:
+        c = workloads.make(cid, M=M)
+        _ORACLE[key] = (c, oracle.step_columns(c, oracle.threads_available()))
+    return _ORACLE[key]
+
+
 @pytest.mark.slow
-def test_config1_flygpt_full():
-    c = workloads.make(1)
+@pytest.mark.parametrize("kernels", list(KERNELS))
+def test_config1_flygpt_full(kernels):
+    _kernels(kernels)
+    c, (ref_out, ref) = _oracle_full(1)
     out, g = run_gpu(c)
-    ref_out, ref = oracle.run_case(c)
     assert_parity(out, g, ref_out, ref, "flygpt")
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("kernels", list(KERNELS))
 @pytest.mark.parametrize("M", [1, 2, 3])
-def test_config2_ragged_full(M):
-    c = workloads.make(2, M=M)
+def test_config2_ragged_full(M, kernels):
+    _kernels(kernels)
+    c, (ref_out, ref) = _oracle_full(2, M)
     out, g = run_gpu(c)
-    ref_out, ref = oracle.run_case(c)
     assert_parity(out, g, ref_out, ref, f"ragged M={M}")
 
 
@@ -105,16 +136,18 @@ def test_config4_connectome_sampled_column():
     _sampled(4, [19])
 
 
-def test_modes_are_bitwise_identical():
-    """One launch per microstep (operands read from global memory), and the
-    graph streamed from global memory, follow the same summation order as the
-    default persistent launch."""
+@pytest.mark.parametrize("kernels", list(KERNELS))
+def test_modes_are_bitwise_identical(kernels):
+    """One launch per microstep (operands read from global memory), the graph
+    streamed from global memory, and row sums kept in the scratch buffer follow
+    the same summation order as the default persistent launch."""
     from sparse_graph_recurrent_gb300 import _ck
+    _kernels(kernels)
     c = workloads.small(201, 400, 30000, 12, 20, 3, 2, hub_deg=10000)
     base_out, base = run_gpu(c)
     again_out, again = run_gpu(c)
     np.testing.assert_array_equal(base_out, again_out)
-    for opt, val in ((_ck.OPT_PERSISTENT, 0), (_ck.OPT_GRAPH_IN_SMEM, 0)):
+    for opt, val in ((_ck.OPT_PERSISTENT, 0), (_ck.OPT_GRAPH_IN_SMEM, 0), (_ck.OPT_ROWS_IN_SMEM, 0)):
         _ck.ck_set_option(opt, val)
         out, g = run_gpu(c)
         _ck.ck_set_option(opt, 1)

@@ -395,3 +395,25 @@ def test_run_case_batch_cols(oracle_lib, cols):
         np.testing.assert_allclose(g_c[k], g_m[k], rtol=1e-13, atol=1e-15, err_msg=k)
         # and the mask matters: the unmasked full run differs
         assert np.abs(g_f[k] - g_c[k]).max() > 1e-6, k
+
+
+# --------------------------------------------------------------------------
+# step_columns: the multi-core statement of one step used for the timed CPU
+# baseline.  It must agree with the single-thread oracle (pinned above) for
+# every thread count, differing only in the grouping of the column sums.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("threads", [1, 2, 3, 4, 16])
+def test_step_columns_matches_single_thread(oracle_lib, threads):
+    c = _case(seed=41, N=20, E=90, n_in=5, B=7, T=3, M=2, hub_deg=30)
+    out_r, g_r = oracle_lib.run_case(c)
+    out_p, g_p = oracle_lib.step_columns(c, threads)
+    assert np.array_equal(out_p, out_r)
+    for k in ("ddrives", "dstate0"):
+        assert np.array_equal(g_p[k], g_r[k]), k
+    for k in ("dw", "dleak", "dbias"):
+        scale = np.abs(g_r[k]).max()
+        assert np.abs(g_p[k] - g_r[k]).max() <= 1e-12 * scale, k
+    # a second run with the same thread count repeats every bit
+    out_q, g_q = oracle_lib.step_columns(c, threads)
+    assert all(np.array_equal(g_q[k], g_p[k]) for k in g_p)
