@@ -188,8 +188,9 @@ ck_status ck_workspace_size(const ck_graph *g, int64_t B, int64_t T, int64_t mic
  *   drives       (device) float[T][n_in][B]; may be NULL when n_in == 0
  *   state0       (device) float[B][N]
  *   states_out   (device) float[T][B][N], overwritten
- *   saved        (device) >= saved_bytes, 16-byte aligned; filled for ck_backward
- *   scratch      (device) >= scratch_bytes, 16-byte aligned
+ *   saved        (device) >= saved_bytes, 32-byte aligned; filled for ck_backward
+ *   scratch      (device) >= scratch_bytes, 32-byte aligned (the kernels gather rows
+ *                with 32-byte loads)
  * Runs as one persistent cooperative kernel with bounded grid-wide barriers
  * between microsteps.  Asynchronous.  A device-side wait that times out makes
  * the kernel stop early and is reported by ck_query_status.
@@ -249,7 +250,7 @@ ck_status ck_workspace_size_recompute(const ck_graph *g, int64_t B, int64_t T,
 /*
  * ck_forward_checkpointed -- ck_forward that writes, instead of `saved`, the
  * state after every input step:
- *   ckpt   (device) >= ckpt_bytes, 16-byte aligned: float[T+1][N][Bp], Bp = B
+ *   ckpt   (device) >= ckpt_bytes, 32-byte aligned: float[T+1][N][Bp], Bp = B
  *          rounded up as in `saved`; ckpt[0] is state0 transposed
  * Other arguments, ownership and errors as ck_forward (scratch sized by
  * ck_workspace_size_recompute).

@@ -44,7 +44,7 @@ ck_status check_graph(const ck_graph *g) {
     return CK_OK;
 }
 
-bool misaligned(const void *p) { return ((uintptr_t)p & 15u) != 0; }
+bool misaligned(const void *p) { return ((uintptr_t)p & 31u) != 0; }
 
 }  // namespace
 }  // namespace ck
@@ -276,7 +276,7 @@ ck_status ck_forward(const ck_graph *g, const float *edge_values, const float *l
         !scratch || (g->n_in > 0 && !drives))
         return fail(CK_ERR_INVALID_ARG, "a required pointer is NULL");
     if (misaligned(saved) || misaligned(scratch))
-        return fail(CK_ERR_INVALID_ARG, "saved and scratch must be 16-byte aligned");
+        return fail(CK_ERR_INVALID_ARG, "saved and scratch must be 32-byte aligned");
     if (saved_bytes < p.saved_bytes || scratch_bytes < p.scratch_bytes)
         return fail(CK_ERR_WORKSPACE, "workspace too small: saved %zu < %zu or scratch %zu < %zu",
                     saved_bytes, p.saved_bytes, scratch_bytes, p.scratch_bytes);
@@ -312,7 +312,7 @@ ck_status ck_forward_checkpointed(const ck_graph *g, const float *edge_values,
         !scratch || (g->n_in > 0 && !drives))
         return fail(CK_ERR_INVALID_ARG, "a required pointer is NULL");
     if (misaligned(ckpt) || misaligned(scratch))
-        return fail(CK_ERR_INVALID_ARG, "ckpt and scratch must be 16-byte aligned");
+        return fail(CK_ERR_INVALID_ARG, "ckpt and scratch must be 32-byte aligned");
     if (ckpt_bytes < p.ckpt_bytes || scratch_bytes < p.scratch_bytes_rc)
         return fail(CK_ERR_WORKSPACE, "workspace too small: ckpt %zu < %zu or scratch %zu < %zu",
                     ckpt_bytes, p.ckpt_bytes, scratch_bytes, p.scratch_bytes_rc);
@@ -336,7 +336,7 @@ ck_status ck_backward_recompute(const ck_graph *g, const float *edge_values, con
         !d_leak || !d_bias || !d_state0 || !scratch || (g->n_in > 0 && (!drives || !d_drives)))
         return fail(CK_ERR_INVALID_ARG, "a required pointer is NULL");
     if (misaligned(ckpt) || misaligned(scratch))
-        return fail(CK_ERR_INVALID_ARG, "ckpt and scratch must be 16-byte aligned");
+        return fail(CK_ERR_INVALID_ARG, "ckpt and scratch must be 32-byte aligned");
     if (ckpt_bytes < p.ckpt_bytes || scratch_bytes < p.scratch_bytes_rc)
         return fail(CK_ERR_WORKSPACE, "workspace too small: ckpt %zu < %zu or scratch %zu < %zu",
                     ckpt_bytes, p.ckpt_bytes, scratch_bytes, p.scratch_bytes_rc);
@@ -360,7 +360,7 @@ ck_status ck_backward(const ck_graph *g, const float *edge_values, const float *
         !d_leak || !d_bias || !d_state0 || !scratch || (g->n_in > 0 && !d_drives))
         return fail(CK_ERR_INVALID_ARG, "a required pointer is NULL");
     if (misaligned(saved) || misaligned(scratch))
-        return fail(CK_ERR_INVALID_ARG, "saved and scratch must be 16-byte aligned");
+        return fail(CK_ERR_INVALID_ARG, "saved and scratch must be 32-byte aligned");
     if (saved_bytes < p.saved_bytes || scratch_bytes < p.scratch_bytes)
         return fail(CK_ERR_WORKSPACE, "workspace too small: saved %zu < %zu or scratch %zu < %zu",
                     saved_bytes, p.saved_bytes, scratch_bytes, p.scratch_bytes);

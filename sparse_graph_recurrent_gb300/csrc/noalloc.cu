@@ -71,7 +71,7 @@ extern "C" ck_status ck_forward_static_scratch(const ck_graph *g, const float *e
     if ((g->E > 0 && !edge_values) || !leak || !bias || !state0 || !states_out || !saved ||
         (g->n_in > 0 && !drives))
         return fail(CK_ERR_INVALID_ARG, "a required pointer is NULL");
-    if (((uintptr_t)saved & 15u) != 0) return fail(CK_ERR_INVALID_ARG, "saved must be 16-byte aligned");
+    if (((uintptr_t)saved & 31u) != 0) return fail(CK_ERR_INVALID_ARG, "saved must be 32-byte aligned");
     if (saved_bytes < p.saved_bytes)
         return fail(CK_ERR_WORKSPACE, "saved too small: %zu < %zu", saved_bytes, p.saved_bytes);
 

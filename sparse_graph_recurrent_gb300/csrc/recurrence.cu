@@ -65,6 +65,9 @@ namespace ck {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+// Gathers of rows held as two 16-byte chunks per lane (NC = 2) use one 256-bit
+// load (sm_100 and later) instead of two 128-bit ones.
+constexpr bool kGatherV8 = true;
 constexpr int kMaxSmem = 227 * 1024;      // shared memory one CTA may take
 constexpr int kSmemPerSm = 228 * 1024;    // shared memory an SM holds
 constexpr int kStaticSmem = 64;
@@ -148,6 +151,13 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 __device__ __forceinline__ int ld_err(const int *p) { return *(volatile const int *)p; }
 
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+// 32 bytes from global memory (32-byte aligned), cached in L1 and L2.
+__device__ __forceinline__ void ld_ca_v8(const float *p, float4 &lo, float4 &hi) {
+    asm volatile("ld.global.ca.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w), "=f"(hi.x), "=f"(hi.y), "=f"(hi.z),
+                   "=f"(hi.w)
+                 : "l"(p));
+}
 __device__ __forceinline__ void fma4(float4 &a, float w, const float4 &x) {
     a.x = fmaf(w, x.x, a.x);
     a.y = fmaf(w, x.y, a.y);
@@ -433,6 +443,12 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                                              bool active, const float *__restrict__ rows,
                                              const float *__restrict__ hprev) {
     const int Bp = a.Bp, CW = 4 * a.LPE;
+    // Columns a lane holds: chunk ch covers LB + ch * CS .. + 3.  With 256-bit
+    // gathers (V8) a lane's two chunks are contiguous (columns 8 lig .. 8 lig
+    // + 7); otherwise chunk ch sits CW columns after chunk ch - 1.
+    constexpr bool V8 = kGatherV8 && NC == 2 && !TT;
+    const int LB = V8 ? lig * 8 : lig * 4;
+    const int CS = V8 ? 4 : CW;
     const int n = c.e1 - c.e0;
     int k0 = c.e0, k1 = c.e0;
     if (active && n > 0) {
@@ -462,16 +478,16 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             int i = row - c.r0;
             const bool in = row >= 0 && i <= c.nrows;  // always, for a valid graph
             if (in && !CK_IN(a.err, i, a.rows_cap)) i = 0;
-            const float *hp = S_st4(a) + (size_t)(in ? i : 0) * Bp + lig * 4;
+            const float *hp = S_st4(a) + (size_t)(in ? i : 0) * Bp + LB;
 #pragma unroll
             for (int ch = 0; ch < HN; ++ch)
-                h.v[ch] = in ? *reinterpret_cast<const float4 *>(hp + ch * CW) : zero4();
+                h.v[ch] = in ? *reinterpret_cast<const float4 *>(hp + ch * CS) : zero4();
         } else {
             if (row >= 0 && !CK_IN(a.err, row, a.N)) row = 0;
-            const float *hp = hprev + (size_t)(row < 0 ? 0 : row) * Bp + lig * 4;
+            const float *hp = hprev + (size_t)(row < 0 ? 0 : row) * Bp + LB;
 #pragma unroll
             for (int ch = 0; ch < HN; ++ch)
-                h.v[ch] = row >= 0 ? __ldg(reinterpret_cast<const float4 *>(hp + ch * CW)) : zero4();
+                h.v[ch] = row >= 0 ? __ldg(reinterpret_cast<const float4 *>(hp + ch * CS)) : zero4();
         }
         return h;
     };
@@ -494,9 +510,9 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     auto flush = [&](int row) {
         const int i = row - c.r0;
         if (i >= 0 && i < c.nrows) {
-            float *dst = c.rows + (size_t)i * Bp + lig * 4;
+            float *dst = c.rows + (size_t)i * Bp + LB;
 #pragma unroll
-            for (int ch = 0; ch < NC; ++ch) *reinterpret_cast<float4 *>(dst + ch * CW) = acc[ch];
+            for (int ch = 0; ch < NC; ++ch) *reinterpret_cast<float4 *>(dst + ch * CS) = acc[ch];
         } else {
             atomicCAS(a.err, 0, kDevInternal);  // cannot happen for a valid graph
         }
@@ -571,10 +587,14 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                 for (int ch = 0; ch < NC; ++ch) bt.v[q][ch] = *reinterpret_cast<const float4 *>(rp + ch * CW);
             } else {
                 if (!CK_IN(a.err, cc, a.N)) cc = 0;
-                const float *rp = rows + (size_t)cc * Bp + lig * 4;
+                const float *rp = rows + (size_t)cc * Bp + LB;
+                if constexpr (V8) {
+                    ld_ca_v8(rp, bt.v[q][0], bt.v[q][NC - 1]);
+                } else {
 #pragma unroll
-                for (int ch = 0; ch < NC; ++ch)
-                    bt.v[q][ch] = __ldca(reinterpret_cast<const float4 *>(rp + ch * CW));
+                    for (int ch = 0; ch < NC; ++ch)
+                        bt.v[q][ch] = __ldca(reinterpret_cast<const float4 *>(rp + ch * CW));
+                }
             }
         }
     };
@@ -686,9 +706,9 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
         }
     }
     if (active && CK_IN(a.err, gam, a.G)) {
-        float *dst = S_scarry(a) + (size_t)gam * Bp + lig * 4;
+        float *dst = S_scarry(a) + (size_t)gam * Bp + LB;
 #pragma unroll
-        for (int ch = 0; ch < NC; ++ch) *reinterpret_cast<float4 *>(dst + ch * CW) = acc[ch];
+        for (int ch = 0; ch < NC; ++ch) *reinterpret_cast<float4 *>(dst + ch * CS) = acc[ch];
     }
 }
 
@@ -1252,7 +1272,9 @@ __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a)
                 if (k >= c.e1) continue;
                 if (SMEMG) {
                     S_scw(a)[k - c.e0] = make_int2(cl[j], __float_as_int(wv));
-                    if (BWD) S_sdw(a)[k - c.e0] = 0.f;
+                    // a recomputing window after the first continues the sums
+                    // the previous window left in dwperm
+                    if (BWD) S_sdw(a)[k - c.e0] = a.zero_dw ? 0.f : __ldcg(a.dwperm + k);
                 } else {
                     a.wperm[k] = wv;
                     if (BWD && a.zero_dw) a.dwperm[k] = 0.f;
@@ -1425,6 +1447,11 @@ __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a)
                 }
             }
         }
+    } else if (SMEMG && BWD) {
+        // a recomputing window that is not the last: its edge sums go on to the
+        // next window through dwperm
+        __syncthreads();
+        for (int k = c.e0 + tid; k < c.e1; k += THREADS) a.dwperm[k] = S_sdw(a)[k - c.e0];
     }
 }
 
@@ -1606,7 +1633,7 @@ __global__ void __launch_bounds__(THREADS, 1) tiled_kernel(const KArgs a) {
                 if (k >= cb.e1) continue;
                 if (SMEMG) {
                     S_scw(a)[k - cb.e0] = make_int2(cl[j], __float_as_int(wv));
-                    if (BWD) S_sdw(a)[k - cb.e0] = 0.f;
+                    if (BWD) S_sdw(a)[k - cb.e0] = a.zero_dw ? 0.f : __ldcg(a.dwperm + k);
                 } else {
                     a.wperm[k] = wv;
                     if (BWD && a.zero_dw) a.dwperm[k] = 0.f;
@@ -2153,8 +2180,10 @@ ck_status make_plan(const ck_graph *g, int64_t B, int64_t T, int64_t M, Plan *p)
         q.lay_fwd = smem_layout(q, 0, want_graph, want_stage, want_rows);
         q.lay_bwd = smem_layout(q, 1, want_graph, want_stage, want_rows);
         // the recomputing backward runs in windows of K input steps (one launch
-        // each), every accumulator in global memory
-        q.lay_bwd_flat = smem_layout(q, 1, false, false, want_rows);
+        // each): the CTA's graph slice and edge sums in shared memory when they
+        // fit (the sums carried between windows through dwperm), every other
+        // accumulator in global memory
+        q.lay_bwd_flat = smem_layout(q, 1, want_graph, false, want_rows);
         const size_t cta_smem = std::min<size_t>(kMaxSmem, kSmemPerSm / kCtasPerSm - 1024) - kStaticSmem;
         if (q.lay_fwd.bytes > cta_smem || q.lay_bwd.bytes > cta_smem || q.lay_bwd_flat.bytes > cta_smem)
             return fail(CK_ERR_UNSUPPORTED, "per-CTA tables exceed shared memory (rows per SM too many)");
