@@ -13,7 +13,9 @@ is outside the timed events.  Prints one JSON line (rank 0).
 --config picks another of the five synthetic workloads (default 1, the FlyGPT
 shape that the headline is quoted on); --microsteps overrides its M.
 --graph-in-host-memory builds the graph with its edge-indexed arrays in pinned
-host memory, read by the kernels over the CPU-GPU link.
+host memory, read by the kernels over the CPU-GPU link.  --recompute times the
+checkpointing forward and the recomputing backward instead of the regular
+pair.  --ncu-steps K only runs K steps (for a profiler) and exits.
 
 With N > 1 (under torchrun) every rank runs an independent replica of the
 same step (the method has no exchange between replicas): weak scaling.
@@ -409,6 +411,29 @@ def l2_read_sweep(timed, buf, sink):
     return out
 
 
+def run_plain_steps(args, c):
+    """`--ncu-steps K`: K forward + backward steps through the public API and
+    nothing else (no probes, no timing), for a profiler to capture; prints one
+    line when done."""
+    import torch
+
+    import sparse_graph_recurrent_gb300 as pkg
+    from sparse_graph_recurrent_gb300 import _ck
+    dev = torch.device("cuda", 0)
+    tt = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    g = pkg.SparseGraph(tt(c["src"]), tt(c["dst"]), c["N"], tt(c["input_nodes"]),
+                        edges_in_host_memory=args.graph_in_host_memory)
+    w, leak, bias, drives, state0, dout = (tt(c[k]) for k in ("w", "leak", "bias", "drives",
+                                                              "state0", "dout"))
+    B, T, M = c["B"], c["T"], c["M"]
+    for _ in range(args.ncu_steps):
+        _, saved, scratch = pkg.forward(g, w, leak, bias, drives, state0, M)
+        pkg.backward(g, w, leak, B, T, M, saved, dout, scratch)
+    _ck.ck_query_status(scratch)
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_steps": args.ncu_steps, "config": {"workload": _workload_name(c)}}))
+
+
 def run_ours(args, c, rank, world, dist):
     import torch
 
@@ -428,8 +453,11 @@ def run_ours(args, c, rank, world, dist):
     ckpt_b, scratch_rc_b = _ck.ck_workspace_size_recompute(g.handle, B, T, M)
     mem = memory_figures(N, E, B, T, n_in, _ck.ck_graph_memory(g.handle)[0], saved_b, scratch_b,
                          ckpt_b, scratch_rc_b)
-    saved = torch.empty(saved_b, dtype=torch.uint8, device=dev)
-    scratch = torch.empty(scratch_b, dtype=torch.uint8, device=dev)
+    # --recompute: the checkpointing forward and the recomputing backward, with
+    # their own workspace (checkpoints instead of saved activations)
+    saved = torch.empty(ckpt_b if args.recompute else saved_b, dtype=torch.uint8, device=dev)
+    scratch = torch.empty(scratch_rc_b if args.recompute else scratch_b, dtype=torch.uint8,
+                          device=dev)
     out = torch.empty((T, B, N), device=dev)
     dw, dl, db = (torch.empty(n, device=dev) for n in (E, N, N))
     dd = torch.empty((T, n_in, B), device=dev)
@@ -439,11 +467,25 @@ def run_ours(args, c, rank, world, dist):
 
     launches = [0]
 
+    def fwd_call():
+        if args.recompute:
+            _ck.ck_forward_checkpointed(g.handle, w, leak, bias, drives, state0, M, out, saved,
+                                        scratch)
+        else:
+            _ck.ck_forward(g.handle, w, leak, bias, drives, state0, M, out, saved, scratch)
+        launches[0] += _ck.ck_last_launch_count()
+
+    def bwd_call():
+        if args.recompute:
+            _ck.ck_backward_recompute(g.handle, w, leak, bias, drives, B, T, M, saved, dout, dw,
+                                      dl, db, dd, dh, scratch)
+        else:
+            _ck.ck_backward(g.handle, w, leak, B, T, M, saved, dout, dw, dl, db, dd, dh, scratch)
+        launches[0] += _ck.ck_last_launch_count()
+
     def step():
-        _ck.ck_forward(g.handle, w, leak, bias, drives, state0, M, out, saved, scratch)
-        launches[0] += _ck.ck_last_launch_count()
-        _ck.ck_backward(g.handle, w, leak, B, T, M, saved, dout, dw, dl, db, dd, dh, scratch)
-        launches[0] += _ck.ck_last_launch_count()
+        fwd_call()
+        bwd_call()
 
     for _ in range(args.warmup):
         step()
@@ -485,11 +527,9 @@ def run_ours(args, c, rank, world, dist):
     for k in range(args.steps):
         flush.fill_(k & 0xff)
         ev[k][0].record(stream)
-        _ck.ck_forward(g.handle, w, leak, bias, drives, state0, M, out, saved, scratch)
-        launches[0] += _ck.ck_last_launch_count()
+        fwd_call()
         ev[k][1].record(stream)
-        _ck.ck_backward(g.handle, w, leak, B, T, M, saved, dout, dw, dl, db, dd, dh, scratch)
-        launches[0] += _ck.ck_last_launch_count()
+        bwd_call()
         ev[k][2].record(stream)
     torch.cuda.synchronize()
     clocks.end()
@@ -523,14 +563,22 @@ def run_ours(args, c, rank, world, dist):
             d_out = h_in["dout"].to(dev, non_blocking=True)
         d_out.record_stream(main)
         dout_in = side.record_event()
-        o, sv, sc = pkg.forward(g, d["w"], d["leak"], d["bias"], d["drives"], d["state0"], M)
+        if args.recompute:
+            o, sv, sc = pkg.forward_checkpointed(g, d["w"], d["leak"], d["bias"], d["drives"],
+                                                 d["state0"], M)
+        else:
+            o, sv, sc = pkg.forward(g, d["w"], d["leak"], d["bias"], d["drives"], d["state0"], M)
         fwd_done = main.record_event()
         with torch.cuda.stream(side):
             side.wait_event(fwd_done)
             h_out[0].copy_(o, non_blocking=True)
         o.record_stream(side)
         main.wait_event(dout_in)
-        grads = pkg.backward(g, d["w"], d["leak"], B, T, M, sv, d_out, sc)
+        if args.recompute:
+            grads = pkg.backward_recompute(g, d["w"], d["leak"], d["bias"], d["drives"], B, T, M,
+                                           sv, d_out, sc)
+        else:
+            grads = pkg.backward(g, d["w"], d["leak"], B, T, M, sv, d_out, sc)
         for hdst, src in zip(h_out[1:], grads):
             hdst.copy_(src, non_blocking=True)
         main.wait_stream(side)
@@ -554,7 +602,8 @@ def run_ours(args, c, rank, world, dist):
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     hbm_peak, hbm_src = _peaks()
     q_hbm = hbm_bytes(N, E, B, T, M, n_in)
-    headline = c.get("config_id", 1) == 1 and M == 2 and not args.graph_in_host_memory
+    headline = (c.get("config_id", 1) == 1 and M == 2 and not args.graph_in_host_memory
+                and not args.recompute)
     props = torch.cuda.get_device_properties(dev)
     sm_mhz = (clk or {}).get("sm_max_mhz") or 2070.0
     fp32_peak = props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12  # 128 FP32 lanes per SM
@@ -568,7 +617,9 @@ def run_ours(args, c, rank, world, dist):
         "config": {"workload": _workload_name(c), "parallelism": "replicas",
                    "l2": "flushed by a 512 MB write before every timed step (outside the events)",
                    **({"graph": "edge-indexed arrays in pinned host memory"}
-                      if args.graph_in_host_memory else {})},
+                      if args.graph_in_host_memory else {}),
+                   **({"pass_pair": "checkpointing forward + recomputing backward"}
+                      if args.recompute else {})},
         "roofline": {"bound": "l2", "kernel": dom, "achieved": achieved, "peak": l2_read,
                      "unit": "GB/s", "frac": achieved / l2_read,
                      "traffic": ncu_traffic(dom) if headline else None,
@@ -609,6 +660,10 @@ def main():
     ap.add_argument("--config", type=int, choices=range(5), default=1)
     ap.add_argument("--microsteps", type=int, default=None)
     ap.add_argument("--graph-in-host-memory", action="store_true")
+    ap.add_argument("--recompute", action="store_true",
+                    help="time the checkpointing forward and the recomputing backward")
+    ap.add_argument("--ncu-steps", type=int, default=0,
+                    help="run this many steps and nothing else (for a profiler), then exit")
     args = ap.parse_args()
 
     import workloads
@@ -621,6 +676,9 @@ def main():
         return
     if args.impl == "torch-sparse":
         run_torch_sparse(args, c, rank)
+        return
+    if args.ncu_steps > 0:
+        run_plain_steps(args, c)
         return
     dist = None
     if world > 1:
