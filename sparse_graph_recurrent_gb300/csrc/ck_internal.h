@@ -120,6 +120,9 @@ struct SmemLayout {
     bool stage;  // finish operands staged in shared memory
     int o_st0, o_st1, o_st2, o_st3, o_st4, o_inp, o_acc;
     int o_chunk;  // tiled kernels: the chunk of gathered rows (0 otherwise)
+    // a streamed graph slice's cp.async ring, per lane group: ring_n chunks of
+    // (edges per batch << ring_chb_sh) {col, w} entries; ring_n == 0: no ring
+    int o_ring, ring_n, ring_chb_sh;
 };
 
 // Launch description of one ck_forward / ck_backward call (recurrence.cu).

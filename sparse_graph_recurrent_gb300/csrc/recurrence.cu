@@ -68,6 +68,9 @@ constexpr unsigned kFull = 0xffffffffu;
 // Gathers of rows held as two 16-byte chunks per lane (NC = 2) use one 256-bit
 // load (sm_100 and later) instead of two 128-bit ones.
 constexpr bool kGatherV8 = true;
+// A streamed graph slice (graphs beyond L2, or in host memory) comes through a
+// per-group cp.async ring several chunks ahead when shared memory has room.
+constexpr bool kStreamRing = true;
 constexpr int kMaxSmem = 227 * 1024;      // shared memory one CTA may take
 constexpr int kSmemPerSm = 228 * 1024;    // shared memory an SM holds
 constexpr int kStaticSmem = 64;
@@ -105,6 +108,7 @@ struct KArgs {
     unsigned bar_base, bar_extra;
     unsigned long long timeout_ns;
     int bounds_probe;  // bounds-checked build: check one out-of-range index (test hook)
+    int o_ring, ring_n, ring_chb_sh;  // streamed graph: per-group cp.async ring (ring_n 0: none)
     // tiled kernels: per-CTA cell descriptions and row pointers, the chunk of
     // gathered rows in shared memory, the exchange of partial row totals
     const int *tmeta, *tptr;
@@ -318,6 +322,7 @@ __device__ __forceinline__ float *S_st4(const KArgs &a) { return reinterpret_cas
 __device__ __forceinline__ int *S_inp(const KArgs &a) { return reinterpret_cast<int *>(ck_smem + a.o_inp); }
 __device__ __forceinline__ float2 *S_acc(const KArgs &a) { return reinterpret_cast<float2 *>(ck_smem + a.o_acc); }
 __device__ __forceinline__ float *S_chunk(const KArgs &a) { return reinterpret_cast<float *>(ck_smem + a.o_chunk); }
+__device__ __forceinline__ int2 *S_ring(const KArgs &a) { return reinterpret_cast<int2 *>(ck_smem + a.o_ring); }
 // Row stride of the staged arrays that are also read or written across rows
 // (forward st0, backward st3): Bp + 1 words, so a warp walking down a column
 // touches 32 distinct banks as well as one walking along a row.
@@ -336,6 +341,17 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // all but the most recently committed group have landed
 __device__ __forceinline__ void cp_async_wait_but_last() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// all but the N most recently committed groups have landed
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Edges per gather batch of part A: more loads in flight per lane measured
+// slower (the L2 path congests); for NC = 2 three per batch measured fastest in
+// the forward and four in the backward (whose dot-product butterfly wants a
+// power of two).
+__host__ __device__ constexpr int edge_batch(bool bwd, int nc) {
+    return bwd ? (nc == 2 ? 4 : 2) : (nc == 2 ? 3 : 4);
+}
 
 // The helpers below spread their work over nt threads, this one being number
 // t of them.
@@ -438,10 +454,14 @@ __device__ __forceinline__ void group_dots(float (&d)[UNR], int lig, int lpe, in
 
 // TT: the gathered rows are the chunk in shared memory (tiled kernels; column
 // indices then count from the chunk's first node), else `rows` in global memory.
-template <int NC, bool SMEMG, bool BWD, int UNR, bool HS, bool TT = false>
+// RG (streamed graph only): {col, w} come through the group's cp.async ring in
+// shared memory, several chunks ahead, instead of registers one batch ahead.
+template <int NC, bool SMEMG, bool BWD, int UNR, bool HS, bool TT = false, bool RG = false>
 __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int gam, int lig,
                                              bool active, const float *__restrict__ rows,
                                              const float *__restrict__ hprev) {
+    static_assert(!(SMEMG && RG), "the ring serves a streamed graph only");
+    constexpr bool REG = !SMEMG && !RG;  // {col, w} one batch ahead in registers
     const int Bp = a.Bp, CW = 4 * a.LPE;
     // Columns a lane holds: chunk ch covers LB + ch * CS .. + 3.  With 256-bit
     // gathers (V8) a lane's two chunks are contiguous (columns 8 lig .. 8 lig
@@ -528,8 +548,8 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
     int per_sh = 0;
     while (bfly && (UNR << per_sh) < a.LPE) ++per_sh;  // log2(LPE / UNR)
     const bool dw_owner = bfly && (lig & ((1 << per_sh) - 1)) == 0;  // writes item lig >> per_sh
-    int gc[SMEMG ? 1 : UNR];
-    float gw[SMEMG ? 1 : UNR];
+    int gc[REG ? UNR : 1];
+    float gw[REG ? UNR : 1];
     // streamed backward with the butterfly layout: the edge-gradient sum this
     // lane updates in a batch, read one batch ahead too, so the update is a
     // store (each edge's sum is touched by its own group only, once per
@@ -542,7 +562,7 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             gdw = kk < k1 ? __ldcg(a.dwperm + kk) : 0.f;
         }
 #pragma unroll
-        for (int q = 0; q < (SMEMG ? 1 : UNR); ++q) {
+        for (int q = 0; q < (REG ? UNR : 0); ++q) {
             const int kk = kb + q;
             int kc = kk < k1 ? kk : c.e0;
             if (!CK_IN(a.err, kc, a.E)) kc = 0;
@@ -550,15 +570,60 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
             gw[q] = __ldcg(a.wperm + kc);
         }
     };
-    auto load = [&](Batch<NC, UNR> &bt, int kb) {
+    // The ring: RN chunks (a power of two) of CHE = UNR << chb_sh edges, as
+    // {col, w bits}.  Chunk ch of the group's range goes to slot ch mod RN,
+    // copied by the group's lanes RN - 1 chunks before it is read; only chunks
+    // that start inside [k0, k1) are copied (their entries past k1 copy edge e0),
+    // and every chunk boundary commits a group, empty or not, which keeps the
+    // wait counts fixed.  Each lane waits for its own copies; a __syncwarp then
+    // makes the group's copies visible to all its lanes.
+    const int chb_sh = RG ? a.ring_chb_sh : 0;
+    const int RN = RG ? a.ring_n : 1;
+    const int CHE = UNR << chb_sh;
+    int2 *ring = RG && active ? S_ring(a) + (size_t)gam * RN * CHE : nullptr;
+    auto issue = [&](int ch) {
+        const int base = k0 + ch * CHE;
+        if (ring && base < k1) {
+            int2 *dst = ring + (ch & (RN - 1)) * CHE;
+            for (int e = lig; e < CHE; e += a.LPE) {
+                const int kk = base + e;
+                int kc = kk < k1 ? kk : c.e0;
+                if (!CK_IN(a.err, kc, a.E)) kc = 0;
+                cp_async4(&dst[e].x, a.col + kc);
+                cp_async4(&dst[e].y, a.wperm + kc);
+            }
+        }
+        cp_async_commit();
+    };
+    auto load = [&](Batch<NC, UNR> &bt, int kb, int it) {
         int cn[UNR];
         float wn[UNR];
-        if (!SMEMG) {
+        if (REG) {
 #pragma unroll
             for (int q = 0; q < UNR; ++q) {
-                cn[q] = gc[SMEMG ? 0 : q];
-                wn[q] = gw[SMEMG ? 0 : q];
+                cn[q] = gc[REG ? q : 0];
+                wn[q] = gw[REG ? q : 0];
             }
+        }
+        if (RG) {
+            const int pos = it & ((1 << chb_sh) - 1);
+            if (pos == 0) {
+                // this chunk's copies (all lanes') have landed, and every lane
+                // is done with the slot the next copy refills
+                if (RN == 4) cp_async_wait_group<2>();
+                else cp_async_wait_group<0>();
+                __syncwarp();
+                issue((it >> chb_sh) + RN - 1);
+            }
+            const int2 *src = ring ? ring + ((it >> chb_sh) & (RN - 1)) * CHE + pos * UNR : nullptr;
+#pragma unroll
+            for (int q = 0; q < UNR; ++q) {
+                const int2 cw = src ? src[q] : make_int2(0, 0);
+                cn[q] = cw.x;
+                wn[q] = __int_as_float(cw.y);
+            }
+        }
+        if (!SMEMG) {
             if (BWD) cdw = gdw;
             load_graph(kb + UNR);  // next batch's edges (valid addresses past the end too)
         }
@@ -576,7 +641,9 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
                 cc = cw.x;
                 wv = __int_as_float(cw.y);
             } else {
-                cc = cn[q];
+                // a ring slot past the group's range holds no copy: row 0
+                // stands in (weight 0)
+                cc = RG && !ok ? 0 : cn[q];
                 wv = wn[q];
             }
             bt.w[q] = ok ? wv : 0.f;
@@ -665,10 +732,18 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
 
     Batch<NC, UNR> bt;
     if (!SMEMG && trips > 0) load_graph(k0);
+    if (RG && trips > 0)
+        for (int ch = 0; ch < RN - 1; ++ch) issue(ch);
     for (int it = 0; it < trips; ++it) {
         const int kb = k0 + it * UNR;
-        load(bt, kb);
+        load(bt, kb, it);
         consume(bt, kb);
+    }
+    if (RG) {
+        // every copy issued was waited for above; this only settles the
+        // (empty) groups committed last
+        cp_async_wait_all();
+        __syncwarp();
     }
     // the row this group stops in: finished here if its last edge is ours and
     // its row end belongs to this CTA (the carry is then 0), else a carry
@@ -710,6 +785,19 @@ __device__ __forceinline__ void stream_piece(const KArgs &a, const Cta &c, int g
 #pragma unroll
         for (int ch = 0; ch < NC; ++ch) *reinterpret_cast<float4 *>(dst + ch * CS) = acc[ch];
     }
+}
+
+// Part A with the streamed graph's ring when the plan gave it room.
+template <int NC, bool SMEMG, bool BWD, int UNR, bool HS>
+__device__ __forceinline__ void part_a(const KArgs &a, const Cta &c, int gam, int lig, bool active,
+                                       const float *__restrict__ rows, const float *__restrict__ hprev) {
+    if constexpr (!SMEMG) {
+        if (a.ring_n > 0) {
+            stream_piece<NC, false, BWD, UNR, HS, false, true>(a, c, gam, lig, active, rows, hprev);
+            return;
+        }
+    }
+    stream_piece<NC, SMEMG, BWD, UNR, HS>(a, c, gam, lig, active, rows, hprev);
 }
 
 // ------------------------------------------------------------ part B
@@ -1189,11 +1277,7 @@ __device__ __forceinline__ void publish_carry(const KArgs &a, const Cta &c, unsi
 
 template <int THREADS, int NC, bool SMEMG, bool BWD>
 __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a) {
-    // edges per gather batch: more loads in flight per lane measured slower
-    // (the L2 path congests); for NC = 2 three per batch measured fastest in
-    // the forward and four in the backward (whose dot-product butterfly wants
-    // a power of two)
-    constexpr int UNR = BWD ? (NC == 2 ? 4 : 2) : (NC == 2 ? 3 : 4);
+    constexpr int UNR = edge_batch(BWD, NC);
     __shared__ int s_ok, s_meta[8];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1381,9 +1465,9 @@ __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a)
             // finish operands committed after it may still be in flight
             cp_async_wait_but_last();
             __syncthreads();
-            stream_piece<NC, SMEMG, BWD, UNR, true>(a, c, gam, lig, active, rows, hrow(a, s));
+            part_a<NC, SMEMG, BWD, UNR, true>(a, c, gam, lig, active, rows, hrow(a, s));
         } else {
-            stream_piece<NC, SMEMG, BWD, UNR, false>(a, c, gam, lig, active, rows, hrow(a, s));
+            part_a<NC, SMEMG, BWD, UNR, false>(a, c, gam, lig, active, rows, hrow(a, s));
         }
         if (c.stage) cp_async_wait_all();
         __syncthreads();
@@ -1910,6 +1994,23 @@ SmemLayout smem_layout(const Plan &p, int dir, bool want_graph, bool want_stage,
     L.o_st4 = (int)o; o += dir == 1 ? sb : 0;
     L.o_acc = (int)o; o = align16(o + (L.stage && dir == 1 ? 8 * 32 * (size_t)rc : 0));
     L.o_inp = (int)o; o = align16(o + (L.stage ? 4 * (size_t)rc : 0));
+    // a streamed graph's cp.async ring, in what is left: the largest of a few
+    // (chunks, log2 batches per chunk) shapes that fits
+    L.o_ring = (int)o;
+    L.ring_n = L.ring_chb_sh = 0;
+    if (!L.graph && kStreamRing) {
+        const int unr = edge_batch(dir == 1, p.NC);
+        static const int shapes[4][2] = {{4, 2}, {4, 1}, {2, 1}, {2, 0}};
+        for (const auto &sh : shapes) {
+            const size_t b = 8 * (size_t)p.groups * sh[0] * ((size_t)unr << sh[1]);
+            if (o + b <= budget) {
+                L.ring_n = sh[0];
+                L.ring_chb_sh = sh[1];
+                o = align16(o + b);
+                break;
+            }
+        }
+    }
     L.bytes = o;
     return L;
 }
@@ -2013,6 +2114,9 @@ void fill_common(KArgs &k, const ck_graph *g, const Plan &p, void *scratch, int 
     k.timeout_ns = (unsigned long long)options().timeout_ns;
     k.bounds_probe = options().bounds_probe;
     k.o_chunk = L.o_chunk;
+    k.o_ring = L.o_ring;
+    k.ring_n = L.ring_n;
+    k.ring_chb_sh = L.ring_chb_sh;
     if (p.tiled) {
         const Tiled &t = g->tiled[dir];
         k.P = p.tP[dir];
