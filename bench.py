@@ -16,6 +16,9 @@ shape that the headline is quoted on); --microsteps overrides its M.
 host memory, read by the kernels over the CPU-GPU link.  --recompute times the
 checkpointing forward and the recomputing backward instead of the regular
 pair.  --ncu-steps K only runs K steps (for a profiler) and exits.
+--barrier-probe times the grid-barrier schemes of ck_probe_grid_barrier on their
+own (ns per crossing, 304 CTAs each writing 16 rows per crossing, and the
+uncontended single-CTA floor) and prints one JSON line instead of the bench line.
 
 With N > 1 (under torchrun) every rank runs an independent replica of the
 same step (the method has no exchange between replicas): weak scaling.
@@ -411,6 +414,51 @@ def l2_read_sweep(timed, buf, sink):
     return out
 
 
+BARRIER_CASES = [
+    # (scheme, CTAs per SM (0: a single CTA), cluster)
+    ("BARRIER_COUNTER", 0, 1), ("BARRIER_COUNTER", 1, 1), ("BARRIER_COUNTER", 2, 1),
+    ("BARRIER_COUNTER_RETURNING", 2, 1), ("BARRIER_COUNTER_RELAXED", 2, 1),
+    ("BARRIER_FLAG", 2, 1), ("BARRIER_FLAGS8", 2, 1),
+    ("BARRIER_CLUSTER_SYNC", 2, 2), ("BARRIER_CLUSTER_SYNC", 2, 8),
+    ("BARRIER_CLUSTER_MBARRIER", 2, 2), ("BARRIER_CLUSTER_MBARRIER", 2, 8),
+]
+
+
+def run_barrier_probe(crossings=4000, rows_per_cta=16):
+    """`--barrier-probe`: ns per grid-barrier crossing for each scheme, timed
+    with CUDA events on the launching stream (second of two runs)."""
+    import torch
+
+    from sparse_graph_recurrent_gb300 import _ck
+    dev = torch.device("cuda", 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = torch.zeros(2 * sms * rows_per_cta * 32, dtype=torch.float32, device=dev)
+    words = torch.zeros(_ck.PROBE_BARRIER_WORDS, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = []
+    for name, cps, cluster in BARRIER_CASES:
+        ctas = 1 if cps == 0 else cps * sms
+        rec = {"scheme": name.lower(), "ctas": ctas, "cluster": cluster}
+        try:
+            ns = None
+            for _ in range(2):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                _ck.ck_probe_grid_barrier(getattr(_ck, name), ctas, cluster, crossings,
+                                          rows_per_cta, rows, words, status)
+                e1.record()
+                torch.cuda.synchronize()
+                if int(status.item()) != 0:
+                    raise RuntimeError("a wait ran out")
+                ns = e0.elapsed_time(e1) * 1e6 / crossings
+            rec["ns_per_crossing"] = round(ns, 1)
+        except (_ck.CKError, RuntimeError) as ex:
+            rec["error"] = str(ex)
+        out.append(rec)
+    print(json.dumps({"barrier_probe": out, "crossings": crossings, "rows_per_cta": rows_per_cta,
+                      "threads_per_cta": 256, "gpu": torch.cuda.get_device_name(0)}))
+
+
 def run_plain_steps(args, c):
     """`--ncu-steps K`: K forward + backward steps through the public API and
     nothing else (no probes, no timing), for a profiler to capture; prints one
@@ -664,7 +712,12 @@ def main():
                     help="time the checkpointing forward and the recomputing backward")
     ap.add_argument("--ncu-steps", type=int, default=0,
                     help="run this many steps and nothing else (for a profiler), then exit")
+    ap.add_argument("--barrier-probe", action="store_true",
+                    help="time the grid-barrier schemes on their own and exit")
     args = ap.parse_args()
+    if args.barrier_probe:
+        run_barrier_probe()
+        return
 
     import workloads
     c = workloads.make(args.config, M=args.microsteps)

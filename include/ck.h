@@ -412,6 +412,38 @@ ck_status ck_probe_read_shape(const void *buf, size_t bytes, int64_t reps, int64
                               int64_t depth, int64_t threads, int64_t ctas_per_sm, float *sink,
                               void *stream);
 
+/*
+ * ck_probe_grid_barrier -- times one grid-barrier scheme on its own (no
+ * counterpart on the pages: it measures the latency under every microstep of
+ * the persistent kernels).  `ctas` co-resident CTAs of 256 threads each cross
+ * `crossings` barriers; before each crossing every CTA writes rows_per_cta
+ * (0..64) rows of 32 floats to (device) `rows`, float[ctas * rows_per_cta * 32]
+ * (may be NULL when rows_per_cta is 0).  `words` is (device)
+ * uint32[CK_PROBE_BARRIER_WORDS] and `status` (device) int32[1]; the call
+ * clears both on `stream`.  `cluster` is 1, or 2, 4 or 8 for the cluster
+ * schemes (then ctas must be a multiple of it).  Every wait gives up after
+ * CK_OPT_BARRIER_TIMEOUT_NS and sets *status to 1, and all CTAs then stop.
+ * Asynchronous: time it with events on `stream`, then read *status.
+ * Errors: CK_ERR_INVALID_ARG for an argument outside these sets,
+ * CK_ERR_UNSUPPORTED when the CTAs cannot all be resident at once.
+ */
+#define CK_PROBE_BARRIER_WORDS 16384
+typedef enum {
+    CK_BARRIER_COUNTER = 0,           /* the recurrence kernels' barrier: one release add per CTA
+                                         on a counter, one thread per CTA polls it (acquire) */
+    CK_BARRIER_COUNTER_RETURNING = 1, /* the add returns the count; the last CTA skips the poll */
+    CK_BARRIER_COUNTER_RELAXED = 2,   /* relaxed polls, an acquire fence once the count is seen */
+    CK_BARRIER_FLAG = 3,              /* the last CTA (returning add) writes a release flag that
+                                         the others poll, apart from the counter */
+    CK_BARRIER_FLAGS8 = 4,            /* as 3 with eight flag copies, each polled by 1/8 of the CTAs */
+    CK_BARRIER_CLUSTER_SYNC = 5,      /* hardware cluster barrier, then one arrival per cluster */
+    CK_BARRIER_CLUSTER_MBARRIER = 6   /* remote mbarrier arrivals on the cluster leader's shared
+                                         memory (bounded waits), one arrival per cluster */
+} ck_barrier_scheme;
+ck_status ck_probe_grid_barrier(int64_t scheme, int64_t ctas, int64_t cluster, int64_t crossings,
+                                int64_t rows_per_cta, float *rows, uint32_t *words, int32_t *status,
+                                void *stream);
+
 const char *ck_status_string(ck_status s);
 const char *ck_last_error_message(void);
 

@@ -21,6 +21,10 @@ STATUS = {0: "CK_OK", 1: "CK_ERR_INVALID_ARG", 2: "CK_ERR_CUDA", 3: "CK_ERR_OUT_
 (OPT_PERSISTENT, OPT_BARRIER_TIMEOUT_NS, OPT_TEST_BARRIER_EXTRA, OPT_GRAPH_IN_SMEM,
  OPT_RECOMPUTE_STEPS, OPT_ROWS_IN_SMEM, OPT_TEST_BOUNDS_PROBE, OPT_TILED) = range(8)
 GRAPH_EDGES_IN_HOST_MEMORY = 1  # ck_graph_flag
+# ck_barrier_scheme (ck_probe_grid_barrier)
+(BARRIER_COUNTER, BARRIER_COUNTER_RETURNING, BARRIER_COUNTER_RELAXED, BARRIER_FLAG,
+ BARRIER_FLAGS8, BARRIER_CLUSTER_SYNC, BARRIER_CLUSTER_MBARRIER) = range(7)
+PROBE_BARRIER_WORDS = 16384
 
 _lib = None
 
@@ -77,6 +81,7 @@ def load() -> ctypes.CDLL:
         "ck_probe_read": [p, sz, i64, p, p],
         "ck_probe_gather": [p, i64, i64, p, i64, p, p],
         "ck_probe_read_shape": [p, sz, i64, i64, i64, i64, i64, p, p],
+        "ck_probe_grid_barrier": [i64, i64, i64, i64, i64, p, p, p, p],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -315,6 +320,21 @@ def ck_probe_read_shape(buf, reps, load_bytes, depth, threads, ctas_per_sm, sink
     _check(load().ck_probe_read_shape(_ptr(buf), buf.numel() * buf.element_size(), reps,
                                       load_bytes, depth, threads, ctas_per_sm, _ptr(sink),
                                       _stream(stream)))
+
+
+def ck_probe_grid_barrier(scheme, ctas, cluster, crossings, rows_per_cta, rows, words, status,
+                          stream=None):
+    _need(words, torch.int32, "words")
+    _need(status, torch.int32, "status")
+    if words.numel() < PROBE_BARRIER_WORDS or status.numel() < 1:
+        raise ValueError(f"words needs {PROBE_BARRIER_WORDS} elements, status one")
+    if rows_per_cta > 0:
+        _need(rows, torch.float32, "rows")
+        if rows.numel() < ctas * rows_per_cta * 32:
+            raise ValueError("rows holds fewer than ctas * rows_per_cta * 32 floats")
+    _check(load().ck_probe_grid_barrier(scheme, ctas, cluster, crossings, rows_per_cta,
+                                        _ptr(rows) if rows_per_cta > 0 else None, _ptr(words),
+                                        _ptr(status), _stream(stream)))
 
 
 def ck_probe_gather(rows, idx, sink, stream=None):

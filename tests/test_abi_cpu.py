@@ -101,3 +101,33 @@ def test_no_cpu_fallback_without_a_device(lib):
     src = (ctypes.c_int64 * 1)(0)
     st = lib.ck_graph_create(src, src, 1, 1, None, 0, None, ctypes.byref(h))
     assert st == 2 and not h.value  # CK_ERR_CUDA, no handle
+
+
+def test_binding_constants_match_the_header():
+    """The binding's option, scheme and size constants are the header's."""
+    from sparse_graph_recurrent_gb300 import _ck
+    text = open(os.path.join(ROOT, "include", "ck.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+
+    def enum_values(prefix):
+        vals = {}
+        for name, val in re.findall(r"\b(" + prefix + r"[A-Z_0-9]+)\s*=\s*(\d+)", text):
+            vals[name] = int(val)
+        return vals
+
+    schemes = enum_values("CK_BARRIER_")
+    assert len(schemes) == 7
+    for name, val in schemes.items():
+        assert getattr(_ck, name[len("CK_"):]) == val, name
+    opts = enum_values("CK_OPT_")
+    for name, val in opts.items():
+        assert getattr(_ck, "OPT_" + name[len("CK_OPT_"):]) == val, name
+    words = re.search(r"#define\s+CK_PROBE_BARRIER_WORDS\s+(\d+)", text)
+    assert words and int(words.group(1)) == _ck.PROBE_BARRIER_WORDS
+
+
+def test_barrier_probe_refuses_bad_arguments_on_the_host(lib):
+    """Argument checks come before any CUDA call (this runs without a GPU)."""
+    assert lib.ck_probe_grid_barrier(9, 8, 1, 10, 0, None, None, None, None) == 1
+    assert lib.ck_probe_grid_barrier(0, 8, 4, 10, 0, None, None, None, None) == 1
+    assert b"scheme" in lib.ck_last_error_message()
