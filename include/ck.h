@@ -84,9 +84,9 @@ ck_status ck_graph_create(const int64_t *src, const int64_t *dst, int64_t E, int
                           const int64_t *input_nodes, int64_t n_in, void *stream,
                           ck_graph **out);
 
-/* Graph residency flags for ck_graph_create_flags. */
+/* Graph flags for ck_graph_create_flags. */
 typedef enum {
-    CK_GRAPH_EDGES_IN_HOST_MEMORY = 1  /* the arrays indexed by edge (col, perm and each edge's
+    CK_GRAPH_EDGES_IN_HOST_MEMORY = 1, /* the arrays indexed by edge (col, perm and each edge's
                                           row, both directions: 24 bytes per edge) go to pinned
                                           host memory that the kernels read in place over the
                                           CPU-GPU link (NVLink-C2C on a Grace-Blackwell node);
@@ -97,11 +97,16 @@ typedef enum {
                                           or stream every microstep.  The connectome runtime
                                           page ("Why this runtime") makes graph residency an
                                           explicit choice in the same way. */
+    CK_GRAPH_TILING = 2                /* also build the shared-memory tilings (ck_graph_tiling)
+                                          that the tiled kernels (CK_OPT_TILED) need: three more
+                                          int32 arrays per edge and direction, built on the host.
+                                          Without it a graph has no tiling and every call runs
+                                          the L2-gather kernels. */
 } ck_graph_flag;
 
 /*
- * ck_graph_create_flags -- ck_graph_create with residency flags (a bitwise OR
- * of ck_graph_flag values; 0 is ck_graph_create).  Errors: as ck_graph_create,
+ * ck_graph_create_flags -- ck_graph_create with flags (a bitwise OR of
+ * ck_graph_flag values; 0 is ck_graph_create).  Errors: as ck_graph_create,
  * plus CK_ERR_INVALID_ARG for an unknown flag bit and CK_ERR_UNSUPPORTED when
  * pinned host memory is not mapped at the same address on the device.
  */
@@ -138,8 +143,9 @@ ck_status ck_graph_export(const ck_graph *g, int32_t *row_ptr, int32_t *col, int
  * t = g * C + j owns cell (g, j): the edges of block g whose column lies in
  * chunk j, in row order.  info receives {C, G, P = G * C, most rows in a block,
  * most rows a CTA finishes, most nodes in a chunk, most edges in a cell, length
- * of the row-pointer array}; all zero when the direction has no tiling (graphs
- * whose state rows do not fit eight CTAs' shared memory).
+ * of the row-pointer array}; all zero when the direction has no tiling (a
+ * graph created without CK_GRAPH_TILING, or one whose state rows do not fit
+ * eight CTAs' shared memory).
  */
 ck_status ck_graph_tiling(const ck_graph *g, int dir, int64_t info[8]);
 
@@ -372,7 +378,8 @@ typedef enum {
                                        sees the report; no effect in the ordinary build
                                        (default 0) */
     CK_OPT_TILED = 7                /* 1: when the graph has a shared-memory tiling
-                                       (ck_graph_tiling) and the padded batch is at most 32
+                                       (created with CK_GRAPH_TILING and small enough;
+                                       ck_graph_tiling) and the padded batch is at most 32
                                        columns, run the tiled kernels; 0 (default): always
                                        the L2-gather kernels.  ck_workspace_size and the
                                        calls after it must see the same value */

@@ -27,10 +27,12 @@ class SparseGraph:
     caller's edge order.  With edges_in_host_memory the arrays indexed by edge
     (24 bytes per edge) live in pinned host memory that the kernels read in
     place over the CPU-GPU link, leaving O(N) of the graph on the device;
-    results are bitwise the same.
+    results are bitwise the same.  With tiling the graph also holds the
+    shared-memory tilings the opt-in tiled kernels need (CK_OPT_TILED).
     """
 
-    def __init__(self, src, dst, num_nodes: int, input_nodes, edges_in_host_memory: bool = False):
+    def __init__(self, src, dst, num_nodes: int, input_nodes, edges_in_host_memory: bool = False,
+                 tiling: bool = False):
         if src.shape != dst.shape or src.dim() != 1:
             raise ValueError("src and dst must be 1-D and of equal length")
         self.device = src.device
@@ -38,7 +40,9 @@ class SparseGraph:
         self.num_edges = int(src.numel())
         self.num_inputs = int(input_nodes.numel())
         self.edges_in_host_memory = bool(edges_in_host_memory)
-        flags = _ck.GRAPH_EDGES_IN_HOST_MEMORY if self.edges_in_host_memory else 0
+        self.tiling = bool(tiling)
+        flags = ((_ck.GRAPH_EDGES_IN_HOST_MEMORY if self.edges_in_host_memory else 0) |
+                 (_ck.GRAPH_TILING if self.tiling else 0))
         with torch.cuda.device(self.device):
             self._h = _ck.ck_graph_create(src.contiguous(), dst.contiguous(), self.num_nodes,
                                           input_nodes.contiguous(), flags=flags)

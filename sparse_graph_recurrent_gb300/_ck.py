@@ -20,7 +20,7 @@ STATUS = {0: "CK_OK", 1: "CK_ERR_INVALID_ARG", 2: "CK_ERR_CUDA", 3: "CK_ERR_OUT_
           7: "CK_ERR_UNSUPPORTED"}
 (OPT_PERSISTENT, OPT_BARRIER_TIMEOUT_NS, OPT_TEST_BARRIER_EXTRA, OPT_GRAPH_IN_SMEM,
  OPT_RECOMPUTE_STEPS, OPT_ROWS_IN_SMEM, OPT_TEST_BOUNDS_PROBE, OPT_TILED) = range(8)
-GRAPH_EDGES_IN_HOST_MEMORY = 1  # ck_graph_flag
+GRAPH_EDGES_IN_HOST_MEMORY, GRAPH_TILING = 1, 2  # ck_graph_flag
 # ck_barrier_scheme (ck_probe_grid_barrier)
 (BARRIER_COUNTER, BARRIER_COUNTER_RETURNING, BARRIER_COUNTER_RELAXED, BARRIER_FLAG,
  BARRIER_FLAGS8, BARRIER_CLUSTER_SYNC, BARRIER_CLUSTER_MBARRIER) = range(7)

@@ -121,7 +121,7 @@ ck_status ck_graph_create_flags(const int64_t *src, const int64_t *dst, int64_t 
                                 void *stream, ck_graph **out) {
     if (!out) return fail(CK_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
-    if (flags & ~(uint32_t)CK_GRAPH_EDGES_IN_HOST_MEMORY)
+    if (flags & ~(uint32_t)(CK_GRAPH_EDGES_IN_HOST_MEMORY | CK_GRAPH_TILING))
         return fail(CK_ERR_INVALID_ARG, "unknown graph flag bits 0x%x", (unsigned)flags);
     if (N < 1 || N >= ((int64_t)1 << 31) - 1) return fail(CK_ERR_INVALID_ARG, "N must be in [1, 2^31 - 1)");
     if (E < 0 || E >= ((int64_t)1 << 31) - 1) return fail(CK_ERR_INVALID_ARG, "E must be in [0, 2^31 - 1)");

@@ -561,10 +561,10 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
             }
         }
     }
-    // Shared-memory tilings (ck::Tiled), one per direction, for graphs whose
-    // state rows fit a few CTAs' shared memory: built on the host from the
-    // compressed rows.
-    {
+    // Shared-memory tilings (ck::Tiled), one per direction, when the caller asks
+    // for them and the graph's state rows fit a few CTAs' shared memory: built
+    // on the host from the compressed rows.
+    if (graph_flags & CK_GRAPH_TILING) {
         CK_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize (graph build)");
         std::vector<int> rp(N + 1), cl((size_t)E), pm((size_t)E);
         const int *rps[2] = {g->row_ptr, g->rowT_ptr};

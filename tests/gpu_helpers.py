@@ -14,9 +14,16 @@ def to_dev(a, dev="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
 
-def make_graph(c):
+def make_graph(c, tiling=None):
+    """The graph of case c; with its shared-memory tilings when `tiling`, by
+    default whenever the tiled kernels are switched on (CK_OPT_TILED), so that
+    a test selecting them runs them where the graph allows."""
     import sparse_graph_recurrent_gb300 as pkg
-    return pkg.SparseGraph(to_dev(c["src"]), to_dev(c["dst"]), c["N"], to_dev(c["input_nodes"]))
+    from sparse_graph_recurrent_gb300 import _ck
+    if tiling is None:
+        tiling = _ck.ck_get_option(_ck.OPT_TILED) != 0
+    return pkg.SparseGraph(to_dev(c["src"]), to_dev(c["dst"]), c["N"], to_dev(c["input_nodes"]),
+                           tiling=tiling)
 
 
 def run_gpu(c, M=None, graph=None, dout=None):

@@ -84,13 +84,16 @@ def test_graph_create_rejects_bad_sizes_before_cuda(lib):
     assert lib.ck_graph_create(None, None, 3, 4, None, 0, None, ctypes.byref(h)) == 1  # NULL src
     assert b"NULL" in lib.ck_last_error_message()
     assert lib.ck_workspace_size(None, 1, 1, 1, None, None) == 1
-    # residency flags: unknown bits refused before any CUDA call
+    # graph flags: unknown bits refused before any CUDA call
     f = lib.ck_graph_create_flags
     f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                   ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
-    assert f(None, None, 0, 4, None, 0, 2, None, ctypes.byref(h)) == 1
-    assert b"flag" in lib.ck_last_error_message()
-    assert f(None, None, 0, 0, None, 0, 1, None, ctypes.byref(h)) == 1  # N < 1, valid flag
+    for bad in (4, 8, 1 << 31, 7):
+        assert f(None, None, 0, 4, None, 0, bad, None, ctypes.byref(h)) == 1
+        assert b"flag" in lib.ck_last_error_message()
+    for ok in (1, 2, 3):  # valid flags: the call gets as far as the size check (N < 1)
+        assert f(None, None, 0, 0, None, 0, ok, None, ctypes.byref(h)) == 1
+        assert b"flag" not in lib.ck_last_error_message()
 
 
 def test_no_cpu_fallback_without_a_device(lib):

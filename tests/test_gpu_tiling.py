@@ -100,7 +100,7 @@ CASES = [
 @pytest.mark.parametrize("seed,N,E,n_in,B,T,M,extra", CASES, ids=[f"N{c[1]}_E{c[2]}" for c in CASES])
 def test_tiling_matches_compressed_rows(seed, N, E, n_in, B, T, M, extra):
     c = workloads.small(seed, N, E, n_in, B, T, M, **extra)
-    g = make_graph(c)
+    g = make_graph(c, tiling=True)
     g.E = c["E"]
     for d in (0, 1):
         info, t = _export(g, d)
@@ -111,7 +111,7 @@ def test_tiling_matches_compressed_rows(seed, N, E, n_in, B, T, M, extra):
 @pytest.mark.slow
 def test_tiling_flygpt_shape():
     c = workloads.make(1)
-    g = make_graph(c)
+    g = make_graph(c, tiling=True)
     g.E = c["E"]
     for d in (0, 1):
         info, t = _export(g, d)
@@ -124,6 +124,32 @@ def test_no_tiling_for_the_wide_graph():
     no tiling (its calls run the L2-gather kernels)."""
     from sparse_graph_recurrent_gb300 import _ck
     c = workloads.small(806, 20000, 60000, 8, 4, 1, 1)
-    g = make_graph(c)
+    g = make_graph(c, tiling=True)
     for d in (0, 1):
         assert _ck.ck_graph_tiling(g.handle, d)["C"] == 0
+
+
+def test_tiling_is_built_only_on_request():
+    """A graph holds tilings only when created with CK_GRAPH_TILING (three int32
+    arrays per edge and direction, plus O(N) tables); without them the tiled
+    option runs the L2-gather kernels, bit for bit what the option off gives."""
+    from sparse_graph_recurrent_gb300 import _ck
+    from gpu_helpers import run_gpu
+    c = workloads.small(807, 700, 40000, 12, 20, 4, 2, hub_deg=9000)
+    plain, tiled = make_graph(c, tiling=False), make_graph(c, tiling=True)
+    for d in (0, 1):
+        assert _ck.ck_graph_tiling(plain.handle, d)["C"] == 0
+        assert _ck.ck_graph_tiling(tiled.handle, d)["C"] > 0
+    dev_plain, _ = _ck.ck_graph_memory(plain.handle)
+    dev_tiled, _ = _ck.ck_graph_memory(tiled.handle)
+    assert dev_tiled - dev_plain >= 2 * 3 * 4 * c["E"]
+    try:
+        _ck.ck_set_option(_ck.OPT_TILED, 0)
+        off_out, off = run_gpu(c, graph=plain)
+        _ck.ck_set_option(_ck.OPT_TILED, 1)
+        on_out, on = run_gpu(c, graph=plain)
+    finally:
+        _ck.ck_set_option(_ck.OPT_TILED, 0)
+    np.testing.assert_array_equal(on_out, off_out)
+    for k in off:
+        np.testing.assert_array_equal(on[k], off[k])
