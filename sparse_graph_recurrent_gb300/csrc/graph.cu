@@ -240,13 +240,28 @@ struct Cut {
     int max_rows = 0, max_edges = 0;
 };
 
+// CTAs P/2 .. P-1 are the second of their SM's two to be dispatched, and on
+// the same work they finish 2-4% later than the first (per-CTA timings, both
+// directions, across boxes and with the pieces rotated: the delay follows the
+// block, not its data or its SM).  Their pieces get kLateShare per mille less
+// of the weighted items, the first half's as much more.
+constexpr int kLateShare = 15;
+
+// Sum of the shares of pieces [0, c), in per mille of an even share.
+long long share_prefix(int c, int P) {
+    const int h = P / 2;
+    return c <= h ? (long long)c * (1000 + kLateShare)
+                  : (long long)h * (1000 + kLateShare) + (long long)(c - h) * (1000 - kLateShare);
+}
+
 Cut cut_pieces(const std::vector<int> &rp, int N, int E, int P, int wt) {
     Cut k;
     k.r.resize(P + 1);
     k.e.resize(P + 1);
     const long long items = (long long)E + (long long)wt * N;
+    const long long total = share_prefix(P, P);
     for (int c = 0; c <= P; ++c) {
-        const long long d = (long long)c * items / P;
+        const long long d = c == P ? items : items * share_prefix(c, P) / total;
         int lo = 0, hi = N;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -266,13 +281,16 @@ Cut cut_pieces(const std::vector<int> &rp, int N, int E, int P, int wt) {
 }
 
 // Estimated time of the slowest piece, for choosing the row weight: part A
-// grows with a piece's edges, part B with the finish passes its rows need.
+// grows with a piece's edges, part B with the finish passes its rows need; the
+// second-dispatched half runs slower by the factor its smaller share offsets.
 double cut_cost(const Cut &k, int P, int pass_rows, double edge_us, double pass_us) {
     double worst = 0.0;
+    const double late = (1000.0 + kLateShare) / (1000.0 - kLateShare);
     for (int c = 0; c < P; ++c) {
         const int rows = k.r[c + 1] - k.r[c], edges = k.e[c + 1] - k.e[c];
         const int passes = (rows + pass_rows - 1) / pass_rows;
-        worst = std::max(worst, edges * edge_us + (passes > 0 ? passes : 1) * pass_us);
+        const double t = edges * edge_us + (passes > 0 ? passes : 1) * pass_us;
+        worst = std::max(worst, c >= P / 2 ? t * late : t);
     }
     return worst;
 }

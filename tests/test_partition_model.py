@@ -5,8 +5,10 @@ for the row it ends inside), on the FlyGPT-shaped graph and on random graphs,
 for row-weighted merge-path pieces of several weights.
 
 The model follows the kernel's rules: piece c starts at diagonal
-c (E + w N) / P (rows whose ends come first, edges between their row
-pointers); lane group g of G takes edges [e0 + g n / G, e0 + (g+1) n / G); a
+(E + w N) S(c) / S(P), where S(c) sums the shares of pieces [0, c): 1000 + L
+per mille for the first half, 1000 - L for the second (the graph build's
+late-dispatch share L), so L = 0 is the even cut c (E + w N) / P (rows whose
+ends come first, edges between their row pointers); lane group g of G takes edges [e0 + g n / G, e0 + (g+1) n / G); a
 group's carry belongs to the row of its last edge (an empty group takes the
 row of edge k0); groups of a warp (EPW of them) with the same row add their
 carries by a segmented suffix sum, so a row spanning groups [ga, gb) reads
@@ -29,11 +31,21 @@ def _piece(row_ptr, N, w, d):
     return lo, min(d - w * lo, row_ptr[min(lo + 1, N)])
 
 
-def _check(row_ptr, N, E, P, G, EPW, w, rng):
+def _share_prefix(c, P, late):
+    h = P // 2
+    return c * (1000 + late) if c <= h else h * (1000 + late) + (c - h) * (1000 - late)
+
+
+def _diagonal(c, P, items, late):
+    return items if c == P else items * _share_prefix(c, P, late) // _share_prefix(P, P, late)
+
+
+def _check(row_ptr, N, E, P, G, EPW, w, rng, late=15):
     items = E + w * N
     rowid = np.repeat(np.arange(N), np.diff(row_ptr))
     for cta in range(P):
-        (r0, e0), (r1, e1) = _piece(row_ptr, N, w, cta * items // P), _piece(row_ptr, N, w, (cta + 1) * items // P)
+        (r0, e0) = _piece(row_ptr, N, w, _diagonal(cta, P, items, late))
+        (r1, e1) = _piece(row_ptr, N, w, _diagonal(cta + 1, P, items, late))
         n, nrows = e1 - e0, r1 - r0
         assert row_ptr[r0] <= e0 <= e1 and nrows >= 0
         carry = np.zeros(G, np.int64)
@@ -97,7 +109,8 @@ def test_flygpt_pieces_and_carries():
         # the cost model picks for this graph (16 forward, 1 backward) and 3
         for P, G in ((304, 64), (152, 128)):
             for w in (1, 3, 16):
-                _check(rp, N, int(rp[-1]), P, G, 8, w, rng)
+                for late in (0, 15):
+                    _check(rp, N, int(rp[-1]), P, G, 8, w, rng, late)
 
 
 def test_random_graphs_pieces_and_carries():
@@ -110,4 +123,17 @@ def test_random_graphs_pieces_and_carries():
         G = EPW * int(rng.integers(1, 5))
         deg = rng.multinomial(E, rng.dirichlet(np.ones(N) * rng.choice([0.05, 1.0])))
         rp = np.concatenate([[0], np.cumsum(deg)])
-        _check(rp, N, E, P, G, EPW, int(rng.choice([1, 2, 3, 4, 8, 16])), rng)
+        _check(rp, N, E, P, G, EPW, int(rng.choice([1, 2, 3, 4, 8, 16])), rng,
+               int(rng.choice([0, 15, 400])))
+
+
+def test_late_share_cut():
+    """The shares: the second half's pieces carry (1000 - L) / (1000 + L) of the
+    first half's weighted items (to rounding), the diagonals rise and end at
+    the total."""
+    items, P, late = 604_324, 304, 15
+    d = [_diagonal(c, P, items, late) for c in range(P + 1)]
+    assert d[0] == 0 and d[-1] == items and all(a <= b for a, b in zip(d, d[1:]))
+    first = np.diff(d[: P // 2 + 1]).mean()
+    second = np.diff(d[P // 2:]).mean()
+    assert abs(second / first - 985 / 1015) < 1e-4
