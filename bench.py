@@ -19,6 +19,9 @@ pair.  --ncu-steps K only runs K steps (for a profiler) and exits.
 --barrier-probe times the grid-barrier schemes of ck_probe_grid_barrier on their
 own (ns per crossing, 304 CTAs each writing 16 rows per crossing, and the
 uncontended single-CTA floor) and prints one JSON line instead of the bench line.
+--phase-profile loads the profiling build (libck_prof.so) and prints, for the
+workload, the mean and slowest-CTA time of each phase of a microstep (part A,
+the CTA sync, the finish, the grid barrier) instead of the bench line.
 
 With N > 1 (under torchrun) every rank runs an independent replica of the
 same step (the method has no exchange between replicas): weak scaling.
@@ -459,6 +462,49 @@ def run_barrier_probe(crossings=4000, rows_per_cta=16):
                       "threads_per_cta": 256, "gpu": torch.cuda.get_device_name(0)}))
 
 
+def run_phase_profile(args, c, steps=5):
+    """`--phase-profile`: per-phase microstep times from the profiling build
+    (ck_phase_profile_read), over `steps` forward + backward steps after one
+    warm-up step."""
+    import torch
+
+    import sparse_graph_recurrent_gb300 as pkg
+    from sparse_graph_recurrent_gb300 import _ck
+    if _ck.library_variant() != "prof":
+        raise SystemExit("--phase-profile needs CK_LIBRARY_VARIANT=prof before the library loads")
+    dev = torch.device("cuda", 0)
+    tt = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    g = pkg.SparseGraph(tt(c["src"]), tt(c["dst"]), c["N"], tt(c["input_nodes"]),
+                        edges_in_host_memory=args.graph_in_host_memory)
+    w, leak, bias, drives, state0, dout = (tt(c[k]) for k in ("w", "leak", "bias", "drives",
+                                                              "state0", "dout"))
+    B, T, M = c["B"], c["T"], c["M"]
+    for i in range(steps + 1):
+        if i == 1:
+            _ck.ck_phase_profile_read(clear=True)
+        _, saved, scratch = pkg.forward(g, w, leak, bias, drives, state0, M)
+        pkg.backward(g, w, leak, B, T, M, saved, dout, scratch)
+    _ck.ck_query_status(scratch)
+    data = _ck.ck_phase_profile_read(clear=True)
+    out = {}
+    for d, name in ((0, "forward"), (1, "backward")):
+        ctas = [q for q in data[d] if q[4] > 0]
+        per = {
+            "part_a": [q[0] / q[4] / 1e3 for q in ctas],
+            "cta_sync": [(q[1] - q[0]) / q[4] / 1e3 for q in ctas],
+            "finish": [q[2] / q[4] / 1e3 for q in ctas],
+            "part_a_sync_finish": [(q[1] + q[2]) / q[4] / 1e3 for q in ctas],
+            "barrier": [q[3] / q[5] / 1e3 for q in ctas if q[5] > 0],
+        }
+        out[name] = {"ctas": len(ctas), "microsteps_per_cta": ctas[0][4] // steps if ctas else 0,
+                     **{k: {"mean_us": round(statistics.fmean(v), 3), "slowest_cta_us": round(max(v), 3)}
+                        for k, v in per.items() if v}}
+    print(json.dumps({"phase_profile": out, "steps": steps, "library": "libck_prof.so",
+                      "config": {"workload": _workload_name(c)},
+                      "note": "per CTA, mean over its microsteps; %globaltimer stamps add one CTA "
+                              "sync per microstep"}))
+
+
 def run_plain_steps(args, c):
     """`--ncu-steps K`: K forward + backward steps through the public API and
     nothing else (no probes, no timing), for a profiler to capture; prints one
@@ -714,7 +760,11 @@ def main():
                     help="run this many steps and nothing else (for a profiler), then exit")
     ap.add_argument("--barrier-probe", action="store_true",
                     help="time the grid-barrier schemes on their own and exit")
+    ap.add_argument("--phase-profile", action="store_true",
+                    help="per-phase microstep times from the profiling build, then exit")
     args = ap.parse_args()
+    if args.phase_profile:
+        os.environ["CK_LIBRARY_VARIANT"] = "prof"  # before the library first loads
     if args.barrier_probe:
         run_barrier_probe()
         return
@@ -732,6 +782,9 @@ def main():
         return
     if args.ncu_steps > 0:
         run_plain_steps(args, c)
+        return
+    if args.phase_profile:
+        run_phase_profile(args, c)
         return
     dist = None
     if world > 1:

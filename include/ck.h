@@ -451,6 +451,27 @@ ck_status ck_probe_grid_barrier(int64_t scheme, int64_t ctas, int64_t cluster, i
                                 int64_t rows_per_cta, float *rows, uint32_t *words, int32_t *status,
                                 void *stream);
 
+/*
+ * ck_phase_profile_read -- the per-microstep phase times of the L2-gather
+ * recurrence kernels (the tiled kernels keep none), kept only by the profiling build of this library (libck_prof.so,
+ * compiled with -DCK_PHASE_PROFILE; every other build returns
+ * CK_ERR_UNSUPPORTED without touching the device).  No counterpart on the
+ * pages: it measures where a microstep's time goes.  Synchronises the device,
+ * copies uint64 host[2][CK_PHASE_PROFILE_CTAS][CK_PHASE_PROFILE_WORDS] (index
+ * 0 forward, 1 backward; then the CTA) and, with `clear`, zeroes the counters.
+ * Per CTA, summed over microsteps and calls since the last clear
+ * (%globaltimer ns): [0] part A (the gather); [1] part A and the CTA's sync
+ * after it; [2] the finish (to its last warp); [3] the grid barrier, from
+ * arrival to release, with the work issued inside its wait; [4] microsteps;
+ * [5] barriers; [6] the SM of the last call; [7] rows << 32 | edges of
+ * the CTA's piece.  The stamps add a CTA sync after the finish, so times are
+ * close to, not equal to, the ordinary build's.  Errors: CK_ERR_INVALID_ARG
+ * for a NULL or short buffer, CK_ERR_CUDA.
+ */
+#define CK_PHASE_PROFILE_CTAS 1024
+#define CK_PHASE_PROFILE_WORDS 8
+ck_status ck_phase_profile_read(uint64_t *host, int64_t words, int64_t clear);
+
 const char *ck_status_string(ck_status s);
 const char *ck_last_error_message(void);
 

@@ -25,6 +25,7 @@ GRAPH_EDGES_IN_HOST_MEMORY, GRAPH_TILING = 1, 2  # ck_graph_flag
 (BARRIER_COUNTER, BARRIER_COUNTER_RETURNING, BARRIER_COUNTER_RELAXED, BARRIER_FLAG,
  BARRIER_FLAGS8, BARRIER_CLUSTER_SYNC, BARRIER_CLUSTER_MBARRIER) = range(7)
 PROBE_BARRIER_WORDS = 16384
+PHASE_PROFILE_CTAS, PHASE_PROFILE_WORDS = 1024, 8  # ck_phase_profile_read
 
 _lib = None
 
@@ -37,8 +38,9 @@ class CKError(RuntimeError):
 
 
 def library_variant():
-    """The library variant this process loads: None (libck.so) or "bounds"
-    (libck_bounds.so, the bounds-checked build), from CK_LIBRARY_VARIANT."""
+    """The library variant this process loads: None (libck.so), "bounds"
+    (libck_bounds.so, the bounds-checked build) or "prof" (libck_prof.so, with
+    the phase profile), from CK_LIBRARY_VARIANT."""
     return os.environ.get("CK_LIBRARY_VARIANT") or None
 
 
@@ -82,6 +84,7 @@ def load() -> ctypes.CDLL:
         "ck_probe_gather": [p, i64, i64, p, i64, p, p],
         "ck_probe_read_shape": [p, sz, i64, i64, i64, i64, i64, p, p],
         "ck_probe_grid_barrier": [i64, i64, i64, i64, i64, p, p, p, p],
+        "ck_phase_profile_read": [p, i64, i64],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -335,6 +338,19 @@ def ck_probe_grid_barrier(scheme, ctas, cluster, crossings, rows_per_cta, rows, 
     _check(load().ck_probe_grid_barrier(scheme, ctas, cluster, crossings, rows_per_cta,
                                         _ptr(rows) if rows_per_cta > 0 else None, _ptr(words),
                                         _ptr(status), _stream(stream)))
+
+
+def ck_phase_profile_read(clear: bool = True):
+    """The profiling build's phase counters as nested lists
+    [direction][CTA][word] of ints (layout in ck.h); raises CKError
+    (CK_ERR_UNSUPPORTED) in every other build."""
+    n = 2 * PHASE_PROFILE_CTAS * PHASE_PROFILE_WORDS
+    buf = (ctypes.c_uint64 * n)()
+    _check(load().ck_phase_profile_read(ctypes.cast(buf, ctypes.c_void_p), n, 1 if clear else 0))
+    flat = list(buf)
+    per = PHASE_PROFILE_CTAS * PHASE_PROFILE_WORDS
+    return [[flat[d * per + c * PHASE_PROFILE_WORDS:d * per + (c + 1) * PHASE_PROFILE_WORDS]
+             for c in range(PHASE_PROFILE_CTAS)] for d in range(2)]
 
 
 def ck_probe_gather(rows, idx, sink, stream=None):

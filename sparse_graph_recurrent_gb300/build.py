@@ -8,6 +8,10 @@ Variant "bounds" builds the same sources with -DCK_DEBUG_BOUNDS into
 _build/libck_bounds.so: every gathered row, table and carry index is checked
 on the device, and a bad one is reported through ck_query_status instead of
 being accessed.  The binding loads it when CK_LIBRARY_VARIANT=bounds.
+
+Variant "prof" (-DCK_PHASE_PROFILE, _build/libck_prof.so) adds %globaltimer
+stamps around each phase of a microstep, read with ck_phase_profile_read; the
+binding loads it when CK_LIBRARY_VARIANT=prof.
 """
 from __future__ import annotations
 
@@ -22,7 +26,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libck.so")
-VARIANTS = {None: ([], "libck.so"), "bounds": (["-DCK_DEBUG_BOUNDS"], "libck_bounds.so")}
+VARIANTS = {None: ([], "libck.so"), "bounds": (["-DCK_DEBUG_BOUNDS"], "libck_bounds.so"),
+            "prof": (["-DCK_PHASE_PROFILE"], "libck_prof.so")}
 
 
 def lib_path(variant=None) -> str:
@@ -83,8 +88,8 @@ def build(force: bool = False, verbose: bool = False, variant=None) -> str:
 
 
 def build_all(force: bool = False) -> list:
-    """Both variants, compiled side by side."""
-    with ThreadPoolExecutor(max_workers=2) as ex:
+    """Every variant, compiled side by side."""
+    with ThreadPoolExecutor(max_workers=len(VARIANTS)) as ex:
         return list(ex.map(lambda v: build(force=force, variant=v), list(VARIANTS)))
 
 

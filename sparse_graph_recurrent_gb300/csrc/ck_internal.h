@@ -106,6 +106,11 @@ __device__ __forceinline__ bool ck_in(int *err, long long i, long long n) {
 #define CK_IN(err, i, n) true
 #endif
 
+// Phase profile of the profiling build (compiled with -DCK_PHASE_PROFILE): per
+// direction and CTA, kPhaseWords counters (layout in ck.h,
+// ck_phase_profile_read).
+constexpr int kPhaseCtas = CK_PHASE_PROFILE_CTAS, kPhaseWords = CK_PHASE_PROFILE_WORDS;
+
 // Control block at the start of scratch: the barrier counter and, on its own
 // 128-byte line, the status word.
 constexpr size_t kStatusOffset = 128;

@@ -154,6 +154,12 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 }
 __device__ __forceinline__ int ld_err(const int *p) { return *(volatile const int *)p; }
 
+#ifdef CK_PHASE_PROFILE
+// The profiling build's counters, summed over microsteps and calls until read
+// and cleared (ck_phase_profile_read).
+__device__ unsigned long long g_phase[2][kPhaseCtas][kPhaseWords];
+#endif
+
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 // 32 bytes from global memory (32-byte aligned), cached in L1 and L2.
 __device__ __forceinline__ void ld_ca_v8(const float *p, float4 &lo, float4 &hi) {
@@ -1443,10 +1449,18 @@ __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a)
     };
     if (c.stage && a.s_count > 0) stage_for(a.s_first, tid, THREADS);
 
+#ifdef CK_PHASE_PROFILE
+    // this launch's phase sums, in registers until the microsteps end
+    unsigned long long ph[4] = {0, 0, 0, 0};
+    unsigned ph_steps = 0, ph_bars = 0;
+#endif
     for (int it = 0; it < a.s_count; ++it) {
         const int s = BWD ? a.s_first - it : a.s_first + it;
         const unsigned phase_id = BWD ? (unsigned)(a.S - s) : (unsigned)(s + 1);
         const float *rows = BWD ? a.da + (size_t)(s & 1) * NBp : hrow(a, s);
+#ifdef CK_PHASE_PROFILE
+        const unsigned long long tp0 = globaltimer();
+#endif
         if (!c.stage && tid == 0 && c.nrows > 0) {
             // part B's operands of this CTA's rows, fetched into L2 during part A
             const unsigned rb = (unsigned)((size_t)c.nrows * Bp * 4);
@@ -1469,11 +1483,27 @@ __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a)
         } else {
             part_a<NC, SMEMG, BWD, UNR, false>(a, c, gam, lig, active, rows, hrow(a, s));
         }
+#ifdef CK_PHASE_PROFILE
+        const unsigned long long tpa = globaltimer();
+#endif
         if (c.stage) cp_async_wait_all();
         __syncthreads();
+#ifdef CK_PHASE_PROFILE
+        const unsigned long long tp1 = globaltimer();
+#endif
         if (warp == THREADS / 32 - 2 && c.publish) publish_carry(a, c, phase_id);
         if (BWD) finish_bwd<THREADS>(a, c, pb, s, phase_id);
         else finish_fwd<THREADS>(a, c, pb, s, phase_id);
+#ifdef CK_PHASE_PROFILE
+        __syncthreads();  // the CTA's finish ends when its last warp's does
+        {
+            const unsigned long long tp2 = globaltimer();
+            ph[0] += tpa - tp0;
+            ph[1] += tp1 - tp0;
+            ph[2] += tp2 - tp1;
+            ++ph_steps;
+        }
+#endif
         if (it + 1 < a.s_count) {
             // while other CTAs finish: copy out the state that ended an input
             // step, and stage the next microstep's operands (this microstep's
@@ -1483,12 +1513,31 @@ __global__ void __launch_bounds__(THREADS, kCtasPerSm) rec_kernel(const KArgs a)
                 if (!BWD && s % a.M == a.M - 1) write_out(a, c, s / a.M, tid, THREADS);
                 stage_for(BWD ? s - 1 : s + 1, tid, THREADS);
             };
+#ifdef CK_PHASE_PROFILE
+            const unsigned long long tb0 = globaltimer();
+#endif
             if (!grid_sync(a, nbar++, &s_ok, between)) {
                 cp_async_wait_all();
                 return;
             }
+#ifdef CK_PHASE_PROFILE
+            ph[3] += globaltimer() - tb0;
+            ++ph_bars;
+#endif
         }
     }
+#ifdef CK_PHASE_PROFILE
+    if (tid == 0 && cta < kPhaseCtas) {
+        unsigned long long *q = g_phase[BWD ? 1 : 0][cta];
+        unsigned sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        for (int j = 0; j < 4; ++j) q[j] += ph[j];
+        q[4] += ph_steps;
+        q[5] += ph_bars;
+        q[6] = sm;
+        q[7] = ((unsigned long long)c.nrows << 32) | (unsigned)(c.e1 - c.e0);
+    }
+#endif
 
     if (a.do_epilogue) {
         __syncthreads();
@@ -2478,3 +2527,29 @@ ck_status launch_backward(const ck_graph *g, const Plan &p, const BwdIO &io, cud
 }
 
 }  // namespace ck
+
+using namespace ck;
+
+extern "C" ck_status ck_phase_profile_read(uint64_t *host, int64_t words, int64_t clear) {
+#ifndef CK_PHASE_PROFILE
+    (void)host;
+    (void)words;
+    (void)clear;
+    return fail(CK_ERR_UNSUPPORTED, "phase profile: only the profiling build (libck_prof.so) keeps one");
+#else
+    const size_t n = sizeof(g_phase) / sizeof(unsigned long long);
+    if (!host || words < (int64_t)n)
+        return fail(CK_ERR_INVALID_ARG, "phase profile: host buffer of %zu words needed", n);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize (phase profile)");
+    e = cudaMemcpyFromSymbol(host, g_phase, sizeof(g_phase));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol (phase profile)");
+    if (clear) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_phase);
+        if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(g_phase));
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the phase profile");
+    }
+    return CK_OK;
+#endif
+}

@@ -33,12 +33,23 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
-def test_bounds_checked_build_exports_the_same_symbols():
-    """The bounds-checked variant (libck_bounds.so) is the same ABI."""
+@pytest.mark.parametrize("variant", ["bounds", "prof"])
+def test_every_build_exports_the_same_symbols(variant):
+    """The bounds-checked (libck_bounds.so) and profiling (libck_prof.so)
+    variants are the same ABI."""
     from sparse_graph_recurrent_gb300 import build
-    lib_b = ctypes.CDLL(build.build(variant="bounds"))
+    lib_v = ctypes.CDLL(build.build(variant=variant))
     for n in sorted(_declared()):
-        assert hasattr(lib_b, n), n
+        assert hasattr(lib_v, n), n
+
+
+def test_phase_profile_only_in_the_profiling_build(lib):
+    """The ordinary build keeps no phase profile and says so without touching
+    the device (this runs without a GPU)."""
+    lib.ck_phase_profile_read.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
+    buf = (ctypes.c_uint64 * 16)()
+    assert lib.ck_phase_profile_read(ctypes.cast(buf, ctypes.c_void_p), 16, 1) == 7  # UNSUPPORTED
+    assert b"profiling build" in lib.ck_last_error_message()
 
 
 def test_status_strings(lib):
