@@ -76,7 +76,7 @@ typedef struct ck_graph ck_graph;
  * position) and the same keyed by src (rowT_ptr, colT = dst, permT), both by a
  * stable sort (equal keys keep ascending edge id), and slot[N] (k where
  * input_nodes[k] = i, else -1).  Validates every index and input-node
- * uniqueness on the device; synchronises `stream` to read the verdict.
+ * uniqueness on the device; synchronises `stream` to read the result.
  * Errors: CK_ERR_INVALID_ARG (sizes, null pointers, an index out of range, a
  * repeated input node), CK_ERR_OUT_OF_MEMORY, CK_ERR_CUDA.
  */
