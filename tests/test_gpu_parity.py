@@ -52,6 +52,12 @@ SMALL = [
     (113, 90, 4000, 9, 300, 1, 2, {}),
     (114, 60, 2500, 4, 512, 1, 1, {}),
     (115, 3000, 200000, 32, 32, 2, 2, dict(hub_deg=150000)),
+    # one source feeding 4,000 edges: a hub row of the backward's transposed rows
+    (116, 500, 6000, 8, 16, 2, 2, dict(src_hub_deg=4000)),
+    # mostly empty rows (E << N): pieces of many rows and few edges
+    (117, 30000, 5000, 16, 5, 2, 2, {}),
+    # self-loops only: every node its own scalar recurrence
+    (118, 300, 900, 4, 8, 3, 3, dict(loops_only=True)),
 ]
 
 

@@ -94,6 +94,30 @@ def test_no_edges_relaxes_geometrically(oracle_lib, M):
                 assert abs(out[t, b, i] - want) < 1e-13
 
 
+@pytest.mark.parametrize("M", [1, 3])
+def test_self_loops_only_is_a_scalar_recursion_per_node(oracle_lib, M):
+    # With every edge a self-loop, W is diagonal (repeated loops add) and each
+    # node follows its own scalar recursion, microstep by microstep:
+    #   h <- (1 - leak_i) h + leak_i tanh(W_ii h + drive_i(t) + bias_i)
+    c = _case(seed=31, N=40, E=120, n_in=5, B=3, T=3, M=M, loops_only=True)
+    N, B, T = c["N"], c["B"], c["T"]
+    assert np.all(c["src"] == c["dst"])
+    out, _, _ = _fwd(oracle_lib, c)
+    wdiag = [0.0] * N
+    for s_, v in zip(c["src"], c["w"]):
+        wdiag[int(s_)] += float(v)
+    slot = {int(node): k for k, node in enumerate(c["input_nodes"])}
+    for b in range(B):
+        for i in range(N):
+            h = float(c["state0"][b, i])
+            lam, beta = float(c["leak"][i]), float(c["bias"][i])
+            for t in range(T):
+                d = float(c["drives"][t, slot[i], b]) if i in slot else 0.0
+                for _ in range(M):
+                    h = (1.0 - lam) * h + lam * math.tanh(wdiag[i] * h + d + beta)
+                assert abs(out[t, b, i] - h) < 1e-13, (b, i, t)
+
+
 @pytest.mark.parametrize("M", [1, 2, 3])
 def test_chain_propagates_one_node_per_microstep(oracle_lib, M):
     # Chain 0 -> 1 -> ... -> N-1, unit weights, leak 1, bias 0, state0 0, drive

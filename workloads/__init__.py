@@ -165,19 +165,23 @@ def make(config_id: int, M: int | None = None, with_dout: bool = True) -> dict:
 
 def small(seed: int, N: int, E: int, n_in: int, B: int, T: int, M: int,
           self_loops: bool = True, dup_frac: float = 0.0, hub_deg: int = 0,
-          w_scale: float | None = None) -> dict:
+          w_scale: float | None = None, src_hub_deg: int = 0, loops_only: bool = False) -> dict:
     """A random small case: uniform edges, optional duplicates and one hub row.
 
     dup_frac of the edges repeat an earlier (src,dst) pair; a hub row, if
-    asked for, takes hub_deg of the E edges into node N-1.
+    asked for, takes hub_deg of the E edges into node N-1; a source hub,
+    src_hub_deg of them out of node 0 (a hub row of the transposed rows);
+    loops_only turns every edge into a self-loop at its source.  The last two
+    draw nothing when unset, so the other cases are unchanged by them.
     """
     rs = _streams(seed)
     perm = rs["perm"].permutation(N).astype(np.int64)
     input_nodes = perm[:n_in].copy()
     rng = rs["src"]
     n_hub = min(hub_deg, E)
-    n_dup = int(round(dup_frac * (E - n_hub)))
-    n_base = E - n_hub - n_dup
+    n_shub = min(src_hub_deg, E - n_hub)
+    n_dup = int(round(dup_frac * (E - n_hub - n_shub)))
+    n_base = E - n_hub - n_shub - n_dup
     src = rng.integers(0, N, size=n_base, dtype=np.int64)
     dst = rng.integers(0, N, size=n_base, dtype=np.int64)
     if not self_loops:
@@ -190,6 +194,11 @@ def small(seed: int, N: int, E: int, n_in: int, B: int, T: int, M: int,
     if n_hub:
         src = np.concatenate([src, rng.integers(0, N, size=n_hub, dtype=np.int64)])
         dst = np.concatenate([dst, np.full(n_hub, N - 1, np.int64)])
+    if n_shub:
+        src = np.concatenate([src, np.zeros(n_shub, np.int64)])
+        dst = np.concatenate([dst, rng.integers(0, N, size=n_shub, dtype=np.int64)])
+    if loops_only:
+        dst = src.copy()
     order = rs["shuffle"].permutation(E)
     src, dst = src[order].astype(np.int64), dst[order].astype(np.int64)
     mean_deg = max(E / N, 1.0)
