@@ -1,5 +1,6 @@
 """The profiling build (libck_prof.so, -DCK_PHASE_PROFILE): its phase counters
-add up per CTA, and its results still match the oracle.
+add up per CTA, and its results still match the oracle; and every build of the
+library (ordinary, bounds-checked, profiling) gives the same bits.
 
 A process loads one variant of the library, so the checks run in a child
 process with CK_LIBRARY_VARIANT=prof.
@@ -51,3 +52,35 @@ def test_profiling_build_counts_and_parity():
     r = subprocess.run([sys.executable, "-c", CHILD], cwd=ROOT, env=env, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0 and "profile ok" in r.stdout, r.stdout[-3000:] + r.stderr[-3000:]
+
+
+RUN = r'''
+import sys
+sys.path.insert(0, "tests")
+import numpy as np
+import workloads
+from gpu_helpers import run_gpu
+c = workloads.small(922, 700, 30000, 10, 32, 3, 2, hub_deg=9000, dup_frac=0.05)
+out, grads = run_gpu(c)
+np.savez(sys.argv[1], out=out, **grads)
+print("saved")
+'''
+
+
+def test_every_build_gives_the_same_bits(tmp_path):
+    """The bounds-checked and profiling builds compute exactly what the
+    ordinary build does (their extra code only checks indices or reads the
+    clock): outputs and all five gradients equal bit for bit."""
+    import numpy as np
+    res = {}
+    for variant in ("", "bounds", "prof"):
+        env = dict(os.environ)
+        env["CK_LIBRARY_VARIANT"] = variant
+        path = str(tmp_path / f"run_{variant or 'plain'}.npz")
+        r = subprocess.run([sys.executable, "-c", RUN, path], cwd=ROOT, env=env, capture_output=True,
+                           text=True, timeout=600)
+        assert r.returncode == 0 and "saved" in r.stdout, (variant, r.stdout[-2000:] + r.stderr[-2000:])
+        res[variant] = np.load(path)
+    for variant in ("bounds", "prof"):
+        for k in res[""].files:
+            np.testing.assert_array_equal(res[variant][k], res[""][k], err_msg=f"{variant} {k}")
