@@ -58,6 +58,8 @@ SMALL = [
     (117, 30000, 5000, 16, 5, 2, 2, {}),
     # self-loops only: every node its own scalar recurrence
     (118, 300, 900, 4, 8, 3, 3, dict(loops_only=True)),
+    # no input nodes: drives [T, 0, B], and d_drives empty
+    (119, 50, 400, 0, 4, 2, 2, {}),
 ]
 
 

@@ -18,6 +18,7 @@ CASES = [
     (404, 300, 20000, 10, 20, 2, 1, dict(hub_deg=12000)),
     (405, 200, 8000, 10, 64, 2, 3, {}),
     (406, 90, 4000, 9, 300, 2, 2, {}),
+    (407, 60, 900, 0, 8, 3, 2, {}),  # no input nodes: drives and their gradient are empty
 ]
 
 
