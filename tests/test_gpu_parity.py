@@ -73,6 +73,21 @@ def test_small_cases(seed, N, E, n_in, B, T, M, extra, kernels):
     assert_parity(out, g, ref_out, ref, f"seed {seed}")
 
 
+def test_side_stream_gives_the_same_bits():
+    """Every call enqueues on the caller's stream: the same case built and run
+    inside a side stream (graph build, workspaces, launches and copies) gives
+    the default stream's outputs and gradients bit for bit."""
+    c = workloads.small(120, 700, 30000, 10, 32, 3, 2, hub_deg=9000)
+    base_out, base = run_gpu(c)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        out, g = run_gpu(c)
+    side.synchronize()
+    np.testing.assert_array_equal(out, base_out)
+    for k in GRAD_KEYS:
+        np.testing.assert_array_equal(g[k], base[k], err_msg=k)
+
+
 @pytest.mark.parametrize("kernels", list(KERNELS))
 def test_config0_tiny(kernels):
     _kernels(kernels)
