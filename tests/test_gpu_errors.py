@@ -46,26 +46,44 @@ def test_workspace_and_shape_errors():
     assert_parity(out2, grads, ref_out, ref, "after errors")
 
 
-def test_barrier_timeout_is_reported_and_context_survives():
+@pytest.mark.parametrize("streamed", [False, True], ids=["graph_in_smem", "graph_streamed"])
+def test_barrier_timeout_is_reported_and_context_survives(streamed):
     """Barriers are told to wait for one more CTA than exists; every wait runs
-    out after 2 ms, the kernel stops, and the status word says so."""
+    out after 2 ms, the kernel stops, and the status word says so -- in the
+    forward and in the backward, with the graph slice in shared memory and
+    streamed (where the ring's copies are in flight when the wait gives up)."""
     import sparse_graph_recurrent_gb300 as pkg
     from sparse_graph_recurrent_gb300 import _ck
     c = workloads.small(402, 60, 600, 4, 8, 2, 2)
     g = make_graph(c)
     t = _io(c)
+    B, T, M = c["B"], c["T"], c["M"]
+    _ck.ck_set_option(_ck.OPT_GRAPH_IN_SMEM, 0 if streamed else 1)
     _ck.ck_set_option(_ck.OPT_BARRIER_TIMEOUT_NS, 2_000_000)
-    _ck.ck_set_option(_ck.OPT_TEST_BARRIER_EXTRA, 1)
     try:
+        _ck.ck_set_option(_ck.OPT_TEST_BARRIER_EXTRA, 1)
         out, saved, scratch = pkg.forward(g, t["w"], t["leak"], t["bias"], t["drives"],
-                                          t["state0"], c["M"])
+                                          t["state0"], M)
+        with pytest.raises(_ck.CKError) as e:
+            _ck.ck_query_status(scratch)
+        assert e.value.name == "CK_ERR_TIMEOUT"
+        # a complete forward, then a backward whose barriers run out
+        _ck.ck_set_option(_ck.OPT_TEST_BARRIER_EXTRA, 0)
+        out, saved, scratch = pkg.forward(g, t["w"], t["leak"], t["bias"], t["drives"],
+                                          t["state0"], M)
+        _ck.ck_query_status(scratch)
+        _ck.ck_set_option(_ck.OPT_TEST_BARRIER_EXTRA, 1)
+        pkg.backward(g, t["w"], t["leak"], B, T, M, saved, t["dout"], scratch)
         with pytest.raises(_ck.CKError) as e:
             _ck.ck_query_status(scratch)
         assert e.value.name == "CK_ERR_TIMEOUT"
     finally:
         _ck.ck_set_option(_ck.OPT_TEST_BARRIER_EXTRA, 0)
         _ck.ck_set_option(_ck.OPT_BARRIER_TIMEOUT_NS, 4_000_000_000)
-    out, grads = run_gpu(c, graph=g)
+    try:
+        out, grads = run_gpu(c, graph=g)
+    finally:
+        _ck.ck_set_option(_ck.OPT_GRAPH_IN_SMEM, 1)
     ref_out, ref = oracle.run_case(c)
     assert_parity(out, grads, ref_out, ref, "after timeout")
 
