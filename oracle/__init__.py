@@ -200,3 +200,20 @@ def graph_layout(N: int, src, dst, input_nodes):
     slot[_i64(input_nodes)] = np.arange(len(input_nodes), dtype=np.int32)
     return dict(row_ptr=row_ptr, col=col, perm=perm, rowT_ptr=rowT_ptr, colT=colT,
                 permT=permT, slot=slot)
+
+
+def adam_update(param, grad, m, v, step: int, lr: float, beta1: float, beta2: float, eps: float):
+    """One Adam step in fp64 (Kingma and Ba, "Adam: A Method for Stochastic
+    Optimization", Algorithm 1), the optional optimizer of a captured training
+    step (TrainKernel page: the captured step holds the parameter update).
+    `step` is t >= 1.  Returns (param, m, v) after the step:
+        m <- beta1 m + (1 - beta1) g;   v <- beta2 v + (1 - beta2) g^2
+        param <- param - lr (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)
+    """
+    p = np.asarray(param, np.float64)
+    g = np.asarray(grad, np.float64)
+    m = beta1 * np.asarray(m, np.float64) + (1.0 - beta1) * g
+    v = beta2 * np.asarray(v, np.float64) + (1.0 - beta2) * g * g
+    mhat = m / (1.0 - beta1 ** step)
+    vhat = v / (1.0 - beta2 ** step)
+    return p - lr * mhat / (np.sqrt(vhat) + eps), m, v

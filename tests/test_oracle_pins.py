@@ -441,3 +441,34 @@ def test_step_columns_matches_single_thread(oracle_lib, threads):
     # a second run with the same thread count repeats every bit
     out_q, g_q = oracle_lib.step_columns(c, threads)
     assert all(np.array_equal(g_q[k], g_p[k]) for k in g_p)
+
+
+# --------------------------------------------------------------------------
+# the optional Adam update of a captured training step
+# --------------------------------------------------------------------------
+
+def test_adam_first_step_closed_form():
+    # from m = v = 0 the bias corrections make m_hat = g and v_hat = g^2, so
+    # the first step moves every parameter by lr g / (|g| + eps)
+    import oracle
+    rng = np.random.default_rng(5)
+    p, g = rng.normal(size=50), rng.normal(size=50)
+    lr, eps = 0.01, 1e-8
+    p1, m1, v1 = oracle.adam_update(p, g, np.zeros(50), np.zeros(50), 1, lr, 0.9, 0.999, eps)
+    np.testing.assert_allclose(p1, p - lr * g / (np.abs(g) + eps), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(m1, 0.1 * g, rtol=1e-15)
+    np.testing.assert_allclose(v1, 0.001 * g * g, rtol=1e-12)
+
+
+def test_adam_constant_gradient_closed_form():
+    # with the same gradient every step, m_t = (1 - beta1^t) g and
+    # v_t = (1 - beta2^t) g^2 exactly, so every step moves by lr g / (|g| + eps)
+    import oracle
+    rng = np.random.default_rng(6)
+    p0, g = rng.normal(size=20), rng.normal(size=20)
+    p, m, v = p0.copy(), np.zeros(20), np.zeros(20)
+    lr, eps, b1, b2 = 0.003, 1e-6, 0.8, 0.95
+    for t in range(1, 26):
+        p, m, v = oracle.adam_update(p, g, m, v, t, lr, b1, b2, eps)
+        np.testing.assert_allclose(m, (1 - b1 ** t) * g, rtol=1e-12)
+        np.testing.assert_allclose(p, p0 - t * lr * g / (np.abs(g) + eps), rtol=0, atol=1e-12)
