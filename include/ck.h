@@ -298,6 +298,25 @@ ck_status ck_backward_recompute(const ck_graph *g, const float *edge_values, con
 ck_status ck_sgd_update(float *param, const float *grad, int64_t n, float lr, void *stream);
 
 /*
+ * ck_adam_update -- one Adam step (Kingma and Ba, "Adam: A Method for
+ * Stochastic Optimization", Algorithm 1) over n floats, the optional
+ * optimizer of a captured training step:
+ *     m <- beta1 m + (1 - beta1) grad;  v <- beta2 v + (1 - beta2) grad^2
+ *     param <- param - lr (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)
+ * with t = *step, a (device) int64 the caller keeps (t >= 1; advance it with
+ * ck_step_advance before each step, so that a captured graph advances its own
+ * count on every replay).  param, m, v: (device) float[n], updated in place;
+ * grad: (device) float[n]; m and v start at zero.  Asynchronous on `stream`.
+ * Errors: CK_ERR_INVALID_ARG (n < 0, betas outside [0, 1), eps <= 0, lr not a
+ * number, NULL pointer), CK_ERR_CUDA.
+ *
+ * ck_step_advance -- *step += 1 on the device (one thread), on `stream`.
+ */
+ck_status ck_adam_update(float *param, const float *grad, float *m, float *v, int64_t n, float lr,
+                         float beta1, float beta2, float eps, const int64_t *step, void *stream);
+ck_status ck_step_advance(int64_t *step, void *stream);
+
+/*
  * ck_forward_static_scratch -- ck_forward without a scratch buffer: the
  * temporary workspace comes from a 32 MiB array of device memory compiled into
  * the library.  The pages have no counterpart for this call; it exists for

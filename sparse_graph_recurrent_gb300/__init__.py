@@ -150,9 +150,11 @@ def backward_recompute(graph: SparseGraph, edge_values, leak, bias, drives, B: i
 
 class TrainStep:
     """One training step -- forward, backward of L = sum(out * d_out), and an
-    SGD update of edge_values, leak and bias -- captured once as a CUDA graph
-    and replayed (TrainKernel page: a captured step holds the forward, the
-    gradients and the SGD update, with no per-operator host launches).
+    update of edge_values, leak and bias (SGD, or Adam with optimizer="adam") --
+    captured once as a CUDA graph and replayed (TrainKernel page: a captured
+    step holds the forward, the gradients and the parameter update, with no
+    per-operator host launches).  Adam's moments and step count live on the
+    device, and each replay advances the count.
 
     The parameters are updated in place; drives, state0 and d_out are read from
     the tensors given here, so copy new inputs into them before a replay.
@@ -160,8 +162,12 @@ class TrainStep:
     (overwritten by the next replay)."""
 
     def __init__(self, graph: SparseGraph, edge_values, leak, bias, drives, state0, d_out,
-                 microsteps: int, lr: float):
+                 microsteps: int, lr: float, optimizer: str = "sgd", betas=(0.9, 0.999),
+                 eps: float = 1e-8):
+        if optimizer not in ("sgd", "adam"):
+            raise ValueError("optimizer is 'sgd' or 'adam'")
         self.graph, self.M = graph, microsteps
+        self.optimizer, self.betas, self.eps = optimizer, tuple(betas), eps
         self.w, self.leak, self.bias = edge_values, leak, bias
         self.drives, self.state0, self.d_out = drives, state0, d_out
         dev = state0.device
@@ -176,13 +182,21 @@ class TrainStep:
         self.grads = (torch.empty(E, device=dev), torch.empty(N, device=dev),
                       torch.empty(N, device=dev), torch.empty((T, n_in, B), device=dev),
                       torch.empty((B, N), device=dev))
+        params = (edge_values, leak, bias)
+        self.moments = [(torch.zeros_like(p), torch.zeros_like(p)) for p in params]
+        self.step_count = torch.zeros(1, dtype=torch.int64, device=dev)
         # one uncaptured pass with lr = 0 sets the kernels up and leaves the
-        # parameters as they are
+        # parameters as they are (Adam's moments and count are reset after it)
         side = torch.cuda.Stream(device=dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side):
             self._step(0.0)
         torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        for m, v in self.moments:
+            m.zero_()
+            v.zero_()
+        self.step_count.zero_()
         torch.cuda.synchronize(dev)
         self.cuda_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.cuda_graph):
@@ -195,9 +209,15 @@ class TrainStep:
                        self.out, self.saved, self.scratch)
         _ck.ck_backward(g.handle, self.w, self.leak, self.B, self.T, M, self.saved, self.d_out,
                         dw, dl, db, dd, dh, self.scratch)
-        _ck.ck_sgd_update(self.w, dw, lr)
-        _ck.ck_sgd_update(self.leak, dl, lr)
-        _ck.ck_sgd_update(self.bias, db, lr)
+        if self.optimizer == "sgd":
+            _ck.ck_sgd_update(self.w, dw, lr)
+            _ck.ck_sgd_update(self.leak, dl, lr)
+            _ck.ck_sgd_update(self.bias, db, lr)
+        else:
+            _ck.ck_step_advance(self.step_count)
+            b1, b2 = self.betas
+            for p, gr, (m, v) in zip((self.w, self.leak, self.bias), (dw, dl, db), self.moments):
+                _ck.ck_adam_update(p, gr, m, v, self.step_count, lr, b1, b2, self.eps)
 
     def __call__(self):
         self.cuda_graph.replay()

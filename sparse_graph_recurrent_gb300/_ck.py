@@ -74,6 +74,9 @@ def load() -> ctypes.CDLL:
         "ck_backward": [p, p, p, i64, i64, i64, p, sz, p, p, p, p, p, p, p, sz, p],
         "ck_workspace_size_recompute": [p, i64, i64, i64, psz, psz],
         "ck_sgd_update": [p, p, i64, ctypes.c_float, p],
+        "ck_adam_update": [p, p, p, p, i64, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                           ctypes.c_float, p, p],
+        "ck_step_advance": [p, p],
         "ck_forward_checkpointed": [p, p, p, p, p, p, i64, i64, i64, p, p, sz, p, sz, p],
         "ck_backward_recompute": [p, p, p, p, p, i64, i64, i64, p, sz, p, p, p, p, p, p, p, sz, p],
         "ck_query_status": [p, p],
@@ -223,6 +226,24 @@ def ck_sgd_update(param, grad, lr: float, stream=None):
         raise ValueError("param and grad differ in shape")
     _check(load().ck_sgd_update(_ptr(param), _ptr(grad), param.numel(), float(lr),
                                 _stream(stream)))
+
+
+def ck_adam_update(param, grad, m, v, step, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+                   eps: float = 1e-8, stream=None):
+    """Adam at the step number held by the device int64 tensor `step`."""
+    for t, name in ((param, "param"), (grad, "grad"), (m, "m"), (v, "v")):
+        _need(t, torch.float32, name)
+        if t.shape != param.shape:
+            raise ValueError(f"{name} differs in shape from param")
+    _need(step, torch.int64, "step")
+    _check(load().ck_adam_update(_ptr(param), _ptr(grad), _ptr(m), _ptr(v), param.numel(),
+                                 float(lr), float(beta1), float(beta2), float(eps), _ptr(step),
+                                 _stream(stream)))
+
+
+def ck_step_advance(step, stream=None):
+    _need(step, torch.int64, "step")
+    _check(load().ck_step_advance(_ptr(step), _stream(stream)))
 
 
 def ck_workspace_size_recompute(handle, B: int, T: int, microsteps: int):

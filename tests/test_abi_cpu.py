@@ -145,3 +145,20 @@ def test_barrier_probe_refuses_bad_arguments_on_the_host(lib):
     assert lib.ck_probe_grid_barrier(9, 8, 1, 10, 0, None, None, None, None) == 1
     assert lib.ck_probe_grid_barrier(0, 8, 4, 10, 0, None, None, None, None) == 1
     assert b"scheme" in lib.ck_last_error_message()
+
+
+def test_adam_refuses_bad_arguments_on_the_host(lib):
+    """Argument checks of the Adam update come before any CUDA call."""
+    f = lib.ck_adam_update
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] + [ctypes.c_float] * 4 + [ctypes.c_void_p] * 2
+    one = (ctypes.c_int64 * 1)(1)
+    step = ctypes.cast(one, ctypes.c_void_p)
+    assert f(None, None, None, None, -1, 0.01, 0.9, 0.999, 1e-8, step, None) == 1   # n < 0
+    assert f(None, None, None, None, 4, 0.01, 1.0, 0.999, 1e-8, step, None) == 1    # beta1 = 1
+    assert f(None, None, None, None, 4, 0.01, 0.9, -0.1, 1e-8, step, None) == 1     # beta2 < 0
+    assert f(None, None, None, None, 4, 0.01, 0.9, 0.999, 0.0, step, None) == 1     # eps = 0
+    assert f(None, None, None, None, 4, float("nan"), 0.9, 0.999, 1e-8, step, None) == 1
+    assert f(None, None, None, None, 4, 0.01, 0.9, 0.999, 1e-8, None, None) == 1    # no step
+    assert f(None, None, None, None, 4, 0.01, 0.9, 0.999, 1e-8, step, None) == 1    # NULL arrays
+    lib.ck_step_advance.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.ck_step_advance(None, None) == 1
