@@ -358,12 +358,13 @@ __device__ __forceinline__ void cp_async_wait_but_last() { asm volatile("cp.asyn
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Edges per gather batch of part A: more loads in flight per lane measured
-// slower (the L2 path congests); for NC = 2 three per batch measured fastest in
-// the forward and four in the backward (whose dot-product butterfly wants a
-// power of two).
+// Edges per gather batch of part A: four for NC = 2 in both directions (the
+// forward, gathering through L2 only, measured fastest at four: three and five
+// each lost on some workload, two and six on all; the backward's dot-product
+// butterfly wants a power of two), two in the four-chunk backward, where more
+// rows in flight per lane measured slower.
 __host__ __device__ constexpr int edge_batch(bool bwd, int nc) {
-    return bwd ? (nc == 2 ? 4 : 2) : (nc == 2 ? 3 : 4);
+    return bwd && nc != 2 ? 2 : 4;
 }
 
 // The helpers below spread their work over nt threads, this one being number
