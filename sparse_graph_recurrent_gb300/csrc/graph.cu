@@ -544,13 +544,14 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
     }
     // Pieces, one per CTA (kCtasPerSm per SM), for each finish pass size.  The row weight is the
     // one (of a few) whose slowest piece is estimated fastest: part A at about
-    // 1.5 ns per edge per 32 batch columns, a finish pass at about 0.8 us
+    // 1.5 ns per edge per 32 batch columns (1.2 ns in the forward, whose gathers
+    // go through L2 alone in batches of four), a finish pass at about 0.8 us
     // (measured on the FlyGPT-shaped graph); ties go to the smaller weight.
     {
         const int P = num_pieces(g);
         std::vector<int> rp(N + 1);
         const int *rps[2] = {g->row_ptr, g->rowT_ptr};
-        static const int weights[] = {1, 2, 3, 4, 6, 8, 12, 16};
+        static const int weights[] = {1, 2, 3, 4, 6, 8, 12, 16, 20, 24};
         for (int d = 0; d < 2; ++d) {
             CK_TRY(cudaMemcpyAsync(rp.data(), rps[d], sizeof(int) * (N + 1), cudaMemcpyDeviceToHost, s),
                    "copy row pointers");
@@ -558,7 +559,7 @@ ck_status build_graph(ck_graph *g, const int64_t *src, const int64_t *dst,
             std::vector<Cut> cuts;
             for (int wt : weights) cuts.push_back(cut_pieces(rp, (int)N, (int)E, P, wt));
             for (int v = 0; v < 3; ++v) {
-                const double edge_us = 1.5e-3 * (v == 0 ? 1 : v == 1 ? 2 : 4);
+                const double edge_us = (d == 0 ? 1.2e-3 : 1.5e-3) * (v == 0 ? 1 : v == 1 ? 2 : 4);
                 int best = 0;
                 double best_cost = 0.0;
                 for (int i = 0; i < (int)cuts.size(); ++i) {
